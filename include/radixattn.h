@@ -1,0 +1,265 @@
+/* radixattn.h: C ABI of the prefix-shared radix-tree KV cache and its kernels.
+ *
+ * Two halves.
+ *
+ *  Host (radix tree, reference counts, LRU, slot allocator, scheduling order):
+ *  rc_create, rc_destroy, rc_match_prefix, rc_insert, rc_release, rc_evict,
+ *  rc_alloc, rc_free, sched_order, rc_stats, rc_dump.  Plain C++ on the
+ *  caller's thread; not thread-safe per cache object.
+ *
+ *  Device (hand-written CUDA for sm_103a): kv_store, attn_decode, attn_extend,
+ *  their workspace queries, and rc_sync.  All device memory is the caller's:
+ *  the library never allocates it.  Device calls enqueue work on `stream` and
+ *  return; an error detected inside a kernel (a slot index outside the pool)
+ *  is OR-ed into the caller's device error word and read back by rc_sync.
+ *
+ * The pages this follows:
+ *  [N49] "RadixAttention, eviction and cache churn" (inference-notes note 49):
+ *        section 2 (edges hold token runs and their KV; lookup walks one token
+ *        at a time; the edge splits at the first differing token; finished
+ *        requests, outputs included, stay cached), section 4 (shared pool;
+ *        reference-count pinning; unpinned least-recently-used leaves evicted
+ *        first; a parent whose children are gone becomes a leaf), section 5
+ *        (longest cached prefix first vs arrival order).
+ *  [SG]  unite.ai article on SGLang: the RadixAttention paragraph (an LRU
+ *        cache of KV in a radix tree for match, insert and evict) and the
+ *        nine-step walkthrough of the tree.
+ *  [LMI] SageMaker LMI / Falcon article, "prefill and decode phases": prefill
+ *        runs the whole prompt at once; decode produces one token per step
+ *        from the cached K/V.
+ *  [DS]  SGLang engineering article, section 1 (MLA): a single KV head whose
+ *        decode kernel serves several query heads per block to cut KV traffic.
+ *
+ * Conventions.  Token ids and slot ids are int32.  A slot is one row of the
+ * KV pool: for grouped-query attention the pool holds K and V as
+ * [n_slots][kv_heads][head_dim] bf16 each; for the latent (MLA) layout one
+ * array [n_slots][head_dim_k] bf16 whose first head_dim_v columns are V.
+ * Every status is an rc_status; nothing aborts and no C++ exception crosses
+ * this boundary.
+ */
+#ifndef RADIXATTN_H
+#define RADIXATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t rc_status;
+#define RC_OK               0
+#define RC_ERR_ARG         -1  /* bad argument: null pointer, negative size, id out of range */
+#define RC_ERR_NOMEM       -2  /* not enough free slots (rc_alloc never evicts by itself) */
+#define RC_ERR_STATE       -3  /* unknown or unpinned node, slot not owned by the caller */
+#define RC_ERR_CUDA        -4  /* a CUDA runtime call failed */
+#define RC_ERR_TIMEOUT     -5  /* a bounded device wait gave up */
+#define RC_ERR_DEVICE      -6  /* a kernel found a slot index outside the pool */
+#define RC_ERR_UNSUPPORTED -7  /* head layout this build has no kernel for */
+
+/* Scheduling policies of sched_order. */
+#define RC_FCFS 0  /* arrival order */
+#define RC_LPM  1  /* longest cached prefix first, ties by arrival [N49 s.5] */
+
+typedef struct rc_cache rc_cache;   /* opaque host object */
+typedef int64_t rc_node;            /* node id: 0 is the root; ids count node creations */
+typedef struct CUstream_st* rc_stream_t;  /* a cudaStream_t; NULL = legacy default stream */
+
+/* ------------------------------------------------------------------ host */
+
+/* Create a cache over a pool of `pool_slots` slots (ids 0..pool_slots-1), all
+ * free.  `pool_slots` in [0, 2^31-1].  *out receives the handle.
+ * Errors: RC_ERR_ARG (bad size or null out), RC_ERR_NOMEM (host allocation). */
+rc_status rc_create(int64_t pool_slots, rc_cache** out);
+void rc_destroy(rc_cache* cache);
+
+/* Longest cached prefix of tok[0..n) [N49 s.2: lookup walks down one token at a
+ * time until a token differs].  A match that ends inside an edge splits that
+ * edge so the prefix ends on a node; the new upper node takes the lower node's
+ * reference count.  Advances the LRU clock by one and stamps every node on the
+ * path root..end.  With pin != 0 every node on that path gets one more
+ * reference [N49 s.4]; undo with rc_release(*out_node).
+ * out_slots: NULL or room for n slot ids; receives the matched prefix's slots.
+ * *matched: matched length.  *out_node: end node (root when nothing matched).
+ * Errors: RC_ERR_ARG (n < 0, null tok with n > 0, null matched/out_node). */
+rc_status rc_match_prefix(rc_cache* cache, const int32_t* tok, int64_t n, int pin,
+                          int64_t* matched, int32_t* out_slots, rc_node* out_node);
+
+/* Insert tok[0..n) whose K/V sit in slots[0..n) [N49 s.2: a finished request's
+ * path stays cached; SG walkthrough: a new turn becomes a new node].  At most
+ * one node is added (the unmatched tail); an edge is split where the new
+ * sequence leaves it or ends inside it.  Ownership: the slots of the new tail
+ * must be held by the caller (from rc_alloc) and pass to the tree; for the
+ * already-present part, a caller slot equal to the tree's slot at that
+ * position is left alone and any other caller slot goes back to the free
+ * pool (a duplicate).  Validation happens before any change: on error nothing
+ * changed.  Advances the LRU clock by one and stamps the path; pins the path
+ * root..end when pin != 0.
+ * *already_present: length of the part that was already cached.
+ * out_slots: NULL or room for n; receives the tree's slots for every position
+ * (what the caller's slot table should hold from now on).
+ * Errors: RC_ERR_ARG (bad sizes/pointers, slot id out of range), RC_ERR_STATE
+ * (a slot that should be the caller's is free or in the tree, or repeats). */
+rc_status rc_insert(rc_cache* cache, const int32_t* tok, const int32_t* slots, int64_t n,
+                    int pin, int64_t* already_present, rc_node* out_node, int32_t* out_slots);
+
+/* Drop one reference from every node on the path root..node [N49 s.4].
+ * Errors: RC_ERR_STATE (unknown or evicted node, or node not pinned). */
+rc_status rc_release(rc_cache* cache, rc_node node);
+
+/* Evict unpinned leaves, least recently used first (ties: lower node id),
+ * until at least n_tokens slots are freed or no candidate is left [N49 s.4;
+ * SG walkthrough steps 5, 8, 9].  Whole leaves only, never the root; a parent
+ * left without children and without pins becomes a candidate in the same call.
+ * *freed: slots freed (may be < n_tokens).  log: NULL or room for log_cap node
+ * ids, in eviction order; *n_evicted: nodes evicted (even beyond log_cap).
+ * Errors: RC_ERR_ARG (n_tokens < 0, null freed or n_evicted). */
+rc_status rc_evict(rc_cache* cache, int64_t n_tokens, int64_t* freed,
+                   int64_t* log, int64_t log_cap, int64_t* n_evicted);
+
+/* Take the n smallest free slot ids, ascending, into out[0..n) [N49 s.4: the
+ * cache and the running requests share one pool].  Never evicts.
+ * Errors: RC_ERR_ARG, RC_ERR_NOMEM (fewer than n free; nothing taken). */
+rc_status rc_alloc(rc_cache* cache, int64_t n, int32_t* out);
+
+/* Give caller-held slots back to the pool.  Errors: RC_ERR_ARG (id out of
+ * range), RC_ERR_STATE (slot not held by the caller, or repeated). */
+rc_status rc_free(rc_cache* cache, const int32_t* slots, int64_t n);
+
+/* Serving order of n pending prompts [N49 s.5].  RC_FCFS: 0..n-1.
+ * RC_LPM: by the length each prompt would match now, longest first, ties by
+ * index; the look-ahead changes nothing (no split, stamp or pin).
+ * prompts: n host pointers; lens: n lengths.  out_order: room for n.
+ * Errors: RC_ERR_ARG. */
+rc_status sched_order(rc_cache* cache, int policy, const int32_t* const* prompts,
+                      const int64_t* lens, int32_t n, int32_t* out_order);
+
+typedef struct rc_stats_t {
+    int64_t pool_slots, free_slots, caller_slots, tree_tokens, nodes;
+    int64_t match_calls, match_tokens, match_hits, match_hit_tokens;
+    int64_t insert_calls, insert_new_tokens, insert_dup_freed;
+    int64_t evicted_nodes, evicted_tokens;
+    int64_t pins;    /* references held on the root = pinned paths */
+    int64_t clock;   /* LRU clock */
+} rc_stats_t;
+rc_status rc_stats(rc_cache* cache, rc_stats_t* out);
+
+/* Text dump of the tree for tests: one line per node, depth first, children
+ * in ascending first-token order:
+ *   "<id> <parent id or -1> <ref> <last access> <ntok>: <tokens> | <slots>\n"
+ * Writes at most cap-1 bytes plus a NUL; *needed = full length (no NUL). */
+rc_status rc_dump(rc_cache* cache, char* buf, int64_t cap, int64_t* needed);
+
+/* ---------------------------------------------------------------- device */
+
+/* KV pool in HBM (caller-owned).  GQA: k and v are [n_slots][kv_heads][head_dim]
+ * bf16, row-major, 16-byte aligned.  Latent (mla != 0): kv_heads == 1, k is
+ * [n_slots][head_dim_k] and its first head_dim_v columns are V; v is NULL.
+ * err: device int32 that kernels OR RC error bits into (may be NULL). */
+typedef struct rc_pool_desc {
+    void* k;
+    void* v;
+    int64_t n_slots;
+    int32_t kv_heads;
+    int32_t head_dim_k;
+    int32_t head_dim_v;
+    int32_t mla;
+    int32_t* err;
+} rc_pool_desc;
+
+typedef struct rc_attn_desc {
+    rc_pool_desc pool;
+    int32_t q_heads;   /* multiple of kv_heads; query head h reads kv head h / (q_heads/kv_heads) */
+    float sm_scale;    /* scale of q.k inside the softmax */
+} rc_attn_desc;
+
+/* Per-request slot tables on the device (caller-owned).  The keys of request b
+ * are, in position order, slots[start[b] .. start[b] + len[b]).  Rows may have
+ * room to grow (kv_store appends).  max_len: a host-side bound on every len[b]
+ * (sizes the grid; longer rows are an error). */
+typedef struct rc_kv_table {
+    const int32_t* slots;
+    const int32_t* start;
+    const int32_t* len;
+    int32_t max_len;
+} rc_kv_table;
+
+/* Scatter n new tokens' K/V rows into the pool [N49 s.2: each edge keeps the
+ * KV of its tokens].  k_new: [n][kv_heads][head_dim_k] bf16; v_new:
+ * [n][kv_heads][head_dim_v] (NULL for the latent layout).  Row i goes to slot
+ * slots[i].  If table and table_pos are both non-NULL, also
+ * table[table_pos[i]] = slots[i] (appends to the slot tables).
+ * A slot outside [0, n_slots) is skipped and flags RC_ERR_DEVICE in pool->err.
+ * Errors (host): RC_ERR_ARG, RC_ERR_UNSUPPORTED (row bytes not a multiple of 16),
+ * RC_ERR_CUDA (launch). */
+rc_status kv_store(const rc_pool_desc* pool, const int32_t* slots, const void* k_new,
+                   const void* v_new, int32_t n, int32_t* table, const int32_t* table_pos,
+                   rc_stream_t stream);
+
+/* Shared-prefix segments for cascade decode (all device arrays caller-owned;
+ * the tree gives them: a node pinned by several running requests is one
+ * segment) [N49 s.1: prompts share in layers, so the shared parts form a tree].
+ * Segment s covers keys seg_slots[seg_indptr[s] .. seg_indptr[s+1]) and is
+ * read once for every batch row listed in seg_rows[seg_row_indptr[s] ..
+ * seg_row_indptr[s+1]).  The inverse map lists, for batch row b, the
+ * positions p in seg_rows with seg_rows[p] == b:
+ * req_seg_pos[req_seg_indptr[b] .. req_seg_indptr[b+1]).  With a cascade, the
+ * kv table of attn_decode holds only each row's remaining (private) keys; the
+ * result equals flat decode over segments + private keys.  max_seg_rows is a
+ * host bound on rows per segment; total_seg_rows = seg_row_indptr[n_seg]. */
+typedef struct rc_cascade {
+    int32_t n_seg;
+    const int32_t* seg_slots;
+    const int32_t* seg_indptr;
+    const int32_t* seg_row_indptr;
+    const int32_t* seg_rows;
+    const int32_t* req_seg_indptr;
+    const int32_t* req_seg_pos;
+    int32_t max_seg_rows;
+    int32_t total_seg_rows;
+} rc_cascade;
+
+/* Workspace bytes attn_decode needs for this batch (split partials). */
+rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_len,
+                                const rc_cascade* cascade, size_t* bytes);
+
+/* One decode step for `batch` requests [LMI decode phase; N49 s.2]: row b's
+ * single query q[b] ([batch][q_heads][head_dim_k] bf16) sits at the last
+ * position of its context and attends to all of it:
+ *   out[b][h] = sum_j softmax_j(sm_scale * q[b][h].K[j][g(h)]) V[j][g(h)]
+ * over the cascade segments of row b (if any) and then its table row.
+ * out: [batch][q_heads][head_dim_v] bf16.  lse: NULL or [batch][q_heads] fp32,
+ * natural log of the softmax denominator.  ws: attn_decode_workspace bytes.
+ * Errors: RC_ERR_ARG, RC_ERR_UNSUPPORTED (head layout), RC_ERR_CUDA. */
+rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv,
+                      int32_t batch, const rc_cascade* cascade, void* out, float* lse,
+                      void* ws, size_t ws_bytes, rc_stream_t stream);
+
+/* Workspace bytes attn_extend needs (0 today; kept for split variants). */
+rc_status attn_extend_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_q,
+                                int32_t max_len, size_t* bytes);
+
+/* Prefill of new tokens over a cached prefix [N49 s.2: only the new part is
+ * computed; LMI prefill phase].  Row b has n_b = qo_indptr[b+1]-qo_indptr[b]
+ * new tokens, the last n_b positions of its table row (their K/V already
+ * stored).  New token i of row b (position p = len[b]-n_b+i) attends to keys
+ * 0..p causally.  q and out: [sum n_b][q_heads][head_dim] bf16.
+ * max_q: host bound on n_b.  lse: NULL or [sum n_b][q_heads] fp32.
+ * Errors: RC_ERR_ARG, RC_ERR_UNSUPPORTED, RC_ERR_CUDA. */
+rc_status attn_extend(const rc_attn_desc* desc, const void* q, const int32_t* qo_indptr,
+                      const rc_kv_table* kv, int32_t batch, int32_t max_q, void* out,
+                      float* lse, void* ws, size_t ws_bytes, rc_stream_t stream);
+
+/* Wait for `stream`, then read and clear the device error word `err` (may be
+ * NULL).  Returns RC_ERR_DEVICE / RC_ERR_TIMEOUT if a kernel flagged one,
+ * RC_ERR_CUDA if the stream reported an error, RC_OK otherwise. */
+rc_status rc_sync(rc_stream_t stream, int32_t* err);
+
+/* Static string for a status. */
+const char* rc_strerror(rc_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RADIXATTN_H */

@@ -1,0 +1,347 @@
+"""Prefix-shared radix-tree KV cache with GB300 (sm_103a) attention kernels.
+
+This module is the thin Python binding of the C-ABI library declared in
+``include/radixattn.h`` (built in-tree as ``_build/libradixattn.so``).  It only
+marshals arguments: every step of the path runs in the library, the host tree
+in C++ and the data path in hand-written CUDA kernels.  There is no fallback:
+if the library is missing, loading it raises.
+
+Function names follow the header: ``rc_create``, ``rc_match_prefix``,
+``rc_insert``, ``rc_release``, ``rc_evict``, ``rc_alloc``, ``rc_free``,
+``sched_order``, ``rc_stats``, ``rc_dump``, ``kv_store``, ``attn_decode``,
+``attn_extend``, ``rc_sync``.  ``RadixCache`` wraps a cache handle with the
+host calls as methods.  Device calls take torch CUDA tensors (PyTorch is used
+for device memory and streams only).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+
+from . import _compile as _build
+
+RC_OK, RC_ERR_ARG, RC_ERR_NOMEM, RC_ERR_STATE = 0, -1, -2, -3
+RC_ERR_CUDA, RC_ERR_TIMEOUT, RC_ERR_DEVICE, RC_ERR_UNSUPPORTED = -4, -5, -6, -7
+RC_FCFS, RC_LPM = 0, 1
+
+I32, I64, VP = C.c_int32, C.c_int64, C.c_void_p
+P = C.POINTER
+
+
+class rc_pool_desc(C.Structure):
+    _fields_ = [("k", VP), ("v", VP), ("n_slots", I64), ("kv_heads", I32), ("head_dim_k", I32),
+                ("head_dim_v", I32), ("mla", I32), ("err", VP)]
+
+
+class rc_attn_desc(C.Structure):
+    _fields_ = [("pool", rc_pool_desc), ("q_heads", I32), ("sm_scale", C.c_float)]
+
+
+class rc_kv_table(C.Structure):
+    _fields_ = [("slots", VP), ("start", VP), ("len", VP), ("max_len", I32)]
+
+
+class rc_cascade(C.Structure):
+    _fields_ = [("n_seg", I32), ("seg_slots", VP), ("seg_indptr", VP), ("seg_row_indptr", VP),
+                ("seg_rows", VP), ("req_seg_indptr", VP), ("req_seg_pos", VP), ("max_seg_rows", I32),
+                ("total_seg_rows", I32)]
+
+
+class rc_stats_t(C.Structure):
+    _fields_ = [(n, I64) for n in (
+        "pool_slots", "free_slots", "caller_slots", "tree_tokens", "nodes", "match_calls", "match_tokens",
+        "match_hits", "match_hit_tokens", "insert_calls", "insert_new_tokens", "insert_dup_freed",
+        "evicted_nodes", "evicted_tokens", "pins", "clock")]
+
+
+# header declarations: name -> (restype, argtypes)
+SIGNATURES = {
+    "rc_create": (I32, [I64, P(VP)]),
+    "rc_destroy": (None, [VP]),
+    "rc_match_prefix": (I32, [VP, VP, I64, C.c_int, P(I64), VP, P(I64)]),
+    "rc_insert": (I32, [VP, VP, VP, I64, C.c_int, P(I64), P(I64), VP]),
+    "rc_release": (I32, [VP, I64]),
+    "rc_evict": (I32, [VP, I64, P(I64), VP, I64, P(I64)]),
+    "rc_alloc": (I32, [VP, I64, VP]),
+    "rc_free": (I32, [VP, VP, I64]),
+    "sched_order": (I32, [VP, C.c_int, VP, VP, I32, VP]),
+    "rc_stats": (I32, [VP, P(rc_stats_t)]),
+    "rc_dump": (I32, [VP, C.c_char_p, I64, P(I64)]),
+    "kv_store": (I32, [P(rc_pool_desc), VP, VP, VP, I32, VP, VP, VP]),
+    "attn_decode_workspace": (I32, [P(rc_attn_desc), I32, I32, P(rc_cascade), P(C.c_size_t)]),
+    "attn_decode": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP, C.c_size_t, VP]),
+    "attn_extend_workspace": (I32, [P(rc_attn_desc), I32, I32, I32, P(C.c_size_t)]),
+    "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
+    "rc_sync": (I32, [VP, VP]),
+    "rc_strerror": (C.c_char_p, [I32]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load the C-ABI library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; "
+                               "g.build()' or python -m radixattention_prefix_shared_tree_gb300._compile)")
+        L = C.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def rc_strerror(status: int) -> str:
+    return lib().rc_strerror(int(status)).decode()
+
+
+class RCError(RuntimeError):
+    def __init__(self, call, status):
+        super().__init__(f"{call}: {rc_strerror(status)} ({status})")
+        self.status = status
+
+
+def _check(call, st):
+    if st != RC_OK:
+        raise RCError(call, st)
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _np_ptr(a):
+    return a.ctypes.data_as(VP) if a is not None and a.size else None
+
+
+# ------------------------------------------------------------------ host calls
+def rc_create(pool_slots: int):
+    h = VP()
+    st = lib().rc_create(int(pool_slots), C.byref(h))
+    _check("rc_create", st)
+    return h
+
+
+def rc_destroy(handle):
+    lib().rc_destroy(handle)
+
+
+def rc_match_prefix(handle, tokens, pin: bool):
+    t = _i32(tokens)
+    out = np.empty(max(len(t), 1), np.int32)
+    m, node = I64(0), I64(-1)
+    st = lib().rc_match_prefix(handle, _np_ptr(t), len(t), int(pin), C.byref(m), out.ctypes.data_as(VP),
+                               C.byref(node))
+    return st, m.value, out[:m.value].copy(), node.value
+
+
+def rc_insert(handle, tokens, slots, pin: bool):
+    t, s = _i32(tokens), _i32(slots)
+    if len(t) != len(s):
+        raise ValueError("tokens and slots differ in length")
+    out = np.empty(max(len(t), 1), np.int32)
+    present, node = I64(0), I64(-1)
+    st = lib().rc_insert(handle, _np_ptr(t), _np_ptr(s), len(t), int(pin), C.byref(present), C.byref(node),
+                         out.ctypes.data_as(VP))
+    return st, present.value, node.value, out[:len(t)].copy()
+
+
+def rc_release(handle, node: int):
+    return lib().rc_release(handle, int(node))
+
+
+def rc_evict(handle, n_tokens: int, log_cap: int = 4096):
+    log = np.empty(max(log_cap, 1), np.int64)
+    freed, cnt = I64(0), I64(0)
+    st = lib().rc_evict(handle, int(n_tokens), C.byref(freed), log.ctypes.data_as(VP), log_cap, C.byref(cnt))
+    return st, freed.value, log[:min(cnt.value, log_cap)].copy()
+
+
+def rc_alloc(handle, n: int):
+    out = np.empty(max(n, 1), np.int32)
+    st = lib().rc_alloc(handle, int(n), out.ctypes.data_as(VP))
+    return st, (out[:n].copy() if st == RC_OK else np.empty(0, np.int32))
+
+
+def rc_free(handle, slots):
+    s = _i32(slots)
+    return lib().rc_free(handle, _np_ptr(s), len(s))
+
+
+def sched_order(handle, policy: int, prompts):
+    arrs = [_i32(p) for p in prompts]
+    ptrs = (VP * max(len(arrs), 1))(*[a.ctypes.data if a.size else None for a in arrs])
+    lens = np.asarray([len(a) for a in arrs], np.int64)
+    out = np.empty(max(len(arrs), 1), np.int32)
+    st = lib().sched_order(handle, int(policy), ptrs, _np_ptr(lens), len(arrs), out.ctypes.data_as(VP))
+    return st, out[:len(arrs)].copy()
+
+
+def rc_stats(handle) -> dict:
+    s = rc_stats_t()
+    _check("rc_stats", lib().rc_stats(handle, C.byref(s)))
+    return {n: int(getattr(s, n)) for n, _ in rc_stats_t._fields_}
+
+
+def rc_dump(handle) -> str:
+    need = I64(0)
+    _check("rc_dump", lib().rc_dump(handle, None, 0, C.byref(need)))
+    buf = C.create_string_buffer(need.value + 1)
+    _check("rc_dump", lib().rc_dump(handle, buf, need.value + 1, C.byref(need)))
+    return buf.value.decode()
+
+
+_STAT_RENAME = {"pool_slots": "pool", "free_slots": "free", "caller_slots": "caller"}
+
+
+class RadixCache:
+    """A cache handle with the host calls as methods (same shapes as the oracle's tree)."""
+
+    def __init__(self, pool_slots: int):
+        self._h = rc_create(pool_slots)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h and _lib is not None:
+            _lib.rc_destroy(h)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def match(self, tokens, pin: bool):
+        return rc_match_prefix(self._h, tokens, pin)
+
+    def insert(self, tokens, slots, pin: bool):
+        return rc_insert(self._h, tokens, slots, pin)
+
+    def release(self, node: int):
+        return rc_release(self._h, node)
+
+    def evict(self, n_tokens: int, log_cap: int = 4096):
+        return rc_evict(self._h, n_tokens, log_cap)
+
+    def alloc(self, n: int):
+        return rc_alloc(self._h, n)
+
+    def free(self, slots):
+        return rc_free(self._h, slots)
+
+    def sched_order(self, policy: int, prompts):
+        return sched_order(self._h, policy, prompts)
+
+    def dump(self) -> str:
+        return rc_dump(self._h)
+
+    def stats(self) -> dict:
+        return {_STAT_RENAME.get(k, k): v for k, v in rc_stats(self._h).items()}
+
+
+# ---------------------------------------------------------------- device calls
+def _tp(t):
+    """Device pointer of a torch tensor (None -> NULL)."""
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = None) -> rc_pool_desc:
+    """Descriptor of a pool held in torch tensors: k [n_slots, Hkv, dk] (or [n_slots, dk] latent)."""
+    d = rc_pool_desc()
+    d.k = k.data_ptr()
+    d.v = v.data_ptr() if v is not None else None
+    d.n_slots = k.shape[0]
+    if mla:
+        d.kv_heads, d.head_dim_k = 1, k.shape[-1]
+        d.head_dim_v = int(head_dim_v)
+    else:
+        d.kv_heads, d.head_dim_k = k.shape[1], k.shape[2]
+        d.head_dim_v = v.shape[2]
+    d.mla = int(mla)
+    d.err = err.data_ptr() if err is not None else None
+    return d
+
+
+def make_attn_desc(pool: rc_pool_desc, q_heads: int, sm_scale: float) -> rc_attn_desc:
+    a = rc_attn_desc()
+    a.pool = pool
+    a.q_heads = int(q_heads)
+    a.sm_scale = float(sm_scale)
+    return a
+
+
+def make_kv_table(slots, start, length, max_len: int) -> rc_kv_table:
+    t = rc_kv_table()
+    t.slots, t.start, t.len = slots.data_ptr(), start.data_ptr(), length.data_ptr()
+    t.max_len = int(max_len)
+    return t
+
+
+def make_cascade(seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos,
+                 max_seg_rows: int) -> rc_cascade:
+    c = rc_cascade()
+    c.n_seg = seg_indptr.numel() - 1
+    c.seg_slots = seg_slots.data_ptr() if seg_slots.numel() else None
+    c.seg_indptr, c.seg_row_indptr = seg_indptr.data_ptr(), seg_row_indptr.data_ptr()
+    c.seg_rows = seg_rows.data_ptr() if seg_rows.numel() else None
+    c.req_seg_indptr = req_seg_indptr.data_ptr()
+    c.req_seg_pos = req_seg_pos.data_ptr() if req_seg_pos.numel() else None
+    c.max_seg_rows = int(max_seg_rows)
+    c.total_seg_rows = int(seg_rows.numel())
+    return c
+
+
+def kv_store(pool: rc_pool_desc, slots, k_new, v_new, table=None, table_pos=None, stream=None):
+    st = lib().kv_store(C.byref(pool), _tp(slots), _tp(k_new), _tp(v_new), int(slots.numel()), _tp(table),
+                        _tp(table_pos), _stream(stream))
+    _check("kv_store", st)
+
+
+def attn_decode_workspace(desc: rc_attn_desc, batch: int, max_len: int, cascade: rc_cascade | None = None) -> int:
+    n = C.c_size_t(0)
+    st = lib().attn_decode_workspace(C.byref(desc), int(batch), int(max_len),
+                                     C.byref(cascade) if cascade is not None else None, C.byref(n))
+    _check("attn_decode_workspace", st)
+    return int(n.value)
+
+
+def attn_decode(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=None, ws=None,
+                cascade: rc_cascade | None = None, stream=None):
+    st = lib().attn_decode(C.byref(desc), _tp(q), C.byref(kv), int(batch),
+                           C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse), _tp(ws),
+                           int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream))
+    _check("attn_decode", st)
+
+
+def attn_extend_workspace(desc: rc_attn_desc, batch: int, max_q: int, max_len: int) -> int:
+    n = C.c_size_t(0)
+    _check("attn_extend_workspace", lib().attn_extend_workspace(C.byref(desc), int(batch), int(max_q),
+                                                                 int(max_len), C.byref(n)))
+    return int(n.value)
+
+
+def attn_extend(desc: rc_attn_desc, q, qo_indptr, kv: rc_kv_table, batch: int, max_q: int, out, lse=None,
+                ws=None, stream=None):
+    st = lib().attn_extend(C.byref(desc), _tp(q), _tp(qo_indptr), C.byref(kv), int(batch), int(max_q), _tp(out),
+                           _tp(lse), _tp(ws), int(ws.numel() * ws.element_size()) if ws is not None else 0,
+                           _stream(stream))
+    _check("attn_extend", st)
+
+
+def rc_sync(err=None, stream=None) -> int:
+    return lib().rc_sync(_stream(stream), _tp(err))

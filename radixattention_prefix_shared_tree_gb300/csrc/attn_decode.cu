@@ -1,0 +1,454 @@
+// attn_decode: one new token per request attends to its whole cached context,
+// read through the request's slot table (decode phase of the SageMaker LMI
+// article; the K/V come from the radix-tree cache of inference-notes note 49,
+// section 2).  Memory-bound: every K/V row of the context is read once per KV
+// head per step, so the design goal is to stream rows at HBM speed.
+//
+//  1. split-K pass (flat): CTA = (key chunk, KV head, request).  The G query
+//     heads of the KV head share each K/V row (grouped-query head grouping).
+//     K/V rows are gathered by slot with 16-byte cp.async into a 3-stage
+//     shared-memory ring; the products run on mma.sync with the keys on the M
+//     side and the G heads on the N side (so G = 4 or 8 wastes at most half of
+//     an n8 tile instead of 12 of 16 rows), and P is moved from accumulator
+//     layout to operand layout in registers with movmatrix.  Each warp runs its
+//     own online softmax over a quarter of every tile; the four warps merge at
+//     the end.  Output: a normalised partial and its log-sum-exp per
+//     (request, head, chunk).
+//  2. cascade pass (optional): each shared prefix segment is read once for all
+//     requests below it (mq_attn.cuh), producing one more partial per
+//     (request, head) and segment.
+//  3. merge pass: per (request, head), combine all partials by log-sum-exp.
+
+#include "common.cuh"
+#include "mq_attn.cuh"
+
+namespace {
+
+constexpr int kDecKeys = 64;    // keys per tile (16 per warp)
+constexpr int kDecStages = 3;
+
+template <int D>
+constexpr int dec_smem_bytes() {
+    return 8 * D * 2 + kDecStages * 2 * kDecKeys * D * 2;
+}
+
+struct DecParams {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* pool_k;
+    const __nv_bfloat16* pool_v;
+    int64_t n_slots;
+    int32_t kv_heads, q_heads;
+    float scale_log2;
+    int32_t* err;
+    const int32_t* table;
+    const int32_t* start;
+    const int32_t* len;
+    int32_t chunk;       // keys per CTA
+    int32_t n_chunks;    // max chunks per request (partial stride)
+    float* part_o;       // [B][Hq][n_chunks][D]
+    float* part_lse;     // [B][Hq][n_chunks]
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p) {
+    constexpr int CH = D / 8;
+    constexpr int KS = D / 16;
+    extern __shared__ __align__(128) unsigned char smem[];
+    unsigned char* sQ = smem;                    // 8 heads x D, swizzled
+    unsigned char* sKV = smem + 8 * D * 2;
+    constexpr int TILE_BYTES = kDecKeys * D * 2;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g_lane = lane >> 2, t_lane = lane & 3;
+    const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int L = p.len[b];
+    const int k_begin = chunk * p.chunk;
+    if (k_begin >= L) return;
+    const int k_count = min(L - k_begin, p.chunk);
+    const int32_t* keys = p.table + p.start[b] + k_begin;
+
+    for (int i = tid; i < 8 * CH; i += 128) {
+        const int r = i / CH, c = i % CH;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (r < G)
+            v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.q_heads + kvh * G + r) * D + c * 8);
+        *reinterpret_cast<uint4*>(sQ + rc::swz<CH>(r, c)) = v;
+    }
+
+    auto load_tile = [&](int kt, int st) {
+        unsigned char* sK = sKV + st * 2 * TILE_BYTES;
+        unsigned char* sV = sK + TILE_BYTES;
+        constexpr int PER = kDecKeys * CH / 128;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int lin = i * 128 + tid;
+            const int r = lin / CH, c = lin % CH;
+            const int key = kt * kDecKeys + r;
+            int slot = 0;
+            uint32_t bytes = 0;
+            if (key < k_count) {
+                slot = __ldg(keys + key);
+                if (slot >= 0 && (int64_t)slot < p.n_slots) bytes = 16;
+                else { slot = 0; rc::flag_error(p.err, rc::kErrBadSlot); }
+            }
+            const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
+            rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes);
+            rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes);
+        }
+    };
+
+    const int n_tiles = (k_count + kDecKeys - 1) / kDecKeys;
+#pragma unroll
+    for (int s = 0; s < kDecStages - 1; ++s) {
+        if (s < n_tiles) load_tile(s, s);
+        rc::cp_async_commit();
+    }
+    __syncthreads();
+
+    // Q as the B operand (k = dims, n = heads): fragments for every k-step.
+    uint32_t qb[KS][2];
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+        const int r = lane & 7;
+        const int c = ks * 2 + (lane >> 3);
+        uint32_t r0, r1, r2, r3;
+        rc::ldmatrix_x4(rc::smem_u32(sQ + rc::swz<CH>(r, c)), r0, r1, r2, r3);
+        qb[ks][0] = r0;
+        qb[ks][1] = r1;
+        if (ks + 1 < KS) {
+            qb[ks + 1][0] = r2;
+            qb[ks + 1][1] = r3;
+        }
+    }
+
+    // O^T accumulators: m = dims (KS tiles of 16), n = heads.
+    float o[KS][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+    for (int kt = 0; kt < n_tiles; ++kt) {
+        rc::cp_async_wait<kDecStages - 2>();
+        __syncthreads();
+        if (kt + kDecStages - 1 < n_tiles) load_tile(kt + kDecStages - 1, (kt + kDecStages - 1) % kDecStages);
+        rc::cp_async_commit();
+        const unsigned char* sK = sKV + (kt % kDecStages) * 2 * TILE_BYTES;
+        const unsigned char* sV = sK + TILE_BYTES;
+        const int kw = warp * 16;  // this warp's 16 keys of the tile
+
+        // S^T (16 keys x 8 heads) = K_w Q^T
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int key = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                rc::ldmatrix_x4(rc::smem_u32(sK + rc::swz<CH>(key, ks * 2 + (lane >> 4))), a0, a1, a2, a3);
+                rc::mma_bf16_16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
+        }
+        const int key_lo = kt * kDecKeys + kw + g_lane;  // rows g and g+8
+        const bool v_lo = key_lo < k_count, v_hi = key_lo + 8 < k_count;
+        s[0] = v_lo ? s[0] * p.scale_log2 : -INFINITY;
+        s[1] = v_lo ? s[1] * p.scale_log2 : -INFINITY;
+        s[2] = v_hi ? s[2] * p.scale_log2 : -INFINITY;
+        s[3] = v_hi ? s[3] * p.scale_log2 : -INFINITY;
+        // heads 2t (elements 0, 2) and 2t+1 (elements 1, 3)
+        float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
+        float alpha[2], mu[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+            mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+            const float m_new = fmaxf(m_run[j], mx[j]);
+            mu[j] = m_new == -INFINITY ? 0.f : m_new;
+            alpha[j] = rc::fast_exp2(m_run[j] - mu[j]);
+            m_run[j] = m_new;
+        }
+        const float p0 = rc::fast_exp2(s[0] - mu[0]), p1 = rc::fast_exp2(s[1] - mu[1]);
+        const float p2 = rc::fast_exp2(s[2] - mu[0]), p3 = rc::fast_exp2(s[3] - mu[1]);
+        l_run[0] = l_run[0] * alpha[0] + p0 + p2;
+        l_run[1] = l_run[1] * alpha[1] + p1 + p3;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            o[i][0] *= alpha[0];
+            o[i][1] *= alpha[1];
+            o[i][2] *= alpha[0];
+            o[i][3] *= alpha[1];
+        }
+        // P^T as the B operand (k = keys, n = heads), transposed in registers.
+        const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));
+        const uint32_t pb1 = rc::movmatrix_trans(rc::pack_bf16(p2, p3));
+        // O^T (dims x heads) += V_w^T P^T
+        {
+            const int key = kw + (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                rc::ldmatrix_x4_trans(rc::smem_u32(sV + rc::swz<CH>(key, mt * 2 + ((lane >> 3) & 1))), a0, a1,
+                                      a2, a3);
+                rc::mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+        }
+    }
+    rc::cp_async_wait<0>();
+
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+    }
+    __syncthreads();  // stages are free: reuse them for the cross-warp merge
+    float* sO = reinterpret_cast<float*>(sKV);          // [4 warps][8 heads][D]
+    float* sM = sO + 4 * 8 * D;                         // [4][8]
+    float* sL = sM + 32;                                // [4][8]
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+        const int d0 = mt * 16 + g_lane;
+        sO[(warp * 8 + 2 * t_lane) * D + d0] = o[mt][0];
+        sO[(warp * 8 + 2 * t_lane + 1) * D + d0] = o[mt][1];
+        sO[(warp * 8 + 2 * t_lane) * D + d0 + 8] = o[mt][2];
+        sO[(warp * 8 + 2 * t_lane + 1) * D + d0 + 8] = o[mt][3];
+    }
+    if (g_lane == 0) {
+        sM[warp * 8 + 2 * t_lane] = m_run[0];
+        sM[warp * 8 + 2 * t_lane + 1] = m_run[1];
+        sL[warp * 8 + 2 * t_lane] = l_run[0];
+        sL[warp * 8 + 2 * t_lane + 1] = l_run[1];
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += 128) {
+        const int h = i / D, d = i % D;
+        float m = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) m = fmaxf(m, sM[w * 8 + h]);
+        float l = 0.f, acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = sM[w * 8 + h];
+            const float f = mw == -INFINITY ? 0.f : rc::fast_exp2(mw - m);
+            l += sL[w * 8 + h] * f;
+            acc += sO[(w * 8 + h) * D + d] * f;
+        }
+        const int64_t idx = ((int64_t)b * p.q_heads + kvh * G + h) * p.n_chunks + chunk;
+        p.part_o[idx * D + d] = acc / l;
+        if (d == 0) p.part_lse[idx] = m + log2f(l);
+    }
+}
+
+// Combine every partial of (request, head): cascade segments first, then the
+// chunks of the request's own table row.
+template <int D>
+__global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tail_o,
+                                                   const float* __restrict__ tail_lse, int32_t n_chunks,
+                                                   int32_t chunk, const int32_t* __restrict__ len,
+                                                   const float* __restrict__ seg_o,
+                                                   const float* __restrict__ seg_lse,
+                                                   const int32_t* __restrict__ req_seg_indptr,
+                                                   const int32_t* __restrict__ req_seg_pos, int32_t q_heads,
+                                                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                   int32_t* err) {
+    constexpr int PER = D / 32;
+    const int bh = blockIdx.x;
+    const int b = bh / q_heads, h = bh % q_heads;
+    const int lane = threadIdx.x;
+    int nc = (len[b] + chunk - 1) / chunk;
+    if (nc > n_chunks) {  // len[b] above the caller's max_len: the split pass skipped keys
+        if (lane == 0 && h == 0) rc::flag_error(err, rc::kErrBadSlot);
+        nc = n_chunks;
+    }
+    const int s0 = req_seg_indptr ? req_seg_indptr[b] : 0;
+    const int ns = req_seg_indptr ? req_seg_indptr[b + 1] - s0 : 0;
+    float m = -INFINITY;
+    for (int i = 0; i < ns; ++i) m = fmaxf(m, seg_lse[(int64_t)req_seg_pos[s0 + i] * q_heads + h]);
+    for (int c = 0; c < nc; ++c) m = fmaxf(m, tail_lse[(int64_t)bh * n_chunks + c]);
+    float acc[PER];
+#pragma unroll
+    for (int j = 0; j < PER; ++j) acc[j] = 0.f;
+    float wsum = 0.f;
+    for (int i = 0; i < ns; ++i) {
+        const int64_t row = (int64_t)req_seg_pos[s0 + i] * q_heads + h;
+        const float w = rc::fast_exp2(seg_lse[row] - m);
+        wsum += w;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] += w * seg_o[row * D + lane + 32 * j];
+    }
+    for (int c = 0; c < nc; ++c) {
+        const int64_t row = (int64_t)bh * n_chunks + c;
+        const float w = rc::fast_exp2(tail_lse[row] - m);
+        wsum += w;
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] += w * tail_o[row * D + lane + 32 * j];
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) out[(int64_t)bh * D + lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
+    if (lse && lane == 0) lse[bh] = (m + log2f(wsum)) * rc::kLn2;
+}
+
+// ------------------------------------------------------------------ planning
+struct DecodePlan {
+    int chunk = 0, n_chunks = 0;
+    size_t tail_o = 0, tail_lse = 0, seg_o = 0, seg_lse = 0, total = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, const rc_cascade* casc,
+                      DecodePlan* pl) {
+    if (!d || batch < 0 || max_len < 0) return RC_ERR_ARG;
+    const int hkv = d->pool.kv_heads;
+    if (hkv <= 0 || d->q_heads <= 0 || d->q_heads % hkv) return RC_ERR_ARG;
+    const int dv = d->pool.head_dim_v;
+    // Split so that the grid covers the SMs about four times over.
+    const int64_t base = (int64_t)batch * hkv;
+    const int64_t target = 4LL * rc_host::sm_count();
+    int64_t splits = base > 0 ? (target + base - 1) / base : 1;
+    const int64_t max_splits = max_len > 0 ? (max_len + 255) / 256 : 1;
+    if (splits > max_splits) splits = max_splits;
+    if (splits < 1) splits = 1;
+    int64_t chunk = max_len > 0 ? (max_len + splits - 1) / splits : kDecKeys;
+    chunk = (chunk + kDecKeys - 1) / kDecKeys * kDecKeys;
+    pl->chunk = (int)chunk;
+    pl->n_chunks = max_len > 0 ? (int)((max_len + chunk - 1) / chunk) : 1;
+    const size_t rows = (size_t)batch * d->q_heads;
+    pl->tail_o = align256(rows * pl->n_chunks * dv * sizeof(float));
+    pl->tail_lse = align256(rows * pl->n_chunks * sizeof(float));
+    const size_t srows = casc ? (size_t)casc->total_seg_rows * d->q_heads : 0;
+    pl->seg_o = align256(srows * dv * sizeof(float));
+    pl->seg_lse = align256(srows * sizeof(float));
+    pl->total = pl->tail_o + pl->tail_lse + pl->seg_o + pl->seg_lse;
+    return RC_OK;
+}
+
+template <int D, int G>
+cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream_t st) {
+    constexpr int smem = dec_smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.n_chunks, kv_heads, batch);
+    decode_split_kernel<D, G><<<grid, 128, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_heads, cudaStream_t st) {
+    constexpr int smem = rc::mq_smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<rc::mq_attn_kernel<D, G, rc::MQMode::kCascade>>(smem);
+    if (e != cudaSuccess) return e;
+    constexpr int TPC = rc::kMQRows / G;
+    dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg);
+    rc::mq_attn_kernel<D, G, rc::MQMode::kCascade><<<grid, 128, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D, int G>
+cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, int batch,
+                    int kv_heads, cudaStream_t st) {
+    cudaError_t e = cudaSuccess;
+    if (casc && casc->n_seg > 0 && casc->max_seg_rows > 0) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
+    if (e == cudaSuccess) e = launch_split<D, G>(dp, batch, kv_heads, st);
+    return e;
+}
+
+template <int D>
+cudaError_t dispatch_group(int G, const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc,
+                           int batch, int kv_heads, cudaStream_t st, bool* ok) {
+    *ok = true;
+    switch (G) {
+        case 1: return run_gqa<D, 1>(dp, mp, casc, batch, kv_heads, st);
+        case 2: return run_gqa<D, 2>(dp, mp, casc, batch, kv_heads, st);
+        case 4: return run_gqa<D, 4>(dp, mp, casc, batch, kv_heads, st);
+        case 8: return run_gqa<D, 8>(dp, mp, casc, batch, kv_heads, st);
+        default: *ok = false; return cudaSuccess;
+    }
+}
+
+}  // namespace
+
+extern "C" rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_len,
+                                           const rc_cascade* cascade, size_t* bytes) {
+    if (!bytes) return RC_ERR_ARG;
+    DecodePlan pl;
+    rc_status s = plan_decode(desc, batch, max_len, cascade, &pl);
+    if (s != RC_OK) return s;
+    *bytes = pl.total;
+    return RC_OK;
+}
+
+extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv, int32_t batch,
+                                 const rc_cascade* casc, void* out, float* lse, void* ws, size_t ws_bytes,
+                                 rc_stream_t stream) {
+    if (!desc || !kv || batch < 0) return RC_ERR_ARG;
+    if (batch == 0) return RC_OK;
+    if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
+    DecodePlan pl;
+    rc_status s = plan_decode(desc, batch, kv->max_len, casc, &pl);
+    if (s != RC_OK) return s;
+    if (!ws || ws_bytes < pl.total) return RC_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return RC_ERR_ARG;
+    const bool use_casc = casc && casc->n_seg > 0;
+    if (use_casc && (!casc->seg_slots || !casc->seg_indptr || !casc->seg_row_indptr || !casc->seg_rows ||
+                     !casc->req_seg_indptr || !casc->req_seg_pos))
+        return RC_ERR_ARG;
+    const rc_pool_desc& P = desc->pool;
+    const int D = P.head_dim_k;
+    if (P.mla || P.head_dim_v != D || !P.v) return RC_ERR_UNSUPPORTED;
+    const int G = desc->q_heads / P.kv_heads;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    DecParams dp;
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.pool_k = static_cast<const __nv_bfloat16*>(P.k);
+    dp.pool_v = static_cast<const __nv_bfloat16*>(P.v);
+    dp.n_slots = P.n_slots;
+    dp.kv_heads = P.kv_heads;
+    dp.q_heads = desc->q_heads;
+    dp.scale_log2 = desc->sm_scale * rc::kLog2e;
+    dp.err = P.err;
+    dp.table = kv->slots;
+    dp.start = kv->start;
+    dp.len = kv->len;
+    dp.chunk = pl.chunk;
+    dp.n_chunks = pl.n_chunks;
+    dp.part_o = reinterpret_cast<float*>(w);
+    dp.part_lse = reinterpret_cast<float*>(w + pl.tail_o);
+    rc::MQParams mp{};
+    mp.q = dp.q;
+    mp.pool_k = dp.pool_k;
+    mp.pool_v = dp.pool_v;
+    mp.n_slots = dp.n_slots;
+    mp.kv_heads = dp.kv_heads;
+    mp.q_heads = dp.q_heads;
+    mp.scale_log2 = dp.scale_log2;
+    mp.err = dp.err;
+    float* seg_o = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse);
+    float* seg_lse = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse + pl.seg_o);
+    if (use_casc) {
+        mp.seg_slots = casc->seg_slots;
+        mp.seg_indptr = casc->seg_indptr;
+        mp.seg_row_indptr = casc->seg_row_indptr;
+        mp.seg_rows = casc->seg_rows;
+        mp.part_o = seg_o;
+        mp.part_lse = seg_lse;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    bool ok = false;
+    cudaError_t e = cudaSuccess;
+    if (D == 128) e = dispatch_group<128>(G, dp, mp, use_casc ? casc : nullptr, batch, P.kv_heads, st, &ok);
+    else if (D == 64) e = dispatch_group<64>(G, dp, mp, use_casc ? casc : nullptr, batch, P.kv_heads, st, &ok);
+    if (!ok) return RC_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return RC_ERR_CUDA;
+    const int32_t* ri = use_casc ? casc->req_seg_indptr : nullptr;
+    const int32_t* rp = use_casc ? casc->req_seg_pos : nullptr;
+    const unsigned nbh = (unsigned)batch * desc->q_heads;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+    if (D == 128)
+        merge_kernel<128><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
+                                              ri, rp, desc->q_heads, o, lse, P.err);
+    else
+        merge_kernel<64><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
+                                             ri, rp, desc->q_heads, o, lse, P.err);
+    return rc_host::launch_status(cudaGetLastError());
+}

@@ -1,0 +1,85 @@
+// attn_extend: prefill of the new (uncached) tokens of each request over its
+// cached prefix.  In inference-notes note 49, section 2, request 2 reuses the
+// shared system prompt and "only Q2" has to be computed; in the SageMaker LMI
+// article's prefill phase all of those tokens are processed at once.  Token i
+// of request b sits at position len[b] - n_b + i of its slot-table row and
+// attends causally to positions 0..itself, prefix included.
+//
+// The kernel body is mq_attn.cuh: a CTA owns 64 query rows = (64/G new tokens)
+// x (the G query heads of one KV head), so each gathered K/V row serves every
+// head of its group; tensor-core products, online softmax, bf16 output written
+// directly (no split, no workspace).
+
+#include "common.cuh"
+#include "mq_attn.cuh"
+
+namespace {
+
+template <int D, int G>
+cudaError_t launch_extend(const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st) {
+    constexpr int smem = rc::mq_smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<rc::mq_attn_kernel<D, G, rc::MQMode::kExtend>>(smem);
+    if (e != cudaSuccess) return e;
+    constexpr int TPC = rc::kMQRows / G;
+    dim3 grid((max_q + TPC - 1) / TPC, kv_heads, batch);
+    rc::mq_attn_kernel<D, G, rc::MQMode::kExtend><<<grid, 128, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch(int G, const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st,
+                     bool* ok) {
+    *ok = true;
+    switch (G) {
+        case 1: return launch_extend<D, 1>(p, batch, max_q, kv_heads, st);
+        case 2: return launch_extend<D, 2>(p, batch, max_q, kv_heads, st);
+        case 4: return launch_extend<D, 4>(p, batch, max_q, kv_heads, st);
+        case 8: return launch_extend<D, 8>(p, batch, max_q, kv_heads, st);
+        default: *ok = false; return cudaSuccess;
+    }
+}
+
+}  // namespace
+
+extern "C" rc_status attn_extend_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_q,
+                                           int32_t max_len, size_t* bytes) {
+    if (!desc || !bytes || batch < 0 || max_q < 0 || max_len < 0) return RC_ERR_ARG;
+    *bytes = 0;
+    return RC_OK;
+}
+
+extern "C" rc_status attn_extend(const rc_attn_desc* desc, const void* q, const int32_t* qo_indptr,
+                                 const rc_kv_table* kv, int32_t batch, int32_t max_q, void* out, float* lse,
+                                 void* ws, size_t ws_bytes, rc_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!desc || !kv || batch < 0 || max_q < 0) return RC_ERR_ARG;
+    if (batch == 0 || max_q == 0) return RC_OK;
+    if (!q || !qo_indptr || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
+    const rc_pool_desc& P = desc->pool;
+    if (P.kv_heads <= 0 || desc->q_heads <= 0 || desc->q_heads % P.kv_heads) return RC_ERR_ARG;
+    if (P.mla || !P.v || P.head_dim_v != P.head_dim_k) return RC_ERR_UNSUPPORTED;
+    rc::MQParams p{};
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.pool_k = static_cast<const __nv_bfloat16*>(P.k);
+    p.pool_v = static_cast<const __nv_bfloat16*>(P.v);
+    p.n_slots = P.n_slots;
+    p.kv_heads = P.kv_heads;
+    p.q_heads = desc->q_heads;
+    p.scale_log2 = desc->sm_scale * rc::kLog2e;
+    p.err = P.err;
+    p.qo_indptr = qo_indptr;
+    p.table = kv->slots;
+    p.start = kv->start;
+    p.len = kv->len;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.lse = lse;
+    const int G = desc->q_heads / P.kv_heads;
+    bool ok = false;
+    cudaError_t e = cudaSuccess;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (P.head_dim_k == 128) e = dispatch<128>(G, p, batch, max_q, P.kv_heads, st, &ok);
+    else if (P.head_dim_k == 64) e = dispatch<64>(G, p, batch, max_q, P.kv_heads, st, &ok);
+    if (!ok) return RC_ERR_UNSUPPORTED;
+    return rc_host::launch_status(e);
+}

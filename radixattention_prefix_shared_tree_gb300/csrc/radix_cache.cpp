@@ -1,0 +1,477 @@
+// Host half of the library: the radix tree over token ids, reference-count
+// pinning, LRU leaf eviction, the slot allocator of the shared KV pool and the
+// scheduling order.  Rules follow "RadixAttention, eviction and cache churn"
+// (inference-notes note 49), sections 2, 4 and 5, and the RadixAttention
+// paragraph and nine-step walkthrough of the unite.ai article on SGLang; the
+// open points are read as documented in include/radixattn.h.
+//
+// Layout, chosen for O(match length) lookups and O(log n) eviction:
+//  * nodes live in a flat vector and are recycled through a free list; a
+//    node's token run and slot run are (offset, length) views into two
+//    parallel append-only arenas, so splitting an edge copies nothing;
+//  * one hash map keyed by (parent index, first token) holds every edge;
+//  * evictable leaves (no children, no pins, not the root) sit in an ordered
+//    set keyed by (last access, id), so the next victim is its first element;
+//  * free slots are a two-level bitmap, so "the n smallest free ids" is a
+//    scan of set bits from the lowest non-empty word.
+
+#include "../../include/radixattn.h"
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <set>
+#include <string>
+#include <unordered_map>
+#include <utility>
+#include <vector>
+
+namespace {
+
+enum : uint8_t { FREE = 0, HELD = 1, CACHED = 2 };
+
+struct Rec {
+    int64_t id = -1;
+    int32_t parent = -1;
+    int32_t nchild = 0;
+    int64_t off = 0;   // run start in the arenas
+    int32_t len = 0;   // run length
+    int64_t ref = 0;
+    uint64_t stamp = 0;
+    bool live = false;
+    bool in_lru = false;
+    uint64_t lru_stamp = 0;  // stamp under which it sits in the LRU set
+};
+
+inline uint64_t edge_key(int32_t parent, int32_t first_tok) {
+    return ((uint64_t)(uint32_t)parent << 32) | (uint32_t)first_tok;
+}
+
+}  // namespace
+
+struct rc_cache {
+    int64_t pool = 0;
+    std::vector<uint8_t> owner;      // per slot: FREE, HELD (by a caller), CACHED (in the tree)
+    std::vector<uint64_t> bits;      // 1 = free
+    std::vector<uint64_t> summary;   // 1 = bits[w] != 0
+    int64_t n_free = 0, n_held = 0, n_cached = 0;
+
+    std::vector<Rec> recs;
+    std::vector<int32_t> spare;      // recycled node indices
+    std::vector<int32_t> tok_arena, slot_arena;
+    int64_t arena_live = 0;
+    std::unordered_map<uint64_t, int32_t> edges;
+    std::unordered_map<int64_t, int32_t> by_id;
+    std::set<std::pair<uint64_t, int64_t>> lru;
+    uint64_t clock = 0;
+    int64_t next_id = 0;
+    int64_t n_nodes = 0;
+
+    std::vector<uint32_t> mark;      // per slot epoch marks for duplicate checks
+    uint32_t epoch = 0;
+    std::vector<int32_t> path;       // scratch
+    std::vector<int32_t> scratch_slots;
+
+    int64_t match_calls = 0, match_tokens = 0, match_hits = 0, match_hit_tokens = 0;
+    int64_t insert_calls = 0, insert_new_tokens = 0, insert_dup_freed = 0;
+    int64_t evicted_nodes = 0, evicted_tokens = 0;
+
+    // ------------------------------------------------------------- slots
+    void slot_set_free(int32_t s) {
+        size_t w = (size_t)s >> 6;
+        bits[w] |= 1ull << (s & 63);
+        summary[w >> 6] |= 1ull << (w & 63);
+    }
+    int64_t next_word(int64_t w) const {  // first word index >= w with free bits, or -1
+        int64_t nw = (int64_t)bits.size();
+        if (w >= nw) return -1;
+        size_t sw = (size_t)w >> 6;
+        uint64_t m = summary[sw] & (~0ull << (w & 63));
+        while (!m) {
+            if (++sw >= summary.size()) return -1;
+            m = summary[sw];
+        }
+        return (int64_t)(sw << 6) + __builtin_ctzll(m);
+    }
+    void take_lowest(int64_t n, int32_t* out) {
+        int64_t got = 0, w = next_word(0);
+        while (got < n) {
+            uint64_t b = bits[(size_t)w];
+            while (b && got < n) {
+                int t = __builtin_ctzll(b);
+                b &= b - 1;
+                int32_t s = (int32_t)(w * 64 + t);
+                out[got++] = s;
+                owner[(size_t)s] = HELD;
+            }
+            bits[(size_t)w] = b;
+            if (!b) summary[(size_t)w >> 6] &= ~(1ull << (w & 63));
+            if (got < n) w = next_word(w + 1);
+        }
+        n_free -= n;
+        n_held += n;
+    }
+
+    // ------------------------------------------------------------- nodes
+    int32_t new_rec(int32_t parent, int64_t off, int32_t len) {
+        int32_t i;
+        if (!spare.empty()) { i = spare.back(); spare.pop_back(); }
+        else { i = (int32_t)recs.size(); recs.emplace_back(); }
+        Rec& r = recs[(size_t)i];
+        r = Rec();
+        r.id = next_id++;
+        r.parent = parent;
+        r.off = off;
+        r.len = len;
+        r.live = true;
+        by_id[r.id] = i;
+        n_nodes += 1;
+        return i;
+    }
+    const int32_t* toks(const Rec& r) const { return tok_arena.data() + r.off; }
+
+    void lru_out(int32_t i) {
+        Rec& r = recs[(size_t)i];
+        if (r.in_lru) { lru.erase({r.lru_stamp, r.id}); r.in_lru = false; }
+    }
+    void lru_fix(int32_t i) {  // put node i in or out of the candidate set per its state
+        Rec& r = recs[(size_t)i];
+        bool want = i != 0 && r.nchild == 0 && r.ref == 0;
+        if (r.in_lru && (!want || r.lru_stamp != r.stamp)) lru_out(i);
+        if (want && !r.in_lru) { lru.insert({r.stamp, r.id}); r.in_lru = true; r.lru_stamp = r.stamp; }
+    }
+
+    // Split node i after k tokens; returns the new upper node.
+    int32_t split(int32_t i, int32_t k) {
+        Rec lower = recs[(size_t)i];
+        int32_t up = new_rec(lower.parent, lower.off, k);  // may reallocate recs
+        Rec& L = recs[(size_t)i];
+        Rec& U = recs[(size_t)up];
+        edges[edge_key(L.parent, tok_arena[(size_t)L.off])] = up;
+        L.off += k;
+        L.len -= k;
+        L.parent = up;
+        edges[edge_key(up, tok_arena[(size_t)L.off])] = i;
+        U.nchild = 1;
+        U.ref = L.ref;
+        U.stamp = clock;
+        return up;
+    }
+
+    // Descend along tok[0..n).  With do_split the end of the match is made a
+    // node boundary and `path` receives root..end; `sl` (if given) receives
+    // the matched slots.  Returns the matched length.
+    int64_t descend(const int32_t* tok, int64_t n, bool do_split, std::vector<int32_t>* pth,
+                    std::vector<int32_t>* sl) {
+        int32_t cur = 0;
+        if (pth) { pth->clear(); pth->push_back(0); }
+        int64_t i = 0;
+        while (i < n) {
+            auto it = edges.find(edge_key(cur, tok[i]));
+            if (it == edges.end()) break;
+            int32_t c = it->second;
+            const Rec& r = recs[(size_t)c];
+            const int32_t* rt = toks(r);
+            int64_t lim = std::min<int64_t>(r.len, n - i);
+            int64_t k = 1;
+            while (k < lim && rt[k] == tok[i + k]) ++k;
+            if (sl) sl->insert(sl->end(), slot_arena.begin() + r.off, slot_arena.begin() + r.off + k);
+            i += k;
+            if (k < r.len) {
+                if (do_split) {
+                    int32_t up = split(c, (int32_t)k);
+                    if (pth) pth->push_back(up);
+                }
+                break;
+            }
+            cur = c;
+            if (pth) pth->push_back(cur);
+        }
+        return i;
+    }
+
+    void touch(const std::vector<int32_t>& pth) {
+        for (int32_t i : pth) {
+            recs[(size_t)i].stamp = clock;
+            lru_fix(i);
+        }
+    }
+    void pin(const std::vector<int32_t>& pth) {
+        for (int32_t i : pth) {
+            recs[(size_t)i].ref += 1;
+            lru_fix(i);
+        }
+    }
+
+    void maybe_compact() {
+        int64_t sz = (int64_t)tok_arena.size();
+        if (sz < (1 << 20) || sz < 3 * arena_live) return;
+        std::vector<int32_t> nt, ns;
+        nt.reserve((size_t)arena_live * 2);
+        ns.reserve((size_t)arena_live * 2);
+        for (Rec& r : recs) {
+            if (!r.live) continue;
+            int64_t o = (int64_t)nt.size();
+            nt.insert(nt.end(), tok_arena.begin() + r.off, tok_arena.begin() + r.off + r.len);
+            ns.insert(ns.end(), slot_arena.begin() + r.off, slot_arena.begin() + r.off + r.len);
+            r.off = o;
+        }
+        tok_arena.swap(nt);
+        slot_arena.swap(ns);
+    }
+
+    void dump_rec(int32_t i, const std::vector<std::vector<int32_t>>& kids, std::string& s) const {
+        const Rec& r = recs[(size_t)i];
+        char b[96];
+        std::snprintf(b, sizeof b, "%lld %lld %lld %llu %d:", (long long)r.id,
+                      (long long)(r.parent >= 0 ? recs[(size_t)r.parent].id : -1),
+                      (long long)r.ref, (unsigned long long)r.stamp, r.len);
+        s += b;
+        for (int32_t k = 0; k < r.len; ++k) { s += ' '; s += std::to_string(tok_arena[(size_t)(r.off + k)]); }
+        s += " |";
+        for (int32_t k = 0; k < r.len; ++k) { s += ' '; s += std::to_string(slot_arena[(size_t)(r.off + k)]); }
+        s += '\n';
+        for (int32_t c : kids[(size_t)i]) dump_rec(c, kids, s);
+    }
+};
+
+extern "C" {
+
+rc_status rc_create(int64_t pool_slots, rc_cache** out) {
+    if (!out || pool_slots < 0 || pool_slots > 0x7FFFFFFF) return RC_ERR_ARG;
+    *out = nullptr;
+    rc_cache* c = new (std::nothrow) rc_cache();
+    if (!c) return RC_ERR_NOMEM;
+    try {
+        c->pool = pool_slots;
+        c->owner.assign((size_t)pool_slots, FREE);
+        c->mark.assign((size_t)pool_slots, 0);
+        size_t nw = (size_t)((pool_slots + 63) / 64);
+        c->bits.assign(nw, ~0ull);
+        if (pool_slots & 63) c->bits[nw - 1] = (1ull << (pool_slots & 63)) - 1;
+        c->summary.assign((nw + 63) / 64 + 1, 0);
+        for (size_t w = 0; w < nw; ++w)
+            if (c->bits[w]) c->summary[w >> 6] |= 1ull << (w & 63);
+        c->n_free = pool_slots;
+        c->new_rec(-1, 0, 0);  // root: index 0, id 0
+    } catch (...) {
+        delete c;
+        return RC_ERR_NOMEM;
+    }
+    *out = c;
+    return RC_OK;
+}
+
+void rc_destroy(rc_cache* c) { delete c; }
+
+rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, int64_t* matched,
+                          int32_t* out_slots, rc_node* out_node) {
+    if (!c || n < 0 || (n > 0 && !tok) || !matched || !out_node) return RC_ERR_ARG;
+    c->clock += 1;
+    c->scratch_slots.clear();
+    int64_t m = c->descend(tok, n, true, &c->path, out_slots ? &c->scratch_slots : nullptr);
+    c->touch(c->path);
+    if (pin) c->pin(c->path);
+    if (out_slots && m) std::memcpy(out_slots, c->scratch_slots.data(), (size_t)m * 4);
+    *matched = m;
+    *out_node = c->recs[(size_t)c->path.back()].id;
+    c->match_calls += 1;
+    c->match_tokens += n;
+    c->match_hit_tokens += m;
+    c->match_hits += m > 0;
+    return RC_OK;
+}
+
+rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64_t n, int pin,
+                    int64_t* already_present, rc_node* out_node, int32_t* out_slots) {
+    if (!c || n < 0 || (n > 0 && (!tok || !slots)) || !already_present || !out_node) return RC_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        if (slots[i] < 0 || slots[i] >= c->pool) return RC_ERR_ARG;
+    std::vector<int32_t>& have = c->scratch_slots;
+    have.clear();
+    int64_t m = c->descend(tok, n, false, nullptr, &have);
+    if (++c->epoch == 0) { std::fill(c->mark.begin(), c->mark.end(), 0); c->epoch = 1; }
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t s = slots[i];
+        if (i < m && s == have[(size_t)i]) continue;
+        if (c->owner[(size_t)s] != HELD || c->mark[(size_t)s] == c->epoch) return RC_ERR_STATE;
+        c->mark[(size_t)s] = c->epoch;
+    }
+    c->clock += 1;
+    c->descend(tok, n, true, &c->path, nullptr);
+    if (m < n) {
+        int32_t parent = c->path.back();
+        int64_t off = (int64_t)c->tok_arena.size();
+        c->tok_arena.insert(c->tok_arena.end(), tok + m, tok + n);
+        c->slot_arena.insert(c->slot_arena.end(), slots + m, slots + n);
+        int32_t leaf = c->new_rec(parent, off, (int32_t)(n - m));
+        c->edges[edge_key(parent, tok[m])] = leaf;
+        c->recs[(size_t)parent].nchild += 1;
+        c->lru_fix(parent);
+        for (int64_t i = m; i < n; ++i) c->owner[(size_t)slots[i]] = CACHED;
+        c->n_held -= n - m;
+        c->n_cached += n - m;
+        c->arena_live += n - m;
+        c->path.push_back(leaf);
+    }
+    int64_t dup = 0;
+    for (int64_t i = 0; i < m; ++i) {
+        int32_t s = slots[i];
+        if (s == have[(size_t)i]) continue;
+        c->owner[(size_t)s] = FREE;
+        c->slot_set_free(s);
+        dup += 1;
+    }
+    c->n_held -= dup;
+    c->n_free += dup;
+    c->touch(c->path);
+    if (pin) c->pin(c->path);
+    if (out_slots) {
+        if (m) std::memcpy(out_slots, have.data(), (size_t)m * 4);
+        if (n > m) std::memcpy(out_slots + m, slots + m, (size_t)(n - m) * 4);
+    }
+    *already_present = m;
+    *out_node = c->recs[(size_t)c->path.back()].id;
+    c->insert_calls += 1;
+    c->insert_new_tokens += n - m;
+    c->insert_dup_freed += dup;
+    return RC_OK;
+}
+
+rc_status rc_release(rc_cache* c, rc_node node) {
+    if (!c) return RC_ERR_ARG;
+    auto it = c->by_id.find(node);
+    if (it == c->by_id.end()) return RC_ERR_STATE;
+    int32_t i = it->second;
+    if (c->recs[(size_t)i].ref <= 0) return RC_ERR_STATE;
+    for (; i >= 0; i = c->recs[(size_t)i].parent) {
+        c->recs[(size_t)i].ref -= 1;
+        c->lru_fix(i);
+    }
+    return RC_OK;
+}
+
+rc_status rc_evict(rc_cache* c, int64_t n_tokens, int64_t* freed, int64_t* log, int64_t log_cap,
+                   int64_t* n_evicted) {
+    if (!c || n_tokens < 0 || !freed || !n_evicted || (log_cap > 0 && !log)) return RC_ERR_ARG;
+    int64_t got = 0, cnt = 0;
+    while (got < n_tokens && !c->lru.empty()) {
+        int64_t id = c->lru.begin()->second;
+        c->lru.erase(c->lru.begin());
+        int32_t i = c->by_id[id];
+        Rec& r = c->recs[(size_t)i];
+        r.in_lru = false;
+        for (int32_t k = 0; k < r.len; ++k) {
+            int32_t s = c->slot_arena[(size_t)(r.off + k)];
+            c->owner[(size_t)s] = FREE;
+            c->slot_set_free(s);
+        }
+        c->n_free += r.len;
+        c->n_cached -= r.len;
+        c->arena_live -= r.len;
+        got += r.len;
+        c->edges.erase(edge_key(r.parent, c->tok_arena[(size_t)r.off]));
+        int32_t p = r.parent;
+        c->recs[(size_t)p].nchild -= 1;
+        if (log && cnt < log_cap) log[cnt] = id;
+        cnt += 1;
+        c->evicted_nodes += 1;
+        c->evicted_tokens += r.len;
+        r.live = false;
+        c->by_id.erase(id);
+        c->n_nodes -= 1;
+        c->spare.push_back(i);
+        c->lru_fix(p);
+    }
+    c->maybe_compact();
+    *freed = got;
+    *n_evicted = cnt;
+    return RC_OK;
+}
+
+rc_status rc_alloc(rc_cache* c, int64_t n, int32_t* out) {
+    if (!c || n < 0 || (n > 0 && !out)) return RC_ERR_ARG;
+    if (n > c->n_free) return RC_ERR_NOMEM;
+    if (n) c->take_lowest(n, out);
+    return RC_OK;
+}
+
+rc_status rc_free(rc_cache* c, const int32_t* slots, int64_t n) {
+    if (!c || n < 0 || (n > 0 && !slots)) return RC_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i)
+        if (slots[i] < 0 || slots[i] >= c->pool) return RC_ERR_ARG;
+    if (++c->epoch == 0) { std::fill(c->mark.begin(), c->mark.end(), 0); c->epoch = 1; }
+    for (int64_t i = 0; i < n; ++i) {
+        int32_t s = slots[i];
+        if (c->owner[(size_t)s] != HELD || c->mark[(size_t)s] == c->epoch) return RC_ERR_STATE;
+        c->mark[(size_t)s] = c->epoch;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        c->owner[(size_t)slots[i]] = FREE;
+        c->slot_set_free(slots[i]);
+    }
+    c->n_free += n;
+    c->n_held -= n;
+    return RC_OK;
+}
+
+rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, const int64_t* lens,
+                      int32_t n, int32_t* out_order) {
+    if (!c || n < 0 || (n > 0 && (!prompts || !lens || !out_order))) return RC_ERR_ARG;
+    if (policy != RC_FCFS && policy != RC_LPM) return RC_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i)
+        if (lens[i] < 0 || (lens[i] > 0 && !prompts[i])) return RC_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i) out_order[i] = i;
+    if (policy == RC_LPM && n > 1) {
+        std::vector<std::pair<int64_t, int32_t>> key((size_t)n);
+        for (int32_t i = 0; i < n; ++i)
+            key[(size_t)i] = {-c->descend(prompts[i], lens[i], false, nullptr, nullptr), i};
+        std::sort(key.begin(), key.end());  // (-match, index): longest first, then arrival
+        for (int32_t i = 0; i < n; ++i) out_order[i] = key[(size_t)i].second;
+    }
+    return RC_OK;
+}
+
+rc_status rc_stats(rc_cache* c, rc_stats_t* o) {
+    if (!c || !o) return RC_ERR_ARG;
+    o->pool_slots = c->pool;
+    o->free_slots = c->n_free;
+    o->caller_slots = c->n_held;
+    o->tree_tokens = c->n_cached;
+    o->nodes = c->n_nodes;
+    o->match_calls = c->match_calls;
+    o->match_tokens = c->match_tokens;
+    o->match_hits = c->match_hits;
+    o->match_hit_tokens = c->match_hit_tokens;
+    o->insert_calls = c->insert_calls;
+    o->insert_new_tokens = c->insert_new_tokens;
+    o->insert_dup_freed = c->insert_dup_freed;
+    o->evicted_nodes = c->evicted_nodes;
+    o->evicted_tokens = c->evicted_tokens;
+    o->pins = c->recs[0].ref;
+    o->clock = (int64_t)c->clock;
+    return RC_OK;
+}
+
+rc_status rc_dump(rc_cache* c, char* buf, int64_t cap, int64_t* needed) {
+    if (!c || !needed || cap < 0 || (cap > 0 && !buf)) return RC_ERR_ARG;
+    std::vector<std::vector<int32_t>> kids(c->recs.size());
+    for (size_t i = 1; i < c->recs.size(); ++i)
+        if (c->recs[i].live) kids[(size_t)c->recs[i].parent].push_back((int32_t)i);
+    for (auto& k : kids)
+        std::sort(k.begin(), k.end(), [&](int32_t a, int32_t b) {
+            return c->tok_arena[(size_t)c->recs[(size_t)a].off] < c->tok_arena[(size_t)c->recs[(size_t)b].off];
+        });
+    std::string s;
+    c->dump_rec(0, kids, s);
+    *needed = (int64_t)s.size();
+    if (cap > 0) {
+        int64_t k = std::min<int64_t>(cap - 1, (int64_t)s.size());
+        std::memcpy(buf, s.data(), (size_t)k);
+        buf[k] = 0;
+    }
+    return RC_OK;
+}
+
+}  // extern "C"

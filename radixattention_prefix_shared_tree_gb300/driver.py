@@ -1,0 +1,304 @@
+"""Request driver over the C-ABI: admission, prefill, decode and finish.
+
+Host side (``Scheduler``): works with any object that has the cache calls of
+``RadixCache`` (the oracle's tree has the same shape, which is how the tests
+replay one trace through both and compare every result).  The rules it
+applies around the cache calls:
+
+* admission runs in ``sched_order`` order and stops at the first request that
+  does not fit, after evicting least-recently-used leaves for it
+  (inference-notes note 49, sections 4 and 5);
+* a request that will decode and whose whole prompt is cached recomputes its
+  last prompt token, so that one new token carries the query; that token's
+  fresh slot is a duplicate that ``rc_insert`` frees;
+* slots for every position the request will ever compute (uncached prompt
+  tail + max_new decode tokens) are taken at admission, so the slot row of a
+  request is complete before its first kernel runs;
+* after prefill the prompt is inserted and stays pinned (concurrent requests
+  can share it); at finish prompt + generated tokens are inserted (note 49,
+  section 2: a finished request's path, outputs included, stays) and the pin
+  is dropped.
+
+Device side (``DeviceEngine``): the KV pool, the slot tables and the kernel
+launches; PyTorch only provides device memory and the stream.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import (RC_ERR_NOMEM, RC_FCFS, RC_LPM, RC_OK, attn_decode, attn_decode_workspace, attn_extend,
+               kv_store, make_attn_desc, make_cascade, make_kv_table, make_pool_desc)
+
+
+@dataclass
+class Request:
+    rid: int
+    tokens: np.ndarray          # prompt followed by the tokens it will generate (int32)
+    prompt_len: int
+    max_new: int
+    node: int = -1              # pinned node
+    matched: int = 0            # cached prefix length found at admission
+    first: int = 0              # first position computed by prefill
+    slots: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))  # one per position
+
+    @property
+    def prompt(self) -> np.ndarray:
+        return self.tokens[:self.prompt_len]
+
+    @property
+    def n_new(self) -> int:
+        return self.prompt_len - self.first
+
+
+class SchedulerError(RuntimeError):
+    pass
+
+
+def _ok(st, what):
+    if st != RC_OK:
+        raise SchedulerError(f"{what} returned {st}")
+
+
+class Scheduler:
+    """Host half of the request lifecycle over a cache object."""
+
+    def __init__(self, cache, log: list | None = None):
+        self.cache = cache
+        self.log = log
+
+    def _rec(self, *item):
+        if self.log is not None:
+            self.log.append(item)
+
+    def admit(self, pending: list, policy: int = RC_LPM, max_batch: int | None = None):
+        """Admit requests in scheduling order; returns (admitted, still pending)."""
+        if not pending:
+            return [], []
+        st, order = self.cache.sched_order(policy, [r.prompt for r in pending])
+        _ok(st, "sched_order")
+        self._rec("order", tuple(int(i) for i in order))
+        admitted, waiting = [], []
+        blocked = False
+        for i in order:
+            r = pending[int(i)]
+            if blocked or (max_batch is not None and len(admitted) >= max_batch):
+                waiting.append(r)
+                continue
+            st, m, mslots, node = self.cache.match(r.prompt, True)
+            _ok(st, "match")
+            first = min(m, r.prompt_len - 1) if r.max_new > 0 else m
+            need = r.prompt_len - first + r.max_new
+            st, new = self.cache.alloc(need)
+            self._rec("match", r.rid, m, node, st)
+            if st == RC_ERR_NOMEM:
+                free = self.cache.stats()["free"]
+                est, freed, evlog = self.cache.evict(need - free)
+                _ok(est, "evict")
+                self._rec("evict", r.rid, need - free, freed, tuple(int(x) for x in evlog))
+                st, new = self.cache.alloc(need)
+            if st != RC_OK:
+                _ok(self.cache.release(node), "release")
+                blocked = True
+                waiting.append(r)
+                self._rec("wait", r.rid)
+                continue
+            r.node, r.matched, r.first = node, m, first
+            r.slots = np.concatenate([mslots[:first], new]).astype(np.int32)
+            self._rec("admit", r.rid, tuple(int(x) for x in new[:4]), len(new))
+            admitted.append(r)
+        return admitted, waiting
+
+    def commit_prompts(self, batch: list):
+        """After prefill: insert each prompt, keep it pinned, drop the admission pin."""
+        for r in batch:
+            L = r.prompt_len
+            st, present, node, canon = self.cache.insert(r.prompt, r.slots[:L], r.max_new > 0)
+            _ok(st, "insert")
+            self._rec("insert", r.rid, present, node)
+            r.slots[:L] = canon
+            _ok(self.cache.release(r.node), "release")
+            r.node = node if r.max_new > 0 else -1
+
+    def finish(self, batch: list):
+        """After decode: insert prompt + generated tokens, unpin."""
+        for r in batch:
+            if r.max_new == 0:
+                continue
+            n = r.prompt_len + r.max_new
+            st, present, node, canon = self.cache.insert(r.tokens[:n], r.slots[:n], False)
+            _ok(st, "insert")
+            self._rec("finish", r.rid, present, node)
+            r.slots[:n] = canon
+            _ok(self.cache.release(r.node), "release")
+            r.node = -1
+
+
+# ------------------------------------------------------------------ cascade
+def plan_cascade(rows: list):
+    """Shared segments of the batch's cached slot rows (a compressed trie).
+
+    rows[b]: slot ids of row b's positions 0..n_b-1 that other rows may share.
+    Returns (segments, private) with segments = [(slots, [row ids])] in the
+    order a depth-first walk meets them, and private[b] = the first position of
+    row b that no other row shares.
+    """
+    B = len(rows)
+    private = np.zeros(B, np.int64)
+    segs = []
+    if B == 0:
+        return segs, private
+    order = sorted(range(B), key=lambda i: rows[i].astype(">i4").tobytes())
+    lcp = np.zeros(max(B - 1, 0), np.int64)
+    for i in range(B - 1):
+        a, b = rows[order[i]], rows[order[i + 1]]
+        n = min(len(a), len(b))
+        ne = np.flatnonzero(a[:n] != b[:n])
+        lcp[i] = ne[0] if ne.size else n
+    stack = [(0, B, 0)]
+    while stack:
+        lo, hi, d = stack.pop()
+        if hi - lo == 1:
+            private[order[lo]] = d
+            continue
+        m = int(lcp[lo:hi - 1].min())
+        if m > d:
+            segs.append((rows[order[lo]][d:m], sorted(order[lo:hi])))
+        parts, s = [], lo
+        for i in range(lo, hi - 1):
+            if lcp[i] == m:
+                parts.append((s, i + 1))
+                s = i + 1
+        parts.append((s, hi))
+        for lo2, hi2 in reversed(parts):
+            stack.append((lo2, hi2, m))
+    return segs, private
+
+
+# ------------------------------------------------------------------- device
+class DeviceEngine:
+    """KV pool + slot tables in HBM and the kernel launches of one batch."""
+
+    def __init__(self, shape, pool_slots: int, device="cuda", table_cap: int = 1 << 22):
+        import torch
+        self.torch = torch
+        self.shape = shape
+        self.device = torch.device(device)
+        dev = self.device
+        if shape.mla:
+            self.pool_k = torch.zeros(pool_slots, shape.head_dim_k, dtype=torch.bfloat16, device=dev)
+            self.pool_v = None
+        else:
+            self.pool_k = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_k, dtype=torch.bfloat16, device=dev)
+            self.pool_v = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_v, dtype=torch.bfloat16, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.pool = make_pool_desc(self.pool_k, self.pool_v, self.err, mla=shape.mla, head_dim_v=shape.head_dim_v)
+        self.desc = make_attn_desc(self.pool, shape.q_heads, shape.scale)
+        self.table = torch.zeros(table_cap, dtype=torch.int32, device=dev)
+        self._ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+
+    def workspace(self, nbytes: int):
+        if self._ws.numel() < nbytes:
+            self._ws = self.torch.empty(int(nbytes * 1.25) + 256, dtype=self.torch.uint8, device=self.device)
+        return self._ws
+
+    def upload_batch(self, batch: list, cascade: bool):
+        """Slot rows of the batch -> device table; returns the batch's device layout."""
+        torch = self.torch
+        lens = np.asarray([len(r.slots) for r in batch], np.int64)
+        starts = np.zeros(len(batch), np.int64)
+        if len(batch) > 1:
+            starts[1:] = np.cumsum(lens[:-1])
+        total = int(lens.sum())
+        if total > self.table.numel():
+            self.table = torch.zeros(total, dtype=torch.int32, device=self.device)
+        flat = np.concatenate([r.slots for r in batch]).astype(np.int32) if batch else np.zeros(0, np.int32)
+        self.table[:total].copy_(torch.from_numpy(flat), non_blocking=False)
+        lay = BatchLayout(self, batch, starts, cascade)
+        return lay
+
+    # -- kernels
+    def store(self, slots_dev, k, v):
+        kv_store(self.pool, slots_dev, k, v)
+
+    def extend(self, lay, q, out, lse=None):
+        kv = lay.extend_table
+        attn_extend(self.desc, q, lay.qo_indptr, kv, lay.batch_size, lay.max_q, out, lse)
+
+    def decode(self, lay, t: int, q, out, lse=None):
+        kv, casc = lay.decode_table(t)
+        ws_bytes = attn_decode_workspace(self.desc, lay.batch_size, kv.max_len, casc)
+        ws = self.workspace(ws_bytes)
+        attn_decode(self.desc, q, kv, lay.batch_size, out, lse, ws, cascade=casc)
+
+
+class BatchLayout:
+    """Device-side index arrays of one admitted batch."""
+
+    def __init__(self, eng: DeviceEngine, batch: list, starts: np.ndarray, cascade: bool):
+        torch = eng.torch
+        dev = eng.device
+        self.eng = eng
+        self.batch = batch
+        self.batch_size = len(batch)
+        B = len(batch)
+        L = np.asarray([r.prompt_len for r in batch], np.int64)
+        first = np.asarray([r.first for r in batch], np.int64)
+        n_new = L - first
+        self.L, self.first, self.starts = L, first, starts
+        self.max_new = max([r.max_new for r in batch], default=0)
+        qo = np.zeros(B + 1, np.int64)
+        qo[1:] = np.cumsum(n_new)
+        self.qo_host = qo
+        self.max_q = int(n_new.max()) if B else 0
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        self.qo_indptr = i32(qo)
+        self.start_dev = i32(starts)
+        self.len_prompt = i32(L)
+        self.extend_table = make_kv_table(eng.table, self.start_dev, self.len_prompt, int(L.max()) if B else 0)
+        # slots of new tokens, in (request, position) order
+        ext = [r.slots[r.first:r.prompt_len] for r in batch]
+        self.extend_slots = i32(np.concatenate(ext) if ext else np.zeros(0, np.int32))
+        # decode: slots of step t for every row, and per-step lengths
+        T = self.max_new
+        if T:
+            dec = np.stack([r.slots[r.prompt_len:r.prompt_len + T] for r in batch], axis=1)  # [T, B]
+            self.decode_slots = i32(dec)
+            lens = (L[None, :] + np.arange(T)[:, None] + 1)
+        else:
+            self.decode_slots = None
+            lens = np.zeros((0, B), np.int64)
+        self.use_cascade = cascade and B > 1
+        self.private = np.zeros(B, np.int64)
+        self.casc = None
+        if self.use_cascade:
+            segs, private = plan_cascade([r.slots[:r.prompt_len] for r in batch])
+            if segs:
+                self.private = private
+                self.segments = segs
+                seg_slots = np.concatenate([s for s, _ in segs]).astype(np.int32)
+                seg_indptr = np.zeros(len(segs) + 1, np.int64)
+                seg_indptr[1:] = np.cumsum([len(s) for s, _ in segs])
+                rows = [rw for _, rw in segs]
+                seg_row_indptr = np.zeros(len(segs) + 1, np.int64)
+                seg_row_indptr[1:] = np.cumsum([len(rw) for rw in rows])
+                seg_rows = np.concatenate([np.asarray(rw, np.int64) for rw in rows])
+                pos_of = [[] for _ in range(B)]
+                for p, b in enumerate(seg_rows):
+                    pos_of[int(b)].append(p)
+                req_indptr = np.zeros(B + 1, np.int64)
+                req_indptr[1:] = np.cumsum([len(x) for x in pos_of])
+                req_pos = np.concatenate([np.asarray(x, np.int64) for x in pos_of]) if len(seg_rows) else np.zeros(0)
+                self._casc_arrays = [i32(seg_slots), i32(seg_indptr), i32(seg_row_indptr), i32(seg_rows),
+                                     i32(req_indptr), i32(req_pos)]
+                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=max(len(rw) for rw in rows))
+            else:
+                self.use_cascade = False
+        self.dec_start = i32(starts + self.private)
+        self.dec_len = i32(lens - self.private[None, :]) if T else None
+        self.dec_max = (lens - self.private[None, :]).max(axis=1) if T else None
+
+    def decode_table(self, t: int):
+        kv = make_kv_table(self.eng.table, self.dec_start, self.dec_len[t], int(self.dec_max[t]))
+        return kv, (self.casc if self.use_cascade else None)

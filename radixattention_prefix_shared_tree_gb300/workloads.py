@@ -1,0 +1,171 @@
+"""Serving loops of the five workloads over the driver.
+
+``Runner.serve`` is one scheduling round of continuous batching: admit (in
+``sched_order`` order, evicting as needed), prefill the admitted batch
+(kv_store of the new tokens, attn_extend), insert the prompts, decode every
+step (kv_store + attn_decode, flat or cascade), insert prompt + outputs and
+unpin.  Without a device engine only the host calls run (used to replay a
+workload through two cache implementations).  The model object supplies
+token sequences and Q/K/V rows; the workload shapes come from the caller.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import RC_LPM
+from .driver import Request, Scheduler
+
+
+def new_request(model, rid: int, prompt, max_new: int) -> Request:
+    toks, hashes = model.sequence(np.asarray(prompt, np.int32), max_new)
+    model.register(rid, hashes)
+    return Request(rid=rid, tokens=toks, prompt_len=len(prompt), max_new=max_new)
+
+
+class Runner:
+    def __init__(self, cache, model, engine=None, policy: int = RC_LPM, cascade: bool = True,
+                 collect: bool = False, prefill_attention: bool = True, log: list | None = None):
+        self.sched = Scheduler(cache, log)
+        self.cache = cache
+        self.model = model
+        self.engine = engine
+        self.policy = policy
+        self.cascade = cascade
+        self.collect = collect
+        self.prefill_attention = prefill_attention
+        self.extend_out = {}   # rid -> (positions, out bf16 [n, Hq, dv], lse [n, Hq])
+        self.decode_out = {}   # rid -> list of (position, out [Hq, dv], lse [Hq])
+        self.next_rid = 0
+
+    def request(self, prompt, max_new: int) -> Request:
+        r = new_request(self.model, self.next_rid, prompt, max_new)
+        self.next_rid += 1
+        return r
+
+    # ------------------------------------------------------------ one round
+    def serve(self, pending: list, max_batch: int | None = None):
+        admitted, waiting = self.sched.admit(pending, self.policy, max_batch)
+        if admitted:
+            if self.engine is not None:
+                self._prefill(admitted)
+            self.sched.commit_prompts(admitted)
+            if self.engine is not None and any(r.max_new for r in admitted):
+                self._decode([r for r in admitted if r.max_new])
+            self.sched.finish(admitted)
+        return admitted, waiting
+
+    def _prefill(self, batch):
+        eng, torch = self.engine, self.engine.torch
+        lay = eng.upload_batch(batch, cascade=False)
+        total = int(lay.qo_host[-1])
+        if total == 0:
+            return
+        inp = self.model.extend_inputs(batch)
+        eng.store(lay.extend_slots, inp["k"], inp["v"])
+        if not self.prefill_attention:
+            return
+        sh = eng.shape
+        out = torch.empty(total, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
+        lse = torch.empty(total, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
+        eng.extend(lay, inp["q"], out, lse)
+        if self.collect:
+            o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+            for i, r in enumerate(batch):
+                a, b = int(lay.qo_host[i]), int(lay.qo_host[i + 1])
+                self.extend_out[r.rid] = (np.arange(r.first, r.prompt_len), o[a:b], l[a:b])
+
+    def _decode(self, batch):
+        eng, torch = self.engine, self.engine.torch
+        lay = eng.upload_batch(batch, cascade=self.cascade)
+        self.last_layout = lay
+        sh = eng.shape
+        B = len(batch)
+        out = torch.empty(B, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
+        lse = torch.empty(B, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
+        for t in range(lay.max_new):
+            inp = self.model.decode_inputs(batch, t)
+            eng.store(lay.decode_slots[t], inp["k"], inp["v"])
+            eng.decode(lay, t, inp["q"], out, lse)
+            if self.collect:
+                o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+                for i, r in enumerate(batch):
+                    self.decode_out.setdefault(r.rid, []).append((r.prompt_len + t, o[i].copy(), l[i].copy()))
+
+
+# ------------------------------------------------------------------ workloads
+def run_tiny(runner: Runner, trace):
+    """Requests one at a time: prefill, decode max_new tokens, finish."""
+    reqs = []
+    for p in trace.prompts:
+        r = runner.request(p, trace.max_new)
+        admitted, waiting = runner.serve([r])
+        assert admitted and not waiting
+        reqs.append(r)
+    return reqs
+
+
+def run_cyclic(runner: Runner, prefixes, order):
+    """Prefill-only requests one at a time; returns the number of hits."""
+    hits = 0
+    for p in order:
+        r = runner.request(prefixes[p], 0)
+        admitted, _ = runner.serve([r])
+        assert admitted
+        hits += r.matched > 0
+    return hits
+
+
+def run_few_shot(runner: Runner, trace, warm: bool = True):
+    """The shared examples once (prefill only), then all questions in one batch."""
+    if warm:
+        runner.serve([runner.request(trace.warm, 0)])
+    reqs = [runner.request(trace.prompt(i), trace.max_new) for i in range(len(trace.questions))]
+    admitted, waiting = runner.serve(reqs)
+    assert not waiting
+    return admitted
+
+
+def run_chat(runner: Runner, trace, max_rounds: int = 10_000):
+    """Sessions grow turn by turn; each round admits the ready turns that fit."""
+    n_sess = len(trace.user_turns)
+    history = [np.zeros(0, np.int32) for _ in range(n_sess)]
+    turn = [0] * n_sess
+    pending = {}
+    for s in range(n_sess):
+        r = runner.request(trace.user_turns[s][0], trace.max_new)
+        r.session = s
+        pending[s] = r
+    rounds = 0
+    served = []
+    while pending and rounds < max_rounds:
+        rounds += 1
+        queue = [pending[s] for s in sorted(pending)]
+        admitted, waiting = runner.serve(queue, trace.max_batch)
+        if not admitted:
+            raise RuntimeError("no progress: pool too small for any waiting turn")
+        for r in admitted:
+            s = r.session
+            served.append(r)
+            history[s] = r.tokens[:r.prompt_len + r.max_new]
+            turn[s] += 1
+            del pending[s]
+            if turn[s] < len(trace.user_turns[s]):
+                nr = runner.request(np.concatenate([history[s], trace.user_turns[s][turn[s]]]), trace.max_new)
+                nr.session = s
+                pending[s] = nr
+    return served, rounds
+
+
+def run_agent(runner: Runner, trace):
+    """Root prompt, then each level of branches (prefill only), then all leaves decode."""
+    runner.serve([runner.request(trace.root, 0)])
+    depth = len(trace.leaves[0])
+    for lvl in range(1, depth):
+        paths = sorted({leaf[:lvl] for leaf in trace.leaves})
+        reqs = [runner.request(trace.prompt(p), 0) for p in paths]
+        admitted, waiting = runner.serve(reqs)
+        assert not waiting
+    reqs = [runner.request(trace.prompt(leaf), trace.max_new) for leaf in trace.leaves]
+    admitted, waiting = runner.serve(reqs)
+    assert not waiting
+    return admitted

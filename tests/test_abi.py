@@ -1,0 +1,69 @@
+"""The C-ABI library loads and exports every function include/*.h declares;
+host-only checks of the device entry points' argument validation (no GPU work
+is launched: every call here fails its checks before any CUDA call)."""
+from __future__ import annotations
+
+import ctypes as C
+import glob
+import os
+import re
+import subprocess
+
+import radixattention_prefix_shared_tree_gb300 as ra
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:rc_status|void|const char\s*\*)\s*(\w+)\s*\(", src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("rc_create", "rc_destroy", "rc_match_prefix", "rc_insert", "rc_release", "rc_evict", "rc_alloc",
+              "rc_free", "sched_order", "rc_stats", "rc_dump", "kv_store", "attn_decode", "attn_extend",
+              "attn_decode_workspace", "attn_extend_workspace", "rc_sync", "rc_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(built):
+    lib = C.CDLL(ra.library_path())
+    out = subprocess.run(["nm", "-D", "--defined-only", ra.library_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for n in declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+    assert set(ra.SIGNATURES) <= declared_functions()
+
+
+def test_strerror_and_argument_checks(built):
+    assert ra.rc_strerror(ra.RC_OK) == "ok"
+    assert "free slots" in ra.rc_strerror(ra.RC_ERR_NOMEM)
+    L = ra.lib()
+    # null descriptors are rejected on the host, before any CUDA call
+    assert L.kv_store(None, None, None, None, 0, None, None, None) == ra.RC_ERR_ARG
+    assert L.attn_decode(None, None, None, 0, None, None, None, None, 0, None) == ra.RC_ERR_ARG
+    assert L.attn_extend(None, None, None, None, 0, 0, None, None, None, 0, None) == ra.RC_ERR_ARG
+    n = C.c_size_t(0)
+    assert L.attn_decode_workspace(None, 1, 1, None, C.byref(n)) == ra.RC_ERR_ARG
+    h = C.c_void_p()
+    assert L.rc_create(-1, C.byref(h)) == ra.RC_ERR_ARG
+    assert L.rc_create(10, None) == ra.RC_ERR_ARG
+
+
+def test_host_calls_reject_bad_arguments(built):
+    c = ra.RadixCache(16)
+    L = ra.lib()
+    m, node = C.c_int64(), C.c_int64()
+    assert L.rc_match_prefix(c.handle, None, -1, 0, C.byref(m), None, C.byref(node)) == ra.RC_ERR_ARG
+    assert c.alloc(17)[0] == ra.RC_ERR_NOMEM
+    assert c.release(999) == ra.RC_ERR_STATE
+    assert c.free([16]) == ra.RC_ERR_ARG
+    assert c.sched_order(7, [[1]])[0] == ra.RC_ERR_ARG
+    assert c.evict(-3)[0] == ra.RC_ERR_ARG

@@ -1,0 +1,245 @@
+"""CUDA kernels through the C-ABI against the oracle, element by element.
+
+Sizes span several 64-key tiles and split chunks with ragged tails; slot
+tables are random permutations of the pool so every gather is scattered.
+Bar (attention): max |gpu - oracle| <= 1e-2 and mean |gpu - oracle| <= 1e-3 on
+the bf16 outputs, |lse - oracle lse| <= 2e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import radixattention_prefix_shared_tree_gb300 as ra
+from radixattention_prefix_shared_tree_gb300.driver import plan_cascade
+from synth import hashgen as hg
+from synth import native
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 2e-3
+
+
+def bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def rand_bf16(gen, shape, dev):
+    return torch.randn(*shape, generator=gen, dtype=torch.float32).to(torch.bfloat16).to(dev)
+
+
+def check(out_bits, ref, lse=None, ref_lse=None):
+    got = hg.bf16_bits_to_f32(out_bits).astype(np.float64)
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_ABS, f"max abs {err.max()}"
+    assert err.mean() <= MEAN_ABS, f"mean abs {err.mean()}"
+    if lse is not None:
+        le = np.abs(lse.astype(np.float64) - ref_lse)
+        assert le.max() <= LSE_ABS, f"lse max abs {le.max()}"
+
+
+class Pool:
+    def __init__(self, n_slots, Hkv, D, dev, seed):
+        g = torch.Generator().manual_seed(seed)
+        self.k = rand_bf16(g, (n_slots, Hkv, D), dev)
+        self.v = rand_bf16(g, (n_slots, Hkv, D), dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.desc = ra.make_pool_desc(self.k, self.v, self.err)
+        self.kb, self.vb = bits(self.k), bits(self.v)
+
+
+def test_synth_gpu_generator_equals_numpy(cuda):
+    h = hg.prefix_hashes(np.arange(300, dtype=np.int32) * 7 % 1000, 11)
+    dh = torch.from_numpy(h.view(np.int64)).to(cuda)
+    for kind, heads, dims in ((hg.KIND_K, 8, 128), (hg.KIND_Q, 32, 128), (hg.KIND_K, 1, 576)):
+        out = torch.empty(len(h), heads * dims, dtype=torch.bfloat16, device=cuda)
+        native.gen_values_gpu(dh, kind, heads, dims, out)
+        ref = hg.gen_values(h, kind, heads, dims).reshape(len(h), -1)
+        assert (bits(out) == ref).all()
+
+
+def test_kv_store_scatter_and_append(cuda):
+    n_slots, Hkv, D = 500, 8, 128
+    pool = Pool(n_slots, Hkv, D, cuda, 0)
+    g = torch.Generator().manual_seed(1)
+    n = 77
+    slots = torch.randperm(n_slots, generator=g)[:n].to(torch.int32).to(cuda)
+    k = rand_bf16(g, (n, Hkv, D), cuda)
+    v = rand_bf16(g, (n, Hkv, D), cuda)
+    table = torch.full((300,), -1, dtype=torch.int32, device=cuda)
+    pos = torch.randperm(300, generator=g)[:n].to(torch.int32).to(cuda)
+    ra.kv_store(pool.desc, slots, k, v, table, pos)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    s = slots.long()
+    assert torch.equal(pool.k[s], k) and torch.equal(pool.v[s], v)
+    assert torch.equal(table[pos.long()], slots)
+    # a slot outside the pool is skipped and reported; the rest is written
+    bad = slots.clone()
+    bad[3] = n_slots + 5
+    k2 = rand_bf16(g, (n, Hkv, D), cuda)
+    ra.kv_store(pool.desc, bad, k2, v)
+    assert ra.rc_sync(pool.err) == ra.RC_ERR_DEVICE
+    assert torch.equal(pool.k[s[:3]], k2[:3]) and torch.equal(pool.k[s[3]], k[3])
+    assert ra.rc_sync(pool.err) == ra.RC_OK   # the error word was cleared
+
+
+def _tables(lens, n_slots, seed, dev):
+    rng = np.random.default_rng(seed)
+    rows = [rng.choice(n_slots, size=L, replace=False).astype(np.int32) for L in lens]
+    starts = np.zeros(len(lens), np.int64)
+    starts[1:] = np.cumsum(lens)[:-1]
+    flat = np.concatenate(rows)
+    t = torch.from_numpy(flat).to(dev)
+    st = torch.from_numpy(starts.astype(np.int32)).to(dev)
+    ln = torch.from_numpy(np.asarray(lens, np.int32)).to(dev)
+    return rows, t, st, ln
+
+
+def _oracle_rows(pool, rows, q_bits, ctx_of_row, Hq, Hkv, D, scale):
+    """Oracle over gathered K/V: query row i sees the first ctx_of_row[i] keys of rows[i]."""
+    ks = np.concatenate([pool.kb[r] for r in rows])
+    vs = np.concatenate([pool.vb[r] for r in rows])
+    offs = np.zeros(len(rows), np.int64)
+    offs[1:] = np.cumsum([len(r) for r in rows])[:-1]
+    return oracle.attention(q_bits, ks, vs, offs, np.asarray(ctx_of_row, np.int64), Hq, Hkv, D, D, scale)
+
+
+DECODE_CASES = [
+    # Hq, Hkv, D, lens
+    (4, 4, 64, [1, 2, 63, 64, 65, 130]),
+    (32, 8, 128, [1, 17, 64, 200, 1000, 2500, 4097]),
+    (64, 8, 128, [5, 129, 3000]),
+    (16, 8, 128, [700, 33]),
+    (8, 8, 128, [1, 1024]),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,lens", DECODE_CASES)
+def test_decode_flat_vs_oracle(cuda, Hq, Hkv, D, lens):
+    n_slots = 6000
+    pool = Pool(n_slots, Hkv, D, cuda, Hq + D)
+    rows, table, start, length = _tables(lens, n_slots, 3, cuda)
+    g = torch.Generator().manual_seed(2)
+    B = len(lens)
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    ws = torch.empty(ra.attn_decode_workspace(desc, B, max(lens)), dtype=torch.uint8, device=cuda)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_decode(desc, q, kv, B, out, lse, ws)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    ref, ref_lse = _oracle_rows(pool, rows, bits(q), lens, Hq, Hkv, D, scale)
+    check(bits(out), ref, lse.cpu().numpy(), ref_lse)
+
+
+EXTEND_CASES = [
+    # Hq, Hkv, D, (prefix, new) per request
+    (4, 4, 64, [(0, 1), (32, 9), (0, 70), (5, 64)]),
+    (32, 8, 128, [(1792, 40), (0, 17), (100, 130), (1792, 64), (0, 1)]),
+    (64, 8, 128, [(2048, 33), (300, 8), (0, 200)]),
+    (16, 8, 128, [(63, 65)]),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,reqs", EXTEND_CASES)
+def test_extend_vs_oracle(cuda, Hq, Hkv, D, reqs):
+    n_slots = 8000
+    pool = Pool(n_slots, Hkv, D, cuda, 7 * Hq + D)
+    lens = [p + n for p, n in reqs]
+    rows, table, start, length = _tables(lens, n_slots, 5, cuda)
+    g = torch.Generator().manual_seed(4)
+    ns = [n for _, n in reqs]
+    T = sum(ns)
+    q = rand_bf16(g, (T, Hq, D), cuda)
+    qo = torch.tensor(np.concatenate([[0], np.cumsum(ns)]).astype(np.int32), device=cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty(T, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_extend(desc, q, qo, kv, len(reqs), max(ns), out, lse)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    row_of, ctx = [], []
+    for b, (p, n) in enumerate(reqs):
+        for i in range(n):
+            row_of.append(rows[b])
+            ctx.append(p + i + 1)
+    ref, ref_lse = _oracle_rows(pool, row_of, bits(q), ctx, Hq, Hkv, D, scale)
+    check(bits(out), ref, lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (64, 8, 128), (4, 4, 64)])
+def test_cascade_equals_flat_and_oracle(cuda, Hq, Hkv, D):
+    """A tree of shared prefixes: root shared by all rows, two mid segments,
+    private tails; cascade decode == flat decode == oracle."""
+    n_slots = 20000
+    pool = Pool(n_slots, Hkv, D, cuda, 99 + Hq)
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(n_slots).astype(np.int32)
+    root, mids = perm[:700], [perm[700:900], perm[900:1157]]
+    off = 1157
+    rows = []
+    for b in range(12):
+        tail_len = int(rng.integers(1, 150))
+        tail = perm[off:off + tail_len]
+        off += tail_len
+        mid = mids[b % 2] if b < 10 else np.zeros(0, np.int32)
+        rows.append(np.concatenate([root, mid, tail]).astype(np.int32))
+    B = len(rows)
+    lens = [len(r) for r in rows]
+    _, table, start, length = _tables(lens, n_slots, 0, cuda)
+    table.copy_(torch.from_numpy(np.concatenate(rows)).to(cuda))
+    g = torch.Generator().manual_seed(6)
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    # flat
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    ws = torch.empty(ra.attn_decode_workspace(desc, B, max(lens)), dtype=torch.uint8, device=cuda)
+    flat = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+    flat_lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_decode(desc, q, kv, B, flat, flat_lse, ws)
+    # cascade from the shared structure of the rows (tails are private)
+    prefix_rows = [r[:len(r) - 1] for r in rows]
+    segs, private = plan_cascade(prefix_rows)
+    assert len(segs) == 3
+    seg_slots = np.concatenate([s for s, _ in segs]).astype(np.int32)
+    seg_indptr = np.concatenate([[0], np.cumsum([len(s) for s, _ in segs])]).astype(np.int32)
+    seg_rows = np.concatenate([np.asarray(r, np.int32) for _, r in segs])
+    seg_row_indptr = np.concatenate([[0], np.cumsum([len(r) for _, r in segs])]).astype(np.int32)
+    pos_of = [[p for p, b in enumerate(seg_rows) if b == bb] for bb in range(B)]
+    req_indptr = np.concatenate([[0], np.cumsum([len(x) for x in pos_of])]).astype(np.int32)
+    req_pos = np.concatenate([np.asarray(x, np.int32) for x in pos_of])
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(cuda)
+    arrs = [T(seg_slots), T(seg_indptr), T(seg_row_indptr), T(seg_rows), T(req_indptr), T(req_pos)]
+    casc = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs))
+    pstart = T(start.cpu().numpy() + private)
+    plen = T(np.asarray(lens) - private)
+    kv2 = ra.make_kv_table(table, pstart, plen, int((np.asarray(lens) - private).max()))
+    ws2 = torch.empty(ra.attn_decode_workspace(desc, B, kv2.max_len, casc), dtype=torch.uint8, device=cuda)
+    cout = torch.empty_like(flat)
+    clse = torch.empty_like(flat_lse)
+    ra.attn_decode(desc, q, kv2, B, cout, clse, ws2, cascade=casc)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    ref, ref_lse = _oracle_rows(pool, rows, bits(q), lens, Hq, Hkv, D, scale)
+    check(bits(flat), ref, flat_lse.cpu().numpy(), ref_lse)
+    check(bits(cout), ref, clse.cpu().numpy(), ref_lse)
+    d = np.abs(hg.bf16_bits_to_f32(bits(cout)).astype(np.float64) - hg.bf16_bits_to_f32(bits(flat)))
+    assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS
+
+
+def test_decode_reports_len_above_max_len(cuda):
+    """A row longer than the promised max_len is reported, not read past."""
+    pool = Pool(300, 8, 128, cuda, 1)
+    rows, table, start, length = _tables([200, 250], 300, 1, cuda)
+    q = rand_bf16(torch.Generator().manual_seed(0), (2, 32, 128), cuda)
+    desc = ra.make_attn_desc(pool.desc, 32, 0.088)
+    kv = ra.make_kv_table(table, start, length, 100)
+    ws = torch.empty(ra.attn_decode_workspace(desc, 2, 100), dtype=torch.uint8, device=cuda)
+    out = torch.empty(2, 32, 128, dtype=torch.bfloat16, device=cuda)
+    ra.attn_decode(desc, q, kv, 2, out, None, ws)
+    assert ra.rc_sync(pool.err) == ra.RC_ERR_DEVICE

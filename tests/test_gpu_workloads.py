@@ -1,0 +1,162 @@
+"""Workloads end to end on the GPU through the C-ABI, against the oracle.
+
+The oracle side never sees the pool or the tree: for a request it regenerates
+K/V of every position of the request's own token sequence from the prefix
+hash (the cache-disabled definition) and computes attention from them.  So a
+wrong match, a wrong slot, a lost duplicate or a bad eviction shows up as a
+numeric mismatch.  Hit counts and slot indices are compared bit for bit with
+the oracle tree running the same trace.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import radixattention_prefix_shared_tree_gb300 as ra
+from radixattention_prefix_shared_tree_gb300 import workloads as wl
+from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
+from synth import hashgen as hg
+from synth import traces
+from synth.model import SynthModel
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 2e-3
+
+
+def oracle_positions(shape, hashes, positions):
+    """Oracle attention for query positions of one request (keys 0..pos)."""
+    n = int(max(positions)) + 1
+    kb = hg.gen_values(hashes[:n], hg.KIND_K, shape.kv_heads, shape.head_dim_k)
+    vb = None if shape.mla else hg.gen_values(hashes[:n], hg.KIND_V, shape.kv_heads, shape.head_dim_v)
+    qb = hg.gen_values(hashes[np.asarray(positions)], hg.KIND_Q, shape.q_heads, shape.head_dim_k)
+    return oracle.attention(qb, kb, vb, np.zeros(len(positions), np.int64), np.asarray(positions, np.int64) + 1,
+                            shape.q_heads, shape.kv_heads, shape.head_dim_k, shape.head_dim_v, shape.scale,
+                            latent=shape.mla)
+
+
+def compare(out_bits, lse, ref, ref_lse, stats):
+    got = hg.bf16_bits_to_f32(out_bits).astype(np.float64)
+    err = np.abs(got - ref)
+    stats["max"] = max(stats.get("max", 0.0), float(err.max()))
+    stats["sum"] = stats.get("sum", 0.0) + float(err.sum())
+    stats["n"] = stats.get("n", 0) + err.size
+    assert err.max() <= MAX_ABS
+    assert np.abs(lse.astype(np.float64) - ref_lse).max() <= LSE_ABS
+
+
+def run(trace, runner_fn, pool, cuda, cascade=True, policy=ra.RC_LPM, cache_cls=ra.RadixCache, **kw):
+    model = SynthModel(trace.shape, trace.seed, trace.vocab, device=cuda)
+    eng = DeviceEngine(trace.shape, pool, device=cuda)
+    cache = cache_cls(pool)
+    log = []
+    runner = wl.Runner(cache, model, eng, policy=policy, cascade=cascade, collect=True, log=log)
+    res = runner_fn(runner, trace, **kw)
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+    return runner, model, cache, log, res
+
+
+def check_requests(runner, model, rids, shape, stats, max_decode_steps=None):
+    for rid in rids:
+        h = model.hashes(rid)
+        if rid in runner.extend_out:
+            pos, o, l = runner.extend_out[rid]
+            ref, ref_l = oracle_positions(shape, h, pos)
+            compare(o, l, ref, ref_l, stats)
+        dec = runner.decode_out.get(rid, [])
+        if max_decode_steps is not None:
+            dec = [d for i, d in enumerate(dec) if i in max_decode_steps]
+        if dec:
+            pos = [p for p, _, _ in dec]
+            ref, ref_l = oracle_positions(shape, h, pos)
+            compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]), ref, ref_l, stats)
+
+
+def test_tiny_config_all_outputs_vs_oracle(cuda):
+    tr = traces.tiny()
+    runner, model, cache, log, reqs = run(tr, wl.run_tiny, tr.pool_slots, cuda)
+    stats = {}
+    check_requests(runner, model, [r.rid for r in reqs], tr.shape, stats)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS
+    # the same trace through the oracle tree: identical host results
+    olog = []
+    orunner = wl.Runner(oracle.OracleTree(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"),
+                        log=olog)
+    wl.run_tiny(orunner, tr)
+    assert olog == log
+
+
+def test_few_shot_reduced_cascade_and_flat(cuda):
+    tr = traces.few_shot(n_questions=48, max_new=6)
+    stats = {}
+    outs = {}
+    for cascade in (True, False):
+        runner, model, cache, log, reqs = run(tr, wl.run_few_shot, 1 << 16, cuda, cascade=cascade)
+        if cascade:
+            assert runner.last_layout.use_cascade and len(runner.last_layout.segments) == 1
+        check_requests(runner, model, [r.rid for r in reqs[::7]], tr.shape, stats)
+        outs[cascade] = {rid: np.stack([o for _, o, _ in d]) for rid, d in runner.decode_out.items()}
+        assert cache.stats()["match_hit_tokens"] == 48 * len(tr.warm)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS
+    for rid in outs[True]:
+        a = hg.bf16_bits_to_f32(outs[True][rid]).astype(np.float64)
+        b = hg.bf16_bits_to_f32(outs[False][rid]).astype(np.float64)
+        assert np.abs(a - b).max() <= MAX_ABS
+
+
+def test_cache_on_equals_cache_off_recompute(cuda):
+    """With the cache off every request computes its whole prompt; the outputs
+    of the shared-prefix path must agree within the same bound."""
+    tr = traces.few_shot(n_questions=24, max_new=4)
+    runner_on, *_ = run(tr, wl.run_few_shot, 1 << 15, cuda)
+
+    class NoCache:
+        """Every lookup misses: a fresh tree per request."""
+
+        def __init__(self, pool):
+            self.pool = pool
+            self.inner = ra.RadixCache(pool)
+
+        def __getattr__(self, name):
+            return getattr(self.inner, name)
+
+        def match(self, tokens, pin):
+            st, m, s, node = self.inner.match(tokens[:0], pin)
+            return st, 0, s[:0], node
+
+        def insert(self, tokens, slots, pin):
+            st, present, node, canon = self.inner.insert(tokens[:0], slots[:0], pin)
+            # keep every slot private: give them back at finish through free()
+            return st, 0, node, np.asarray(slots, np.int32)
+
+    model = SynthModel(tr.shape, tr.seed, tr.vocab, device=cuda)
+    eng = DeviceEngine(tr.shape, 1 << 17, device=cuda)
+    off = wl.Runner(NoCache(1 << 17), model, eng, cascade=False, collect=True)
+    wl.run_few_shot(off, tr, warm=False)
+    for rid_on, rid_off in zip(sorted(runner_on.decode_out)[:24], sorted(off.decode_out)[:24]):
+        a = np.stack([o for _, o, _ in runner_on.decode_out[rid_on]])
+        b = np.stack([o for _, o, _ in off.decode_out[rid_off]])
+        d = np.abs(hg.bf16_bits_to_f32(a).astype(np.float64) - hg.bf16_bits_to_f32(b))
+        assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS
+
+
+def test_agent_tree_cascade_vs_oracle(cuda):
+    tr = traces.agent_tree(root_len=512, branch_len=64, max_new=5)
+    runner, model, cache, log, reqs = run(tr, wl.run_agent, 8192, cuda, cascade=True)
+    lay = runner.last_layout
+    assert lay.use_cascade and len(lay.segments) == 1 + 4 + 16
+    stats = {}
+    check_requests(runner, model, [r.rid for r in reqs[::9]], tr.shape, stats)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS
+
+
+def test_chat_reduced_with_eviction_vs_oracle(cuda):
+    tr = traces.chat(n_sessions=16, n_turns=4, umin=32, umax=128, max_new=8)
+    tr.max_batch = 6
+    runner, model, cache, log, (served, rounds) = run(tr, wl.run_chat, tr.pool_slots, cuda)
+    assert cache.stats()["evicted_nodes"] > 0
+    stats = {}
+    check_requests(runner, model, [r.rid for r in served[::5]], tr.shape, stats)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS

@@ -1,0 +1,130 @@
+"""Host half of the product library against the oracle, bit for bit.
+
+The same trace of calls runs through both; every returned value (status,
+matched length, slot arrays, node ids, eviction logs, orders, statistics)
+and the full tree dump must be identical.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import radixattention_prefix_shared_tree_gb300 as ra
+from radixattention_prefix_shared_tree_gb300 import workloads as wl
+from synth import traces
+from synth.model import SynthModel
+from tests import scenarios as sc
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("vocab,pool", [(3, 24), (5, 64), (50, 200)])
+def test_random_traces_bit_exact(built, seed, vocab, pool):
+    a, b = oracle.OracleTree(pool), ra.RadixCache(pool)
+    la, lb = [], []
+    ra_rng, rb_rng = np.random.default_rng(seed), np.random.default_rng(seed)
+    sc.random_trace(a, ra_rng, 250, vocab=vocab, log=la)
+    sc.random_trace(b, rb_rng, 250, vocab=vocab, log=lb)
+    assert len(la) == len(lb)
+    for x, y in zip(la, lb):
+        assert x == y
+    assert a.dump() == b.dump()
+
+
+def test_dump_after_every_op(built):
+    rng = np.random.default_rng(77)
+    a, b = oracle.OracleTree(30), ra.RadixCache(30)
+    for i in range(200):
+        la, lb = [], []
+        s = int(rng.integers(0, 1 << 30))
+        sc.random_trace(a, np.random.default_rng(s), 1, vocab=3, log=la)
+        sc.random_trace(b, np.random.default_rng(s), 1, vocab=3, log=lb)
+        assert la == lb
+        assert a.dump() == b.dump(), f"op {i}"
+
+
+@pytest.mark.parametrize("grouped", [False, True])
+def test_cyclic_trace_same_log(built, grouped):
+    prefixes = traces.cyclic_prefixes(5, 64)
+    order = traces.cyclic_order(5, 2, grouped)
+    logs = []
+    for make in (oracle.OracleTree, ra.RadixCache):
+        t = make(256)
+        log = []
+        for p in order:
+            sc.serve_prefill(t, prefixes[p], log)
+        logs.append((log, t.dump()))
+    assert logs[0] == logs[1]
+    hits = sum(1 for e in logs[0][0] if e[1] > 0)
+    assert hits == (5 if grouped else 0)
+
+
+def _host_run(make_cache, trace_fn, runner_fn, seed, vocab, shape, pool, policy=ra.RC_LPM):
+    cache = make_cache(pool)
+    log = []
+    model = SynthModel(shape, seed, vocab, device="cpu")
+    runner = wl.Runner(cache, model, engine=None, policy=policy, log=log)
+    res = runner_fn(runner, trace_fn())
+    return log, cache.dump(), cache.stats(), res
+
+
+def test_tiny_workload_host_trace(built):
+    tr = traces.tiny()
+    outs = [_host_run(m, traces.tiny, wl.run_tiny, tr.seed, tr.vocab, tr.shape, tr.pool_slots)
+            for m in (oracle.OracleTree, ra.RadixCache)]
+    assert outs[0][:3] == outs[1][:3]
+    st = outs[1][2]
+    # every request after the first finds the 32-token system prompt
+    assert st["match_hits"] == len(tr.prompts) - 1
+
+
+@pytest.mark.parametrize("policy", [ra.RC_LPM, ra.RC_FCFS])
+def test_few_shot_workload_host_trace(built, policy):
+    small = lambda: traces.few_shot(n_questions=64, max_new=16)
+    tr = small()
+    outs = [_host_run(m, small, wl.run_few_shot, tr.seed, tr.vocab, tr.shape, 1 << 16, policy)
+            for m in (oracle.OracleTree, ra.RadixCache)]
+    assert outs[0][:3] == outs[1][:3]
+    st = outs[1][2]
+    assert st["match_hit_tokens"] == 64 * len(tr.warm)
+
+
+def test_chat_workload_host_trace_with_eviction(built):
+    small = lambda: traces.chat(n_sessions=24, n_turns=5, umin=16, umax=64, max_new=16)
+    tr = small()
+    tr.max_batch = 8
+    outs = []
+    for make in (oracle.OracleTree, ra.RadixCache):
+        cache = make(tr.pool_slots)
+        log = []
+        model = SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu")
+        runner = wl.Runner(cache, model, log=log)
+        served, rounds = wl.run_chat(runner, tr)
+        outs.append((log, cache.dump(), cache.stats(), rounds))
+    assert outs[0] == outs[1]
+    st = outs[1][2]
+    assert st["evicted_nodes"] > 0          # the pool holds 75% of the working set
+    assert st["match_hits"] > 0
+
+
+def test_agent_tree_host_trace(built):
+    small = lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8)
+    tr = small()
+    outs = [_host_run(m, small, wl.run_agent, tr.seed, tr.vocab, tr.shape, 4096)
+            for m in (oracle.OracleTree, ra.RadixCache)]
+    assert outs[0][:3] == outs[1][:3]
+
+
+def test_full_chat_host_trace_bit_exact(built):
+    """The chat workload at full size (256 sessions x 8 turns, pool = 75% of
+    the working set): eviction log, hits and final tree identical."""
+    tr = traces.chat()
+    outs = []
+    for make in (oracle.OracleTree, ra.RadixCache):
+        cache = make(tr.pool_slots)
+        log = []
+        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=log)
+        served, rounds = wl.run_chat(runner, tr)
+        outs.append((log, cache.stats(), rounds))
+    assert outs[0] == outs[1]
+    assert outs[1][1]["evicted_tokens"] > 0
