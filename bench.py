@@ -1,0 +1,497 @@
+"""Benchmark: prefix-shared serving step on the few-shot workload.
+
+Workload (one step): a batch of 256 distinct questions of 32..64 tokens behind
+a cached 1792-token prefix (512-token system prompt + 5 x 256-token examples),
+GQA 32 query / 8 KV heads, head_dim 128, bf16, KV pool of 2^21 slots.  One
+step is the whole hot path over that batch: sched_order (longest prefix
+first), rc_match_prefix + pin, rc_alloc, slot tables to the device, kv_store
++ attn_extend of the questions, rc_insert of the prompts, 128 decode steps
+(kv_store + cascade attn_decode), rc_insert of prompt + outputs and
+rc_release.  Every step serves a new batch of questions (inputs already in
+HBM, ~0.55 GB per step, larger than L2).
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefix-shared decode attn tokens/s; HBM GB/s vs ~8 TB/s peak; prefix hit rate"
+UNIT = "tokens/s"
+N_QUESTIONS, MAX_NEW = 256, 128
+WARM_LEN = 512 + 5 * 256
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--policy", default="lpm", choices=["lpm", "fcfs"])
+    ap.add_argument("--no-cascade", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
+    ap.add_argument("--questions", type=int, default=N_QUESTIONS)
+    ap.add_argument("--max-new", type=int, default=MAX_NEW)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ replay model
+class ReplayModel:
+    """The synthetic model with every step's Q/K/V rows generated ahead of time
+    in the order the batch will be served (arrival order: every question
+    matches the same cached prefix, so longest-prefix-first keeps arrival)."""
+
+    def __init__(self, base, torch):
+        self.base = base
+        self.torch = torch
+        self.ready = {}          # tuple(rids) -> dict
+        self.host = None         # e2e: pinned host copies, moved to the device on use
+        self.h2d_bytes = 0
+
+    def sequence(self, prompt, max_new):
+        return self.base.sequence(prompt, max_new)
+
+    def register(self, rid, hashes):
+        self.base.register(rid, hashes)
+
+    def hashes(self, rid):
+        return self.base.hashes(rid)
+
+    def prepare(self, reqs, first: int):
+        torch = self.torch
+        ext_h = np.concatenate([self.base.hashes(r.rid)[first:r.prompt_len] for r in reqs])
+        T = reqs[0].max_new
+        dec_h = np.stack([self.base.hashes(r.rid)[r.prompt_len:r.prompt_len + T] for r in reqs], axis=1)
+        ext = self.base.rows(ext_h)
+        dec = self.base.rows(dec_h.reshape(-1))
+        B = len(reqs)
+        entry = {"ext": ext, "dec": {k: (v.view(T, B, *v.shape[1:]) if v is not None else None)
+                                     for k, v in dec.items()},
+                 "first": first}
+        self.ready[tuple(r.rid for r in reqs)] = entry
+        return entry
+
+    def to_host(self, key):
+        """e2e: keep this step's inputs in pinned host memory only."""
+        e = self.ready[key]
+        pin = lambda t: t.cpu().pin_memory() if t is not None else None
+        e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()},
+                     "dec": {k: pin(v) for k, v in e["dec"].items()}}
+        e["ext"] = {k: (torch_empty_like(self.torch, v)) for k, v in e["ext"].items()}
+        e["dec_dev"] = {k: (torch_empty_like(self.torch, v[0]) if v is not None else None)
+                        for k, v in e["dec"].items()}
+        e["dec"] = None
+
+    def _entry(self, batch):
+        key = tuple(r.rid for r in batch)
+        e = self.ready.get(key)
+        if e is None or any(r.first != e["first"] for r in batch):
+            raise RuntimeError("batch differs from the prepared one (order or cached prefix)")
+        return e
+
+    def extend_inputs(self, batch):
+        e = self._entry(batch)
+        if "host" in e:
+            for k, v in e["ext"].items():
+                if v is not None:
+                    v.copy_(e["host"]["ext"][k], non_blocking=True)
+                    self.h2d_bytes += v.numel() * v.element_size()
+        return e["ext"]
+
+    def decode_inputs(self, batch, t):
+        e = self._entry(batch)
+        if "host" in e:
+            out = {}
+            for k, v in e["dec_dev"].items():
+                if v is not None:
+                    v.copy_(e["host"]["dec"][k][t], non_blocking=True)
+                    self.h2d_bytes += v.numel() * v.element_size()
+                out[k] = v
+            return out
+        return {k: (v[t] if v is not None else None) for k, v in e["dec"].items()}
+
+
+def torch_empty_like(torch, t):
+    return None if t is None else torch.empty_like(t)
+
+
+# -------------------------------------------------------------- algorithmic
+def decode_bytes(lay, t, shape):
+    """Unique K/V rows touched (shared segments once) x row bytes + indices + Q + O."""
+    R = 2 * shape.kv_heads * shape.head_dim_k * 2
+    L = lay.L + t + 1
+    tail = (L - lay.private).sum()
+    seg = sum(len(s) for s, _ in lay.segments) if lay.use_cascade else 0
+    B = lay.batch_size
+    qo = B * shape.q_heads * (shape.head_dim_k + shape.head_dim_v) * 2
+    return int((seg + tail) * R + (seg + tail) * 4 + qo), int(L.sum() * R)
+
+
+def extend_flops(lay, shape):
+    tot = 0
+    for P, n in zip(lay.first, lay.L - lay.first):
+        i = np.arange(n)
+        tot += int((4 * shape.head_dim_k * shape.q_heads * (P + i + 1)).sum())
+    return tot
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
+    """The oracle as it stands, on a bounded sample of one step, scaled to the
+    metric's unit: host tree calls of a whole step (full), attention of sampled
+    extend rows and decode tokens (timed until the budget is spent)."""
+    import oracle
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from synth import hashgen as hg
+    from synth.model import SynthModel
+    tr = trace_fn(0)
+    model = SynthModel(shape, seed, vocab, device="cpu")
+    tree = oracle.OracleTree(1 << 21)
+    runner = wl.Runner(tree, model)
+    runner.serve([runner.request(tr.warm, 0)])
+    reqs = [runner.request(tr.prompt(i), tr.max_new) for i in range(len(tr.questions))]
+    t0 = time.perf_counter()
+    admitted, _ = runner.serve(reqs)
+    t_tree = time.perf_counter() - t0
+    n_ext_total = sum(r.prompt_len - r.first for r in admitted)
+    n_dec_total = len(admitted) * tr.max_new
+    # attention sample: inputs of two requests generated once on the CPU (not timed)
+    rng = np.random.default_rng(0)
+    pre = []
+    for r in admitted[:2]:
+        h = model.hashes(r.rid)
+        n = r.prompt_len + tr.max_new
+        pre.append((r, hg.gen_values(h[:n], hg.KIND_K, shape.kv_heads, shape.head_dim_k),
+                    hg.gen_values(h[:n], hg.KIND_V, shape.kv_heads, shape.head_dim_v),
+                    hg.gen_values(h[:n], hg.KIND_Q, shape.q_heads, shape.head_dim_k)))
+    t_att_ext = t_att_dec = 0.0
+    n_ext = n_dec = 0
+    while t_att_ext + t_att_dec < budget_s:
+        r, kb, vb, qb = pre[int(rng.integers(0, len(pre)))]
+        pos_dec = r.prompt_len + int(rng.integers(0, tr.max_new))
+        pos_ext = np.arange(r.first, r.prompt_len)
+        a = time.perf_counter()
+        oracle.attention(qb[[pos_dec]], kb, vb, [0], [pos_dec + 1], shape.q_heads, shape.kv_heads,
+                         shape.head_dim_k, shape.head_dim_v, shape.scale)
+        b = time.perf_counter()
+        t_att_dec += b - a
+        n_dec += 1
+        if n_dec % 16 == 1:
+            oracle.attention(qb[pos_ext], kb, vb, np.zeros(len(pos_ext), np.int64), pos_ext + 1, shape.q_heads,
+                             shape.kv_heads, shape.head_dim_k, shape.head_dim_v, shape.scale)
+            t_att_ext += time.perf_counter() - b
+            n_ext += len(pos_ext)
+    est = t_tree + t_att_ext / n_ext * n_ext_total + t_att_dec / n_dec * n_dec_total
+    value = n_dec_total / est
+    sample = (f"oracle tree calls of one full step ({t_tree:.2f} s) + attention of {n_dec} decode tokens and "
+              f"{n_ext} prefill rows ({t_att_dec + t_att_ext:.1f} s), scaled to {n_dec_total} decode tokens and "
+              f"{n_ext_total} prefill rows per step")
+    return {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle", "sample": sample,
+            "est_s_per_step": est}
+
+
+# -------------------------------------------------------------------- main
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from synth import traces
+    trace_fn = lambda salt: traces.few_shot(n_questions=args.questions, max_new=args.max_new, batch_salt=salt)
+    tr0 = trace_fn(0)
+    shape = tr0.shape
+    config = {"workload": f"few-shot sharing: {WARM_LEN}-token shared prefix (512 system + 5x256 examples), "
+                          f"{args.questions} questions U[32,64], {args.max_new} decode steps, "
+                          "GQA 32q/8kv, head_dim 128, bf16, pool 2^21 slots",
+              "policy": args.policy, "cascade": not args.no_cascade,
+              "l2": "inputs larger than L2 (a new batch per step, ~0.55 GB of Q/K/V each)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        cb = oracle_baseline(trace_fn, shape, tr0.seed, tr0.vocab, max(args.cpu_seconds, 5.0))
+        steps_t = []
+        for _ in range(args.warmup + args.steps):
+            steps_t.append(cb["est_s_per_step"])
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["est_s_per_step"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import radixattention_prefix_shared_tree_gb300 as ra
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
+    from synth.model import SynthModel
+
+    policy = ra.RC_LPM if args.policy == "lpm" else ra.RC_FCFS
+    base = SynthModel(shape, tr0.seed, tr0.vocab, device=dev)
+    model = ReplayModel(base, torch)
+    eng = DeviceEngine(shape, tr0.pool_slots, device=dev, table_cap=1 << 22)
+    cache = ra.RadixCache(tr0.pool_slots)
+    runner = wl.Runner(cache, model, eng, policy=policy, cascade=not args.no_cascade)
+    # warm prefix cached (setup, untimed)
+    runner.model = base
+    runner.serve([runner.request(tr0.warm, 0)])
+    runner.model = model
+
+    n_main = args.warmup + args.steps
+    n_e2e = 0 if args.no_e2e else args.steps
+    batches = []
+    for s in range(n_main + n_e2e):
+        tr = trace_fn(s + 1)
+        reqs = [runner.request(tr.prompt(i), tr.max_new) for i in range(len(tr.questions))]
+        model.prepare(reqs, WARM_LEN)
+        batches.append(reqs)
+    torch.cuda.synchronize()
+
+    def step(reqs):
+        admitted, waiting = runner.serve(reqs)
+        if waiting or len(admitted) != len(reqs):
+            raise RuntimeError("batch did not fit")
+        return admitted
+
+    for s in range(args.warmup):
+        step(batches[s])
+    torch.cuda.synchronize()
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+
+    # ---------------------------------------------------------- timed region
+    eng.events.clear()
+    eng.timing = True
+    launches0 = eng.launches
+    st0 = cache.stats()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    ev0.record()
+    for s in range(args.warmup, n_main):
+        step(batches[s])
+    ev1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    eng.timing = False
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    launches = eng.launches - launches0
+    st1 = cache.stats()
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+
+    tokens = args.steps * args.questions * args.max_new
+    value = tokens * world / (ms / 1e3)
+
+    # per-call durations (events on the launching stream)
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    calls = {}
+    for name, evs in eng.events.items():
+        durs = [a.elapsed_time(b) for a, b, _ in evs]
+        info = [i for _, _, i in evs]
+        calls[name] = (durs, info)
+    summary = {}
+    for name, (durs, info) in calls.items():
+        tot = sum(durs)
+        d = {"launches": len(durs), "total_ms": tot, "avg_us": 1e3 * tot / max(len(durs), 1)}
+        if name == "attn_decode":
+            b = [decode_bytes(i[1], i[2], shape) for i in info]
+            uniq = sum(x for x, _ in b) / len(b)
+            logical = sum(y for _, y in b) / len(b)
+            d.update(bytes_per_launch=uniq, logical_bytes_per_launch=logical,
+                     gbs=uniq / (d["avg_us"] * 1e-6) / 1e9, logical_gbs=logical / (d["avg_us"] * 1e-6) / 1e9)
+        elif name == "attn_extend":
+            f = sum(extend_flops(i[1], shape) for i in info) / len(info)
+            d.update(flops_per_launch=f, tflops=f / (d["avg_us"] * 1e-6) / 1e12)
+        elif name == "kv_store":
+            R = 2 * shape.kv_heads * shape.head_dim_k * 2
+            by = sum(2 * i[1] * R for i in info) / len(info)
+            d.update(bytes_per_launch=by, gbs=by / (d["avg_us"] * 1e-6) / 1e9)
+        summary[name] = d
+    dom = max(summary, key=lambda k: summary[k]["total_ms"])
+    dd = summary[dom]
+    if dom == "attn_extend":
+        roof = {"bound": "tensor", "achieved": dd["tflops"], "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": dd["tflops"] / bf16_sus, "traffic": None, "kernel": dom,
+                "peak_source": f"{peak_src} bf16 dense sustained"}
+    else:
+        roof = {"bound": "hbm", "achieved": dd["gbs"], "peak": hbm, "unit": "GB/s", "frac": dd["gbs"] / hbm,
+                "traffic": None, "kernel": dom, "peak_source": f"{peak_src} HBM copy"}
+
+    hit_tok = (st1["match_hit_tokens"] - st0["match_hit_tokens"]) / max(st1["match_tokens"] - st0["match_tokens"], 1)
+    hit_req = (st1["match_hits"] - st0["match_hits"]) / max(st1["match_calls"] - st0["match_calls"], 1)
+
+    # ------------------------------------------------------------------ e2e
+    e2e = None
+    if n_e2e:
+        keys = []
+        for s in range(n_main, n_main + n_e2e):
+            key = tuple(r.rid for r in batches[s])
+            model.to_host(key)
+            keys.append(key)
+        torch.cuda.synchronize()
+        sh = shape
+        out_host = torch.empty(args.questions, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16).pin_memory()
+        d2h = [0]
+        orig_decode = eng.decode
+
+        def decode_and_copy(lay, t, q, out, lse=None):
+            orig_decode(lay, t, q, out, lse)
+            out_host[:out.shape[0]].copy_(out, non_blocking=True)
+            d2h[0] += out.numel() * out.element_size()
+
+        orig_extend = eng.extend
+        ext_host = {}
+
+        def extend_and_copy(lay, q, out, lse=None):
+            orig_extend(lay, q, out, lse)
+            h = ext_host.get(out.shape)
+            if h is None:
+                h = ext_host[out.shape] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+            h.copy_(out, non_blocking=True)
+            d2h[0] += out.numel() * out.element_size()
+
+        eng.decode = decode_and_copy
+        eng.extend = extend_and_copy
+        model.h2d_bytes = 0
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(n_main, n_main + n_e2e):
+            step(batches[s])
+        e1.record()
+        torch.cuda.synchronize()
+        eng.decode = orig_decode
+        eng.extend = orig_extend
+        ems = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": n_e2e * args.questions * args.max_new * world / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": model.h2d_bytes // n_e2e, "d2h_bytes_per_step": d2h[0] // n_e2e,
+               "ms_per_step": ems / n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        import oracle
+        oracle.build()
+        cpu = oracle_baseline(trace_fn, shape, tr0.seed, tr0.vocab, args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk, "hit_rate": {"tokens": hit_tok, "requests": hit_req},
+                "kernels": summary, "wall_s_timed": wall,
+                "parallelism": "replicas" if world > 1 else "single"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

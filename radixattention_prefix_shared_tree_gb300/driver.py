@@ -197,6 +197,22 @@ class DeviceEngine:
         self.desc = make_attn_desc(self.pool, shape.q_heads, shape.scale)
         self.table = torch.zeros(table_cap, dtype=torch.int32, device=dev)
         self._ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
+        self.timing = False          # record CUDA events around every device call
+        self.events = {}             # call name -> [(start, end, info)]
+        self.launches = 0            # kernels launched by the library (counted per call)
+
+    def _call(self, name, kernels, info, fn):
+        if self.timing:
+            st = self.torch.cuda.current_stream()
+            a = self.torch.cuda.Event(enable_timing=True)
+            b = self.torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            self.events.setdefault(name, []).append((a, b, info))
+        else:
+            fn()
+        self.launches += kernels
 
     def workspace(self, nbytes: int):
         if self._ws.numel() < nbytes:
@@ -220,17 +236,21 @@ class DeviceEngine:
 
     # -- kernels
     def store(self, slots_dev, k, v):
-        kv_store(self.pool, slots_dev, k, v)
+        n = int(slots_dev.numel())
+        if n:
+            self._call("kv_store", 1, ("store", n), lambda: kv_store(self.pool, slots_dev, k, v))
 
     def extend(self, lay, q, out, lse=None):
         kv = lay.extend_table
-        attn_extend(self.desc, q, lay.qo_indptr, kv, lay.batch_size, lay.max_q, out, lse)
+        self._call("attn_extend", 1, ("extend", lay),
+                   lambda: attn_extend(self.desc, q, lay.qo_indptr, kv, lay.batch_size, lay.max_q, out, lse))
 
     def decode(self, lay, t: int, q, out, lse=None):
         kv, casc = lay.decode_table(t)
         ws_bytes = attn_decode_workspace(self.desc, lay.batch_size, kv.max_len, casc)
         ws = self.workspace(ws_bytes)
-        attn_decode(self.desc, q, kv, lay.batch_size, out, lse, ws, cascade=casc)
+        self._call("attn_decode", 3 if casc is not None else 2, ("decode", lay, t),
+                   lambda: attn_decode(self.desc, q, kv, lay.batch_size, out, lse, ws, cascade=casc))
 
 
 class BatchLayout:

@@ -117,7 +117,10 @@ def few_shot(n_questions: int = 256, system_len: int = 512, n_examples: int = 5,
     parts += [_tokens(rng, example_len, tr.vocab) for _ in range(n_examples)]
     tr.warm = np.concatenate(parts).astype(np.int32)
     qrng = _rng(1, salt=1 + batch_salt)
-    firsts = _distinct_firsts(qrng, n_questions, tr.vocab)
+    # first tokens: one fixed permutation of the vocabulary, a disjoint slice
+    # per batch, so a batch never matches another batch's cached questions
+    perm = _rng(1, salt=100_000).permutation(tr.vocab).astype(np.int32)
+    firsts = np.take(perm, np.arange(batch_salt * n_questions, (batch_salt + 1) * n_questions), mode="wrap")
     for i in range(n_questions):
         qlen = int(qrng.integers(qmin, qmax + 1))
         tr.questions.append(_tokens(qrng, qlen, tr.vocab, first=firsts[i]))
