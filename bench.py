@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
     ap.add_argument("--questions", type=int, default=N_QUESTIONS)
     ap.add_argument("--max-new", type=int, default=MAX_NEW)
+    ap.add_argument("--pool-slots", type=int, default=0, help="KV pool size (default: the workload's 2^21)")
     return ap.parse_args()
 
 
@@ -318,8 +319,11 @@ def main():
     policy = ra.RC_LPM if args.policy == "lpm" else ra.RC_FCFS
     base = SynthModel(shape, tr0.seed, tr0.vocab, device=dev)
     model = ReplayModel(base, torch)
-    eng = DeviceEngine(shape, tr0.pool_slots, device=dev, table_cap=1 << 22)
-    cache = ra.RadixCache(tr0.pool_slots)
+    pool_slots = args.pool_slots or tr0.pool_slots
+    if args.pool_slots:
+        config["pool_slots"] = pool_slots
+    eng = DeviceEngine(shape, pool_slots, device=dev, table_cap=1 << 22)
+    cache = ra.RadixCache(pool_slots)
     runner = wl.Runner(cache, model, eng, policy=policy, cascade=not args.no_cascade)
     # warm prefix cached (setup, untimed)
     runner.model = base
