@@ -9,7 +9,8 @@
  *
  *  Device (hand-written CUDA for sm_103a): kv_store, attn_decode, attn_extend,
  *  their workspace queries, and rc_sync.  All device memory is the caller's:
- *  the library never allocates it.  Device calls enqueue work on `stream` and
+ *  the library never allocates it (its one device array is the fixed scratch
+ *  of attn_decode_static).  Device calls enqueue work on `stream` and
  *  return; an error detected inside a kernel (a slot index outside the pool)
  *  is OR-ed into the caller's device error word and read back by rc_sync.
  *
@@ -56,6 +57,7 @@ typedef int32_t rc_status;
 #define RC_ERR_TIMEOUT     -5  /* a bounded device wait gave up */
 #define RC_ERR_DEVICE      -6  /* a kernel found a slot index outside the pool */
 #define RC_ERR_UNSUPPORTED -7  /* head layout this build has no kernel for */
+#define RC_ERR_SCRATCH     -8  /* needs more than the library's fixed scratch area */
 
 /* Scheduling policies of sched_order. */
 #define RC_FCFS 0  /* arrival order */
@@ -234,6 +236,27 @@ rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t batch, int32_t
 rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv,
                       int32_t batch, const rc_cascade* cascade, void* out, float* lse,
                       void* ws, size_t ws_bytes, rc_stream_t stream);
+
+/* attn_decode without any device allocation, for callers that cannot call
+ * cudaMalloc or hand over a workspace: for example a serving loop whose
+ * device memory is all carved up at start-up (the KV pool takes what is left)
+ * or a host framework whose plugin interface passes only input and output
+ * pointers.  The pages have no counterpart: this is a library convenience.
+ * Same arguments, result and errors as attn_decode, minus ws/ws_bytes: the
+ * split partials live in a fixed scratch array inside the library,
+ * RC_STATIC_SCRATCH_BYTES long, which every GPU that loads the library holds
+ * until the process exits.  A call whose partials need more (see
+ * attn_decode_workspace) returns RC_ERR_SCRATCH and launches nothing.
+ * The first call on a device looks up that device's scratch address (with
+ * the device current), so make the first call before any stream capture.
+ * All calls share the one array, which keeps the last call's contents (the
+ * partials are written in full before they are read, so nothing needs
+ * clearing): calls that can overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller. */
+#define RC_STATIC_SCRATCH_BYTES (32u << 20)
+rc_status attn_decode_static(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv,
+                             int32_t batch, const rc_cascade* cascade, void* out, float* lse,
+                             rc_stream_t stream);
 
 /* Workspace bytes attn_extend needs (0 today; kept for split variants). */
 rc_status attn_extend_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_q,

@@ -24,6 +24,8 @@ from . import _compile as _build
 
 RC_OK, RC_ERR_ARG, RC_ERR_NOMEM, RC_ERR_STATE = 0, -1, -2, -3
 RC_ERR_CUDA, RC_ERR_TIMEOUT, RC_ERR_DEVICE, RC_ERR_UNSUPPORTED = -4, -5, -6, -7
+RC_ERR_SCRATCH = -8
+RC_STATIC_SCRATCH_BYTES = 32 << 20
 RC_FCFS, RC_LPM = 0, 1
 
 I32, I64, VP = C.c_int32, C.c_int64, C.c_void_p
@@ -72,6 +74,7 @@ SIGNATURES = {
     "kv_store": (I32, [P(rc_pool_desc), VP, VP, VP, I32, VP, VP, VP]),
     "attn_decode_workspace": (I32, [P(rc_attn_desc), I32, I32, P(rc_cascade), P(C.c_size_t)]),
     "attn_decode": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP, C.c_size_t, VP]),
+    "attn_decode_static": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP]),
     "attn_extend_workspace": (I32, [P(rc_attn_desc), I32, I32, I32, P(C.c_size_t)]),
     "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
     "rc_sync": (I32, [VP, VP]),
@@ -326,6 +329,16 @@ def attn_decode(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=Non
                            C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse), _tp(ws),
                            int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream))
     _check("attn_decode", st)
+
+
+def attn_decode_static(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=None,
+                       cascade: rc_cascade | None = None, stream=None) -> int:
+    """attn_decode with the library's fixed scratch area (no workspace, no
+    allocation).  Returns the status instead of raising, so callers can see
+    RC_ERR_SCRATCH."""
+    return lib().attn_decode_static(C.byref(desc), _tp(q), C.byref(kv), int(batch),
+                                    C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse),
+                                    _stream(stream))
 
 
 def attn_extend_workspace(desc: rc_attn_desc, batch: int, max_q: int, max_len: int) -> int:

@@ -452,3 +452,50 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
                                              ri, rp, desc->q_heads, o, lse, P.err);
     return rc_host::launch_status(cudaGetLastError());
 }
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.  The split partials go to a file-scope device
+// array instead of a caller workspace.  In host code the array's name is only
+// a host-side stand-in, so its device address is looked up once per device
+// (with that device current) and passed to the kernels like any workspace.
+
+#include <mutex>
+
+namespace {
+
+static __device__ __align__(256) unsigned char rc_decode_scratch[RC_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void* g_scratch_ptr[kMaxDevices] = {nullptr};
+std::mutex g_scratch_mu;
+
+rc_status scratch_for_current_device(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return RC_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return RC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, rc_decode_scratch) != cudaSuccess || !p) return RC_ERR_CUDA;
+        g_scratch_ptr[dev] = p;
+    }
+    *out = g_scratch_ptr[dev];
+    return RC_OK;
+}
+
+}  // namespace
+
+extern "C" rc_status attn_decode_static(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv,
+                                        int32_t batch, const rc_cascade* casc, void* out, float* lse,
+                                        rc_stream_t stream) {
+    if (!desc || !kv || batch < 0) return RC_ERR_ARG;
+    if (batch == 0) return RC_OK;
+    size_t need = 0;
+    rc_status s = attn_decode_workspace(desc, batch, kv->max_len, casc, &need);
+    if (s != RC_OK) return s;
+    if (need > (size_t)RC_STATIC_SCRATCH_BYTES) return RC_ERR_SCRATCH;
+    void* ws = nullptr;
+    s = scratch_for_current_device(&ws);
+    if (s != RC_OK) return s;
+    return attn_decode(desc, q, kv, batch, casc, out, lse, ws, (size_t)RC_STATIC_SCRATCH_BYTES, stream);
+}

@@ -46,6 +46,7 @@ extern "C" const char* rc_strerror(rc_status s) {
         case RC_ERR_TIMEOUT: return "bounded device wait gave up";
         case RC_ERR_DEVICE: return "kernel found a slot index outside the pool";
         case RC_ERR_UNSUPPORTED: return "head layout not supported by this build";
+        case RC_ERR_SCRATCH: return "batch needs more split scratch than the library's fixed area holds";
         default: return "unknown status";
     }
 }

@@ -1,0 +1,127 @@
+"""attn_decode_static: decode for callers that cannot allocate device memory.
+
+Some callers cannot call cudaMalloc or hand the library a workspace (a serving
+loop whose device memory is all carved up at start-up, a host framework whose
+plugin interface passes only input and output pointers).  For them the
+library keeps the split partials in a fixed device array of its own.  This
+file checks, through the C ABI, that two calls in a row give the same result
+as attn_decode with a caller workspace, and that a batch needing more scratch
+than the fixed area is refused.  It runs last (file name) and also passes on
+its own in a fresh process.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import radixattention_prefix_shared_tree_gb300 as ra
+from radixattention_prefix_shared_tree_gb300.driver import plan_cascade
+from synth import hashgen as hg
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 1e-2, 1e-3
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _case(dev, seed, Hq, Hkv, D, lens, n_slots=12000):
+    g = torch.Generator().manual_seed(seed)
+    k = torch.randn(n_slots, Hkv, D, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(n_slots, Hkv, D, generator=g).to(torch.bfloat16).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    rng = np.random.default_rng(seed)
+    shared = rng.choice(n_slots, size=600, replace=False).astype(np.int32)
+    rest = np.setdiff1d(np.arange(n_slots, dtype=np.int32), shared)
+    rng.shuffle(rest)
+    rows, off = [], 0
+    for L in lens:
+        rows.append(np.concatenate([shared, rest[off:off + L]]).astype(np.int32))
+        off += L
+    B = len(rows)
+    full = [len(r) for r in rows]
+    starts = np.concatenate([[0], np.cumsum(full)[:-1]]).astype(np.int32)
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    state = dict(k=k, v=v, err=err, table=T(np.concatenate(rows)), start=T(starts), len=T(full))
+    state["pool"] = ra.make_pool_desc(k, v, err)
+    state["desc"] = ra.make_attn_desc(state["pool"], Hq, 1.0 / np.sqrt(D))
+    state["kv"] = ra.make_kv_table(state["table"], state["start"], state["len"], max(full))
+    state["q"] = torch.randn(B, Hq, D, generator=g).to(torch.bfloat16).to(dev)
+    # cascade over the shared part (the last position of every row stays private)
+    segs, private = plan_cascade([r[:-1] for r in rows])
+    seg_rows = np.concatenate([np.asarray(r, np.int32) for _, r in segs])
+    pos_of = [[p for p, b in enumerate(seg_rows) if b == bb] for bb in range(B)]
+    arrs = [T(np.concatenate([s for s, _ in segs])), T(np.concatenate([[0], np.cumsum([len(s) for s, _ in segs])])),
+            T(np.concatenate([[0], np.cumsum([len(r) for _, r in segs])])), T(seg_rows),
+            T(np.concatenate([[0], np.cumsum([len(x) for x in pos_of])])), T(np.concatenate(pos_of))]
+    state["casc_arrays"] = arrs
+    state["casc"] = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs))
+    state["pstart"], state["plen"] = T(starts + private), T(np.asarray(full) - private)
+    state["kv_tail"] = ra.make_kv_table(state["table"], state["pstart"], state["plen"],
+                                        int((np.asarray(full) - private).max()))
+    state["B"] = B
+    return state
+
+
+def _with_workspace(st, cascade):
+    kv, casc = (st["kv_tail"], st["casc"]) if cascade else (st["kv"], None)
+    n = ra.attn_decode_workspace(st["desc"], st["B"], kv.max_len, casc)
+    ws = torch.empty(n, dtype=torch.uint8, device=st["q"].device)
+    out = torch.empty(st["B"], st["q"].shape[1], st["q"].shape[2], dtype=torch.bfloat16, device=ws.device)
+    lse = torch.empty(st["B"], st["q"].shape[1], dtype=torch.float32, device=ws.device)
+    ra.attn_decode(st["desc"], st["q"], kv, st["B"], out, lse, ws, cascade=casc)
+    return out, lse
+
+
+def _static(st, cascade):
+    kv, casc = (st["kv_tail"], st["casc"]) if cascade else (st["kv"], None)
+    out = torch.empty(st["B"], st["q"].shape[1], st["q"].shape[2], dtype=torch.bfloat16, device=st["q"].device)
+    lse = torch.empty(st["B"], st["q"].shape[1], dtype=torch.float32, device=out.device)
+    status = ra.attn_decode_static(st["desc"], st["q"], kv, st["B"], out, lse, cascade=casc)
+    assert status == ra.RC_OK, ra.rc_strerror(status)
+    return out, lse
+
+
+def _close(a, b):
+    d = np.abs(hg.bf16_bits_to_f32(_bits(a[0])).astype(np.float64) - hg.bf16_bits_to_f32(_bits(b[0])))
+    assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS
+    assert (a[1] - b[1]).abs().max().item() <= 2e-3
+
+
+@pytest.mark.parametrize("cascade", [False, True])
+def test_static_scratch_matches_workspace_twice(cascade):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda:0")
+    a = _case(dev, 1, 32, 8, 128, [1, 40, 300, 1500, 77, 5])
+    b = _case(dev, 2, 64, 8, 128, [900, 3, 64, 65])
+    for st in (a, b):          # two calls in a row, different batches, shared scratch reused
+        ref = _with_workspace(st, cascade)
+        got = _static(st, cascade)
+        torch.cuda.synchronize()
+        _close(got, ref)
+        assert ra.rc_sync(st["err"]) == ra.RC_OK
+    again = _static(a, cascade)   # and back to the first batch after the second overwrote the scratch
+    _close(again, _with_workspace(a, cascade))
+
+
+def test_static_scratch_refuses_oversized_batch():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda:0")
+    st = _case(dev, 3, 32, 8, 128, [10, 10])
+    # a batch whose partials exceed the fixed area: refused before any launch
+    big_b = 4096
+    kv = ra.make_kv_table(st["table"], st["start"], st["len"], 1 << 15)
+    need = ra.attn_decode_workspace(st["desc"], big_b, 1 << 15)
+    assert need > ra.RC_STATIC_SCRATCH_BYTES
+    out = torch.empty(1, dtype=torch.bfloat16, device=dev)
+    assert ra.attn_decode_static(st["desc"], st["q"], kv, big_b, out) == ra.RC_ERR_SCRATCH
+    assert "scratch" in ra.rc_strerror(ra.RC_ERR_SCRATCH)
