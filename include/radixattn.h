@@ -136,6 +136,48 @@ rc_status rc_free(rc_cache* cache, const int32_t* slots, int64_t n);
 rc_status sched_order(rc_cache* cache, int policy, const int32_t* const* prompts,
                       const int64_t* lens, int32_t n, int32_t* out_order);
 
+/* One request for the batched calls below.  tokens: host buffer holding the
+ * prompt (prompt_len tokens) followed, by the time rc_commit(RC_COMMIT_FINISH)
+ * runs, by the max_new generated tokens.  slots: caller buffer of
+ * prompt_len + max_new entries that rc_admit fills and rc_commit updates.
+ * The remaining fields are outputs. */
+typedef struct rc_request {
+    const int32_t* tokens;
+    int64_t prompt_len;
+    int64_t max_new;
+    int32_t* slots;
+    int64_t matched;   /* cached prefix found at admission */
+    int64_t first;     /* first position the prefill computes */
+    rc_node node;      /* node the request holds a pin on (-1: none) */
+    int32_t admitted;
+} rc_request;
+
+/* Admission of one scheduling round, natively: sched_order(policy), then in
+ * that order rc_match_prefix(pin), first = min(matched, prompt_len - 1) for a
+ * request that will decode (one new token carries the query) else matched,
+ * rc_alloc(prompt_len - first + max_new) with rc_evict of the shortfall on
+ * RC_ERR_NOMEM; a request that still does not fit is unpinned and stops
+ * admission for the round (no overtaking), as does reaching max_batch
+ * (<= 0: no limit) [N49 s.4, s.5].  slots[0..first) = the matched slots,
+ * slots[first..) = the new ones, in allocation order.  out_order receives the
+ * indices of the admitted requests in admission order; *n_admitted their count.
+ * Errors: RC_ERR_ARG. */
+rc_status rc_admit(rc_cache* cache, int policy, rc_request* reqs, int32_t n, int32_t max_batch,
+                   int32_t* out_order, int32_t* n_admitted);
+
+/* Inserts for a batch of admitted requests (indices idx[0..n)).
+ * RC_COMMIT_PREFILL: rc_insert(prompt, slots[0..prompt_len)) pinned if the
+ *   request will decode, drop the admission pin, slots[0..prompt_len) = the
+ *   tree's slots (duplicates were freed) [N49 s.2: only the new part computed].
+ * RC_COMMIT_FINISH: rc_insert(prompt + generated, slots) unpinned and drop the
+ *   request's pin [N49 s.2: a finished request's path, outputs included,
+ *   stays] (requests with max_new == 0 are skipped).
+ * Errors: RC_ERR_ARG, or the first failing rc_insert / rc_release status
+ * (requests before it are committed). */
+#define RC_COMMIT_PREFILL 0
+#define RC_COMMIT_FINISH  1
+rc_status rc_commit(rc_cache* cache, rc_request* reqs, const int32_t* idx, int32_t n, int mode);
+
 typedef struct rc_stats_t {
     int64_t pool_slots, free_slots, caller_slots, tree_tokens, nodes;
     int64_t match_calls, match_tokens, match_hits, match_hit_tokens;
@@ -178,12 +220,14 @@ typedef struct rc_attn_desc {
 /* Per-request slot tables on the device (caller-owned).  The keys of request b
  * are, in position order, slots[start[b] .. start[b] + len[b]).  Rows may have
  * room to grow (kv_store appends).  max_len: a host-side bound on every len[b]
- * (sizes the grid; longer rows are an error). */
+ * (sizes the grid; longer rows are an error).  table_len: entries in `slots`;
+ * a row outside [0, table_len) is not read and flags RC_ERR_DEVICE. */
 typedef struct rc_kv_table {
     const int32_t* slots;
     const int32_t* start;
     const int32_t* len;
     int32_t max_len;
+    int64_t table_len;
 } rc_kv_table;
 
 /* Scatter n new tokens' K/V rows into the pool [N49 s.2: each edge keeps the
@@ -207,8 +251,9 @@ rc_status kv_store(const rc_pool_desc* pool, const int32_t* slots, const void* k
  * positions p in seg_rows with seg_rows[p] == b:
  * req_seg_pos[req_seg_indptr[b] .. req_seg_indptr[b+1]).  With a cascade, the
  * kv table of attn_decode holds only each row's remaining (private) keys; the
- * result equals flat decode over segments + private keys.  max_seg_rows is a
- * host bound on rows per segment; total_seg_rows = seg_row_indptr[n_seg]. */
+ * result equals flat decode over segments + private keys.  max_seg_len and
+ * max_seg_rows are host bounds on keys and rows per segment (they size the
+ * grid); total_seg_rows = seg_row_indptr[n_seg]. */
 typedef struct rc_cascade {
     int32_t n_seg;
     const int32_t* seg_slots;
@@ -217,6 +262,7 @@ typedef struct rc_cascade {
     const int32_t* seg_rows;
     const int32_t* req_seg_indptr;
     const int32_t* req_seg_pos;
+    int32_t max_seg_len;
     int32_t max_seg_rows;
     int32_t total_seg_rows;
 } rc_cascade;

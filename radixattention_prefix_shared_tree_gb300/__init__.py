@@ -42,13 +42,21 @@ class rc_attn_desc(C.Structure):
 
 
 class rc_kv_table(C.Structure):
-    _fields_ = [("slots", VP), ("start", VP), ("len", VP), ("max_len", I32)]
+    _fields_ = [("slots", VP), ("start", VP), ("len", VP), ("max_len", I32), ("table_len", I64)]
 
 
 class rc_cascade(C.Structure):
     _fields_ = [("n_seg", I32), ("seg_slots", VP), ("seg_indptr", VP), ("seg_row_indptr", VP),
-                ("seg_rows", VP), ("req_seg_indptr", VP), ("req_seg_pos", VP), ("max_seg_rows", I32),
+                ("seg_rows", VP), ("req_seg_indptr", VP), ("req_seg_pos", VP), ("max_seg_len", I32), ("max_seg_rows", I32),
                 ("total_seg_rows", I32)]
+
+
+class rc_request(C.Structure):
+    _fields_ = [("tokens", VP), ("prompt_len", I64), ("max_new", I64), ("slots", VP), ("matched", I64),
+                ("first", I64), ("node", I64), ("admitted", I32)]
+
+
+RC_COMMIT_PREFILL, RC_COMMIT_FINISH = 0, 1
 
 
 class rc_stats_t(C.Structure):
@@ -70,6 +78,8 @@ SIGNATURES = {
     "rc_free": (I32, [VP, VP, I64]),
     "sched_order": (I32, [VP, C.c_int, VP, VP, I32, VP]),
     "rc_stats": (I32, [VP, P(rc_stats_t)]),
+    "rc_admit": (I32, [VP, C.c_int, VP, I32, I32, VP, P(I32)]),
+    "rc_commit": (I32, [VP, VP, VP, I32, C.c_int]),
     "rc_dump": (I32, [VP, C.c_char_p, I64, P(I64)]),
     "kv_store": (I32, [P(rc_pool_desc), VP, VP, VP, I32, VP, VP, VP]),
     "attn_decode_workspace": (I32, [P(rc_attn_desc), I32, I32, P(rc_cascade), P(C.c_size_t)]),
@@ -205,6 +215,19 @@ def rc_dump(handle) -> str:
     return buf.value.decode()
 
 
+def rc_admit(handle, policy: int, reqs, n: int, max_batch: int, out_order):
+    """reqs: ctypes array of rc_request; out_order: int32 numpy array of n."""
+    cnt = I32(0)
+    st = lib().rc_admit(handle, int(policy), C.cast(reqs, VP), int(n), int(max_batch), _np_ptr(out_order),
+                        C.byref(cnt))
+    return st, cnt.value
+
+
+def rc_commit(handle, reqs, idx, mode: int):
+    idx = _i32(idx)
+    return lib().rc_commit(handle, C.cast(reqs, VP), _np_ptr(idx), len(idx), int(mode))
+
+
 _STAT_RENAME = {"pool_slots": "pool", "free_slots": "free", "caller_slots": "caller"}
 
 
@@ -247,6 +270,13 @@ class RadixCache:
     def dump(self) -> str:
         return rc_dump(self._h)
 
+    # batched calls used by the scheduler's fast path
+    def admit_batch(self, policy, reqs, n, max_batch, out_order):
+        return rc_admit(self._h, policy, reqs, n, max_batch, out_order)
+
+    def commit_batch(self, reqs, idx, mode):
+        return rc_commit(self._h, reqs, idx, mode)
+
     def stats(self) -> dict:
         return {_STAT_RENAME.get(k, k): v for k, v in rc_stats(self._h).items()}
 
@@ -277,6 +307,7 @@ def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = N
         d.head_dim_v = v.shape[2]
     d.mla = int(mla)
     d.err = err.data_ptr() if err is not None else None
+    d._keep = (k, v, err)   # the descriptor holds raw pointers: keep the tensors alive with it
     return d
 
 
@@ -285,18 +316,21 @@ def make_attn_desc(pool: rc_pool_desc, q_heads: int, sm_scale: float) -> rc_attn
     a.pool = pool
     a.q_heads = int(q_heads)
     a.sm_scale = float(sm_scale)
+    a._keep = getattr(pool, "_keep", None)
     return a
 
 
-def make_kv_table(slots, start, length, max_len: int) -> rc_kv_table:
+def make_kv_table(slots, start, length, max_len: int, table_len: int | None = None) -> rc_kv_table:
     t = rc_kv_table()
     t.slots, t.start, t.len = slots.data_ptr(), start.data_ptr(), length.data_ptr()
     t.max_len = int(max_len)
+    t.table_len = int(slots.numel() if table_len is None else table_len)
+    t._keep = (slots, start, length)   # raw pointers inside: keep the tensors alive with it
     return t
 
 
 def make_cascade(seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos,
-                 max_seg_rows: int) -> rc_cascade:
+                 max_seg_rows: int, max_seg_len: int) -> rc_cascade:
     c = rc_cascade()
     c.n_seg = seg_indptr.numel() - 1
     c.seg_slots = seg_slots.data_ptr() if seg_slots.numel() else None
@@ -305,7 +339,9 @@ def make_cascade(seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr
     c.req_seg_indptr = req_seg_indptr.data_ptr()
     c.req_seg_pos = req_seg_pos.data_ptr() if req_seg_pos.numel() else None
     c.max_seg_rows = int(max_seg_rows)
+    c.max_seg_len = int(max_seg_len)
     c.total_seg_rows = int(seg_rows.numel())
+    c._keep = (seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos)
     return c
 
 

@@ -24,13 +24,7 @@
 
 namespace {
 
-constexpr int kDecKeys = 64;    // keys per tile (16 per warp)
-constexpr int kDecStages = 3;
-
-template <int D>
-constexpr int dec_smem_bytes() {
-    return 8 * D * 2 + kDecStages * 2 * kDecKeys * D * 2;
-}
+constexpr int kDecKeys = 64;    // chunk sizes are multiples of this
 
 struct DecParams {
     const __nv_bfloat16* q;
@@ -43,76 +37,129 @@ struct DecParams {
     const int32_t* table;
     const int32_t* start;
     const int32_t* len;
+    int64_t table_len;
     int32_t chunk;       // keys per CTA
     int32_t n_chunks;    // max chunks per request (partial stride)
-    float* part_o;       // [B][Hq][n_chunks][D]
+    float* part_o;       // [B][Hq][n_chunks][D]      (unfused)
     float* part_lse;     // [B][Hq][n_chunks]
+    // fused epilogue: combine with the cascade partials and write the result
+    const float* seg_o;  // [total_seg_rows][Hq][seg_chunks][D]
+    const float* seg_lse;
+    const int32_t* req_seg_indptr;  // NULL: no cascade
+    const int32_t* req_seg_pos;
+    int32_t seg_chunks;
+    __nv_bfloat16* out;
+    float* lse;
 };
 
-template <int D, int G>
-__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p) {
-    constexpr int CH = D / 8;
+// Decode with one warp per item (request b, KV head, key chunk).  Each warp
+// streams its keys through a private ring of 16-key tiles (one m16 tile of
+// the swapped product) with cp.async, synchronising with __syncwarp only, so
+// the warps of an SM overlap each other's load latency and epilogues freely.
+constexpr int kWarpKeys = 16;
+constexpr int kWarpStages = 3;
+constexpr int kWarpsPerCta = 4;
+
+constexpr int kSlotRing = 4;     // tiles of slot ids: written 4 ahead into the entry of the tile issued 2 iterations ago
+
+template <int D>
+__host__ __device__ constexpr int warp_smem_bytes() {  // per warp: K/V ring + Q + slot ring
+    return kWarpStages * 2 * kWarpKeys * D * 2 + 8 * D * 2 + kSlotRing * kWarpKeys * 4;
+}
+template <int D>
+__host__ __device__ constexpr int dec_smem_bytes() {
+    return kWarpsPerCta * warp_smem_bytes<D>();
+}
+
+template <int D, int G, bool FUSED>
+__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p, int n_items) {
+    constexpr int CH = D / 8;                       // 16-byte chunks per row
     constexpr int KS = D / 16;
+    constexpr int PER = kWarpKeys * CH / 32;        // chunks per lane per matrix
+    constexpr int TILE_BYTES = kWarpKeys * D * 2;
     extern __shared__ __align__(128) unsigned char smem[];
-    unsigned char* sQ = smem;                    // 8 heads x D, swizzled
-    unsigned char* sKV = smem + 8 * D * 2;
-    constexpr int TILE_BYTES = kDecKeys * D * 2;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g_lane = lane >> 2, t_lane = lane & 3;
-    const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int L = p.len[b];
-    const int k_begin = chunk * p.chunk;
-    if (k_begin >= L) return;
-    const int k_count = min(L - k_begin, p.chunk);
-    const int32_t* keys = p.table + p.start[b] + k_begin;
+    const int it = blockIdx.x * kWarpsPerCta + warp;
+    if (it >= n_items) return;
+    unsigned char* wbase = smem + warp * warp_smem_bytes<D>();
+    unsigned char* sQ = wbase + kWarpStages * 2 * TILE_BYTES;
 
-    for (int i = tid; i < 8 * CH; i += 128) {
-        const int r = i / CH, c = i % CH;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < G)
-            v = *reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.q_heads + kvh * G + r) * D + c * 8);
-        *reinterpret_cast<uint4*>(sQ + rc::swz<CH>(r, c)) = v;
+    const int kvh = it % p.kv_heads;
+    const int rest = it / p.kv_heads;
+    const int chunk = rest % p.n_chunks;
+    const int b = rest / p.n_chunks;
+    const int64_t row0 = p.start[b];
+    int L = p.len[b];
+    if (row0 < 0 || L < 0 || row0 + L > p.table_len) {  // row outside the table: read nothing
+        if (lane == 0 && kvh == 0 && chunk == 0) rc::flag_error(p.err, rc::kErrBadSlot);
+        L = 0;
     }
+    if (FUSED && lane == 0 && kvh == 0 && L > p.chunk) rc::flag_error(p.err, rc::kErrBadSlot);
+    const int k0 = chunk * p.chunk;
+    const int count = max(0, min(L - k0, p.chunk));
+    if (!FUSED && count == 0) return;
+    const int32_t* keys = p.table + row0 + k0;
+    const int n_tiles = (count + kWarpKeys - 1) / kWarpKeys;
 
-    auto load_tile = [&](int kt, int st) {
-        unsigned char* sK = sKV + st * 2 * TILE_BYTES;
-        unsigned char* sV = sK + TILE_BYTES;
-        constexpr int PER = kDecKeys * CH / 128;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int lin = i * 128 + tid;
-            const int r = lin / CH, c = lin % CH;
-            const int key = kt * kDecKeys + r;
-            int slot = 0;
-            uint32_t bytes = 0;
-            if (key < k_count) {
-                slot = __ldg(keys + key);
-                if (slot >= 0 && (int64_t)slot < p.n_slots) bytes = 16;
-                else { slot = 0; rc::flag_error(p.err, rc::kErrBadSlot); }
-            }
-            const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
-            rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes);
-            rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes);
+    int32_t* sSlot = reinterpret_cast<int32_t*>(sQ + 8 * D * 2);  // [kSlotRing][kWarpKeys]
+    // Slot ids travel through the cp.async pipeline too: the group committed at
+    // iteration t holds K/V of tile t+2 and the slot ids of tile t+4, so the
+    // gather of a tile reads ids that landed two iterations earlier.
+    auto copy_slots = [&](int t) {
+        if (lane < kWarpKeys) {
+            const int key = t * kWarpKeys + lane;
+            const bool ok = t < n_tiles && key < count;
+            rc::cp_async4(rc::smem_u32(sSlot + (t % kSlotRing) * kWarpKeys + lane), ok ? keys + key : keys,
+                          ok ? 4u : 0u);
         }
     };
-
-    const int n_tiles = (k_count + kDecKeys - 1) / kDecKeys;
+    auto issue = [&](int t) {
+        if (t < n_tiles) {
+            unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
+            unsigned char* sV = sK + TILE_BYTES;
+            const int32_t* ring = sSlot + (t % kSlotRing) * kWarpKeys;
 #pragma unroll
-    for (int s = 0; s < kDecStages - 1; ++s) {
-        if (s < n_tiles) load_tile(s, s);
-        rc::cp_async_commit();
+            for (int i = 0; i < PER; ++i) {
+                const int lin = i * 32 + lane;
+                const int r = lin / CH, c = lin % CH;
+                int slot = ring[r];
+                uint32_t bytes = 16;
+                if (t * kWarpKeys + r >= count) { slot = 0; bytes = 0; }
+                else if (slot < 0 || (int64_t)slot >= p.n_slots) {
+                    rc::flag_error(p.err, rc::kErrBadSlot);
+                    slot = 0;
+                    bytes = 0;
+                }
+                const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
+                rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes);
+                rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes);
+            }
+        }
+    };
+    // prologue: slot ids of tiles 0..3, then Q + K/V of tiles 0 and 1
+#pragma unroll
+    for (int t = 0; t < 4; ++t) copy_slots(t);
+    rc::cp_async_commit();
+    rc::cp_async_wait<0>();
+    __syncwarp();
+    for (int i = lane; i < 8 * CH; i += 32) {
+        const int r = i / CH, c = i % CH;
+        const __nv_bfloat16* src = p.q + ((int64_t)b * p.q_heads + kvh * G + (r < G ? r : 0)) * D + c * 8;
+        rc::cp_async16(rc::smem_u32(sQ + rc::swz<CH>(r, c)), src, r < G ? 16u : 0u);
     }
-    __syncthreads();
+    issue(0);
+    rc::cp_async_commit();
+    issue(1);
+    rc::cp_async_commit();
+    rc::cp_async_wait<1>();
+    __syncwarp();
 
-    // Q as the B operand (k = dims, n = heads): fragments for every k-step.
     uint32_t qb[KS][2];
 #pragma unroll
     for (int ks = 0; ks < KS; ks += 2) {
-        const int r = lane & 7;
-        const int c = ks * 2 + (lane >> 3);
         uint32_t r0, r1, r2, r3;
-        rc::ldmatrix_x4(rc::smem_u32(sQ + rc::swz<CH>(r, c)), r0, r1, r2, r3);
+        rc::ldmatrix_x4(rc::smem_u32(sQ + rc::swz<CH>(lane & 7, ks * 2 + (lane >> 3))), r0, r1, r2, r3);
         qb[ks][0] = r0;
         qb[ks][1] = r1;
         if (ks + 1 < KS) {
@@ -120,26 +167,25 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p)
             qb[ks + 1][1] = r3;
         }
     }
-
-    // O^T accumulators: m = dims (KS tiles of 16), n = heads.
     float o[KS][4];
 #pragma unroll
     for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-    for (int kt = 0; kt < n_tiles; ++kt) {
-        rc::cp_async_wait<kDecStages - 2>();
-        __syncthreads();
-        if (kt + kDecStages - 1 < n_tiles) load_tile(kt + kDecStages - 1, (kt + kDecStages - 1) % kDecStages);
+    for (int t = 0; t < n_tiles; ++t) {
+        if (t > 0) {
+            rc::cp_async_wait<1>();
+            __syncwarp();
+        }
+        issue(t + 2);
+        copy_slots(t + 4);
         rc::cp_async_commit();
-        const unsigned char* sK = sKV + (kt % kDecStages) * 2 * TILE_BYTES;
+        const unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
-        const int kw = warp * 16;  // this warp's 16 keys of the tile
-
-        // S^T (16 keys x 8 heads) = K_w Q^T
+        // S^T (16 keys x 8 heads) = K Q^T
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            const int key = kw + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a0, a1, a2, a3;
@@ -147,13 +193,12 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p)
                 rc::mma_bf16_16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
         }
-        const int key_lo = kt * kDecKeys + kw + g_lane;  // rows g and g+8
-        const bool v_lo = key_lo < k_count, v_hi = key_lo + 8 < k_count;
+        const int key_lo = t * kWarpKeys + g_lane;
+        const bool v_lo = key_lo < count, v_hi = key_lo + 8 < count;
         s[0] = v_lo ? s[0] * p.scale_log2 : -INFINITY;
         s[1] = v_lo ? s[1] * p.scale_log2 : -INFINITY;
         s[2] = v_hi ? s[2] * p.scale_log2 : -INFINITY;
         s[3] = v_hi ? s[3] * p.scale_log2 : -INFINITY;
-        // heads 2t (elements 0, 2) and 2t+1 (elements 1, 3)
         float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
         float alpha[2], mu[2];
 #pragma unroll
@@ -177,75 +222,109 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p)
             o[i][2] *= alpha[0];
             o[i][3] *= alpha[1];
         }
-        // P^T as the B operand (k = keys, n = heads), transposed in registers.
         const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));
         const uint32_t pb1 = rc::movmatrix_trans(rc::pack_bf16(p2, p3));
-        // O^T (dims x heads) += V_w^T P^T
         {
-            const int key = kw + (lane & 7) + (lane >> 4) * 8;
+            const int key = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a0, a1, a2, a3;
-                rc::ldmatrix_x4_trans(rc::smem_u32(sV + rc::swz<CH>(key, mt * 2 + ((lane >> 3) & 1))), a0, a1,
-                                      a2, a3);
+                rc::ldmatrix_x4_trans(rc::smem_u32(sV + rc::swz<CH>(key, mt * 2 + ((lane >> 3) & 1))), a0, a1, a2,
+                                      a3);
                 rc::mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
     }
     rc::cp_async_wait<0>();
+    __syncwarp();
 
+    // ---------------------------------------------------------- epilogue
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
     }
-    __syncthreads();  // stages are free: reuse them for the cross-warp merge
-    float* sO = reinterpret_cast<float*>(sKV);          // [4 warps][8 heads][D]
-    float* sM = sO + 4 * 8 * D;                         // [4][8]
-    float* sL = sM + 32;                                // [4][8]
+    // this warp's normalised output per (head, dim) into its (now free) ring
+    float* sE = reinterpret_cast<float*>(wbase);           // [8][D]
+    float* sOwn = sE + 8 * D;                               // [8] log2-sum-exp per head
+    const float inv0 = l_run[0] > 0.f ? 1.f / l_run[0] : 0.f;
+    const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
         const int d0 = mt * 16 + g_lane;
-        sO[(warp * 8 + 2 * t_lane) * D + d0] = o[mt][0];
-        sO[(warp * 8 + 2 * t_lane + 1) * D + d0] = o[mt][1];
-        sO[(warp * 8 + 2 * t_lane) * D + d0 + 8] = o[mt][2];
-        sO[(warp * 8 + 2 * t_lane + 1) * D + d0 + 8] = o[mt][3];
+        sE[(2 * t_lane) * D + d0] = o[mt][0] * inv0;
+        sE[(2 * t_lane + 1) * D + d0] = o[mt][1] * inv1;
+        sE[(2 * t_lane) * D + d0 + 8] = o[mt][2] * inv0;
+        sE[(2 * t_lane + 1) * D + d0 + 8] = o[mt][3] * inv1;
     }
     if (g_lane == 0) {
-        sM[warp * 8 + 2 * t_lane] = m_run[0];
-        sM[warp * 8 + 2 * t_lane + 1] = m_run[1];
-        sL[warp * 8 + 2 * t_lane] = l_run[0];
-        sL[warp * 8 + 2 * t_lane + 1] = l_run[1];
+        sOwn[2 * t_lane] = l_run[0] > 0.f ? m_run[0] + log2f(l_run[0]) : -INFINITY;
+        sOwn[2 * t_lane + 1] = l_run[1] > 0.f ? m_run[1] + log2f(l_run[1]) : -INFINITY;
     }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += 128) {
-        const int h = i / D, d = i % D;
-        float m = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) m = fmaxf(m, sM[w * 8 + h]);
-        float l = 0.f, acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const float mw = sM[w * 8 + h];
-            const float f = mw == -INFINITY ? 0.f : rc::fast_exp2(mw - m);
-            l += sL[w * 8 + h] * f;
-            acc += sO[(w * 8 + h) * D + d] * f;
+    __syncwarp();
+    if constexpr (!FUSED) {
+        for (int h = 0; h < G; ++h) {
+            const int64_t idx = ((int64_t)b * p.q_heads + kvh * G + h) * p.n_chunks + chunk;
+            for (int d = lane; d < D; d += 32) p.part_o[idx * D + d] = sE[h * D + d];
+            if (lane == 0) p.part_lse[idx] = sOwn[h];
         }
-        const int64_t idx = ((int64_t)b * p.q_heads + kvh * G + h) * p.n_chunks + chunk;
-        p.part_o[idx * D + d] = acc / l;
-        if (d == 0) p.part_lse[idx] = m + log2f(l);
+    } else {
+        // the row's whole table part is here: fold in its cascade partials
+        // (every chunk of every segment it reads; partial (e, c) of head h
+        // sits at row (req_seg_pos[e] * Hq + h) * seg_chunks + c)
+        int e0 = 0, n_parts = 0;
+        if (p.req_seg_indptr) {
+            e0 = p.req_seg_indptr[b];
+            n_parts = (p.req_seg_indptr[b + 1] - e0) * p.seg_chunks;
+        }
+        const int sc = p.seg_chunks;
+        auto part_row = [&](int j) -> int64_t {
+            return (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc);
+        };
+        for (int h = 0; h < G; ++h) {
+            const int head = kvh * G + h;
+            const int64_t hoff = (int64_t)head * sc;
+            const float own = sOwn[h];
+            float m = own;
+            for (int j = lane; j < n_parts; j += 32) m = fmaxf(m, p.seg_lse[part_row(j) + hoff]);
+#pragma unroll
+            for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+            float w = 0.f;
+            for (int j = lane; j < n_parts; j += 32) {
+                const float l2 = p.seg_lse[part_row(j) + hoff];
+                w += l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m);
+            }
+#pragma unroll
+            for (int k = 16; k > 0; k >>= 1) w += __shfl_xor_sync(0xffffffffu, w, k);
+            const float wo = own == -INFINITY ? 0.f : rc::fast_exp2(own - m);
+            w += wo;
+            const float invw = w > 0.f ? 1.f / w : 0.f;
+            const int64_t orow = (int64_t)b * p.q_heads + head;
+            for (int d = lane; d < D; d += 32) {
+                float acc = wo * sE[h * D + d];
+#pragma unroll 4
+                for (int j = 0; j < n_parts; ++j) {
+                    const int64_t row = part_row(j) + hoff;
+                    const float l2 = p.seg_lse[row];
+                    const float v = p.seg_o[row * D + d];
+                    acc += l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m) * v;
+                }
+                p.out[orow * D + d] = __float2bfloat16_rn(acc * invw);
+            }
+            if (p.lse && lane == 0) p.lse[orow] = w > 0.f ? (m + log2f(w)) * rc::kLn2 : -INFINITY;
+        }
     }
 }
 
-// Combine every partial of (request, head): cascade segments first, then the
-// chunks of the request's own table row.
+// Combine every partial of (request, head): cascade segments (all chunks)
+// then the chunks of the request's own table row.
 template <int D>
 __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tail_o,
                                                    const float* __restrict__ tail_lse, int32_t n_chunks,
                                                    int32_t chunk, const int32_t* __restrict__ len,
                                                    const float* __restrict__ seg_o,
-                                                   const float* __restrict__ seg_lse,
+                                                   const float* __restrict__ seg_lse, int32_t seg_chunks,
                                                    const int32_t* __restrict__ req_seg_indptr,
                                                    const int32_t* __restrict__ req_seg_pos, int32_t q_heads,
                                                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
@@ -262,18 +341,24 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
     const int s0 = req_seg_indptr ? req_seg_indptr[b] : 0;
     const int ns = req_seg_indptr ? req_seg_indptr[b + 1] - s0 : 0;
     float m = -INFINITY;
-    for (int i = 0; i < ns; ++i) m = fmaxf(m, seg_lse[(int64_t)req_seg_pos[s0 + i] * q_heads + h]);
+    for (int i = 0; i < ns; ++i)
+        for (int c = 0; c < seg_chunks; ++c)
+            m = fmaxf(m, seg_lse[((int64_t)req_seg_pos[s0 + i] * q_heads + h) * seg_chunks + c]);
     for (int c = 0; c < nc; ++c) m = fmaxf(m, tail_lse[(int64_t)bh * n_chunks + c]);
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
     float wsum = 0.f;
     for (int i = 0; i < ns; ++i) {
-        const int64_t row = (int64_t)req_seg_pos[s0 + i] * q_heads + h;
-        const float w = rc::fast_exp2(seg_lse[row] - m);
-        wsum += w;
+        for (int c = 0; c < seg_chunks; ++c) {
+            const int64_t row = ((int64_t)req_seg_pos[s0 + i] * q_heads + h) * seg_chunks + c;
+            const float l2 = seg_lse[row];
+            if (l2 == -INFINITY) continue;
+            const float w = rc::fast_exp2(l2 - m);
+            wsum += w;
 #pragma unroll
-        for (int j = 0; j < PER; ++j) acc[j] += w * seg_o[row * D + lane + 32 * j];
+            for (int j = 0; j < PER; ++j) acc[j] += w * seg_o[row * D + lane + 32 * j];
+        }
     }
     for (int c = 0; c < nc; ++c) {
         const int64_t row = (int64_t)bh * n_chunks + c;
@@ -290,7 +375,9 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
 
 // ------------------------------------------------------------------ planning
 struct DecodePlan {
-    int chunk = 0, n_chunks = 0;
+    int chunk = 0, n_chunks = 0;        // table part: keys per CTA, CTAs per row
+    int seg_chunk = 0, seg_chunks = 0;  // cascade: keys per CTA, CTAs per segment
+    bool fused = false;                 // one CTA per (row, KV head): no merge pass
     size_t tail_o = 0, tail_lse = 0, seg_o = 0, seg_lse = 0, total = 0;
 };
 
@@ -302,34 +389,59 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     const int hkv = d->pool.kv_heads;
     if (hkv <= 0 || d->q_heads <= 0 || d->q_heads % hkv) return RC_ERR_ARG;
     const int dv = d->pool.head_dim_v;
-    // Split so that the grid covers the SMs about four times over.
+    const int64_t sms = rc_host::sm_count();
+    // Table part: one warp per (row, KV head) when that already gives every
+    // SM eight warps (the merge is then fused); otherwise split the keys so
+    // that there are about sixteen warps per SM.
     const int64_t base = (int64_t)batch * hkv;
-    const int64_t target = 4LL * rc_host::sm_count();
-    int64_t splits = base > 0 ? (target + base - 1) / base : 1;
-    const int64_t max_splits = max_len > 0 ? (max_len + 255) / 256 : 1;
-    if (splits > max_splits) splits = max_splits;
-    if (splits < 1) splits = 1;
+    int64_t splits = 1;
+    if (base < 8 * sms) {
+        splits = base > 0 ? (16 * sms + base - 1) / base : 1;
+        const int64_t max_splits = max_len > 0 ? (max_len + 255) / 256 : 1;
+        if (splits > max_splits) splits = max_splits;
+        if (splits < 1) splits = 1;
+    }
     int64_t chunk = max_len > 0 ? (max_len + splits - 1) / splits : kDecKeys;
     chunk = (chunk + kDecKeys - 1) / kDecKeys * kDecKeys;
     pl->chunk = (int)chunk;
     pl->n_chunks = max_len > 0 ? (int)((max_len + chunk - 1) / chunk) : 1;
+    pl->fused = pl->n_chunks == 1;
+    // Cascade part: split each segment's keys so the grid covers the SMs a
+    // few times (the rows of one segment share every key tile).
+    pl->seg_chunk = 0;
+    pl->seg_chunks = 1;
+    if (casc && casc->n_seg > 0 && casc->max_seg_len > 0) {
+        const int G = d->q_heads / hkv;
+        const int64_t row_blocks = (casc->max_seg_rows * (int64_t)G + rc::kMQRows - 1) / rc::kMQRows;
+        const int64_t cbase = (int64_t)casc->n_seg * row_blocks * hkv;
+        int64_t sc = cbase > 0 ? (3 * sms + cbase - 1) / cbase : 1;
+        const int64_t sc_max = (casc->max_seg_len + 255) / 256;
+        if (sc > sc_max) sc = sc_max;
+        if (sc < 1) sc = 1;
+        int64_t len = (casc->max_seg_len + sc - 1) / sc;
+        len = (len + rc::kMQKeys - 1) / rc::kMQKeys * rc::kMQKeys;
+        pl->seg_chunk = (int)len;
+        pl->seg_chunks = (int)((casc->max_seg_len + len - 1) / len);
+    }
     const size_t rows = (size_t)batch * d->q_heads;
-    pl->tail_o = align256(rows * pl->n_chunks * dv * sizeof(float));
-    pl->tail_lse = align256(rows * pl->n_chunks * sizeof(float));
-    const size_t srows = casc ? (size_t)casc->total_seg_rows * d->q_heads : 0;
+    pl->tail_o = pl->fused ? 0 : align256(rows * pl->n_chunks * dv * sizeof(float));
+    pl->tail_lse = pl->fused ? 0 : align256(rows * pl->n_chunks * sizeof(float));
+    const size_t srows = casc ? (size_t)casc->total_seg_rows * d->q_heads * pl->seg_chunks : 0;
     pl->seg_o = align256(srows * dv * sizeof(float));
     pl->seg_lse = align256(srows * sizeof(float));
     pl->total = pl->tail_o + pl->tail_lse + pl->seg_o + pl->seg_lse;
+    if (pl->total == 0) pl->total = 256;
     return RC_OK;
 }
 
-template <int D, int G>
+template <int D, int G, bool FUSED>
 cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream_t st) {
     constexpr int smem = dec_smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G>>(smem);
+    cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G, FUSED>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.n_chunks, kv_heads, batch);
-    decode_split_kernel<D, G><<<grid, 128, smem, st>>>(p);
+    const int n_items = batch * kv_heads * p.n_chunks;
+    const int grid = (n_items + kWarpsPerCta - 1) / kWarpsPerCta;
+    decode_split_kernel<D, G, FUSED><<<grid, 32 * kWarpsPerCta, smem, st>>>(p, n_items);
     return cudaGetLastError();
 }
 
@@ -339,29 +451,30 @@ cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_he
     cudaError_t e = rc_host::ensure_smem<rc::mq_attn_kernel<D, G, rc::MQMode::kCascade>>(smem);
     if (e != cudaSuccess) return e;
     constexpr int TPC = rc::kMQRows / G;
-    dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg);
+    dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
     rc::mq_attn_kernel<D, G, rc::MQMode::kCascade><<<grid, 128, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 template <int D, int G>
-cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, int batch,
+cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused, int batch,
                     int kv_heads, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     if (casc && casc->n_seg > 0 && casc->max_seg_rows > 0) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
-    if (e == cudaSuccess) e = launch_split<D, G>(dp, batch, kv_heads, st);
-    return e;
+    if (e != cudaSuccess) return e;
+    return fused ? launch_split<D, G, true>(dp, batch, kv_heads, st)
+                 : launch_split<D, G, false>(dp, batch, kv_heads, st);
 }
 
 template <int D>
-cudaError_t dispatch_group(int G, const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc,
+cudaError_t dispatch_group(int G, const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused,
                            int batch, int kv_heads, cudaStream_t st, bool* ok) {
     *ok = true;
     switch (G) {
-        case 1: return run_gqa<D, 1>(dp, mp, casc, batch, kv_heads, st);
-        case 2: return run_gqa<D, 2>(dp, mp, casc, batch, kv_heads, st);
-        case 4: return run_gqa<D, 4>(dp, mp, casc, batch, kv_heads, st);
-        case 8: return run_gqa<D, 8>(dp, mp, casc, batch, kv_heads, st);
+        case 1: return run_gqa<D, 1>(dp, mp, casc, fused, batch, kv_heads, st);
+        case 2: return run_gqa<D, 2>(dp, mp, casc, fused, batch, kv_heads, st);
+        case 4: return run_gqa<D, 4>(dp, mp, casc, fused, batch, kv_heads, st);
+        case 8: return run_gqa<D, 8>(dp, mp, casc, fused, batch, kv_heads, st);
         default: *ok = false; return cudaSuccess;
     }
 }
@@ -384,12 +497,12 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     if (!desc || !kv || batch < 0) return RC_ERR_ARG;
     if (batch == 0) return RC_OK;
     if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
+    const bool use_casc = casc && casc->n_seg > 0;
     DecodePlan pl;
-    rc_status s = plan_decode(desc, batch, kv->max_len, casc, &pl);
+    rc_status s = plan_decode(desc, batch, kv->max_len, use_casc ? casc : nullptr, &pl);
     if (s != RC_OK) return s;
     if (!ws || ws_bytes < pl.total) return RC_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(ws) & 255) return RC_ERR_ARG;
-    const bool use_casc = casc && casc->n_seg > 0;
     if (use_casc && (!casc->seg_slots || !casc->seg_indptr || !casc->seg_row_indptr || !casc->seg_rows ||
                      !casc->req_seg_indptr || !casc->req_seg_pos))
         return RC_ERR_ARG;
@@ -398,6 +511,8 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     if (P.mla || P.head_dim_v != D || !P.v) return RC_ERR_UNSUPPORTED;
     const int G = desc->q_heads / P.kv_heads;
     unsigned char* w = static_cast<unsigned char*>(ws);
+    float* seg_o = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse);
+    float* seg_lse = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse + pl.seg_o);
     DecParams dp;
     dp.q = static_cast<const __nv_bfloat16*>(q);
     dp.pool_k = static_cast<const __nv_bfloat16*>(P.k);
@@ -410,10 +525,18 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     dp.table = kv->slots;
     dp.start = kv->start;
     dp.len = kv->len;
+    dp.table_len = kv->table_len;
     dp.chunk = pl.chunk;
     dp.n_chunks = pl.n_chunks;
     dp.part_o = reinterpret_cast<float*>(w);
     dp.part_lse = reinterpret_cast<float*>(w + pl.tail_o);
+    dp.seg_o = seg_o;
+    dp.seg_lse = seg_lse;
+    dp.req_seg_indptr = use_casc ? casc->req_seg_indptr : nullptr;
+    dp.req_seg_pos = use_casc ? casc->req_seg_pos : nullptr;
+    dp.seg_chunks = pl.seg_chunks;
+    dp.out = static_cast<__nv_bfloat16*>(out);
+    dp.lse = lse;
     rc::MQParams mp{};
     mp.q = dp.q;
     mp.pool_k = dp.pool_k;
@@ -423,8 +546,6 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     mp.q_heads = dp.q_heads;
     mp.scale_log2 = dp.scale_log2;
     mp.err = dp.err;
-    float* seg_o = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse);
-    float* seg_lse = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse + pl.seg_o);
     if (use_casc) {
         mp.seg_slots = casc->seg_slots;
         mp.seg_indptr = casc->seg_indptr;
@@ -432,24 +553,28 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
         mp.seg_rows = casc->seg_rows;
         mp.part_o = seg_o;
         mp.part_lse = seg_lse;
+        mp.seg_chunk = pl.seg_chunk;
+        mp.seg_chunks = pl.seg_chunks;
     }
     cudaStream_t st = (cudaStream_t)stream;
     bool ok = false;
     cudaError_t e = cudaSuccess;
-    if (D == 128) e = dispatch_group<128>(G, dp, mp, use_casc ? casc : nullptr, batch, P.kv_heads, st, &ok);
-    else if (D == 64) e = dispatch_group<64>(G, dp, mp, use_casc ? casc : nullptr, batch, P.kv_heads, st, &ok);
+    const rc_cascade* cc = use_casc ? casc : nullptr;
+    if (D == 128) e = dispatch_group<128>(G, dp, mp, cc, pl.fused, batch, P.kv_heads, st, &ok);
+    else if (D == 64) e = dispatch_group<64>(G, dp, mp, cc, pl.fused, batch, P.kv_heads, st, &ok);
     if (!ok) return RC_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return RC_ERR_CUDA;
+    if (pl.fused) return RC_OK;
     const int32_t* ri = use_casc ? casc->req_seg_indptr : nullptr;
     const int32_t* rp = use_casc ? casc->req_seg_pos : nullptr;
     const unsigned nbh = (unsigned)batch * desc->q_heads;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
     if (D == 128)
         merge_kernel<128><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                              ri, rp, desc->q_heads, o, lse, P.err);
+                                              pl.seg_chunks, ri, rp, desc->q_heads, o, lse, P.err);
     else
         merge_kernel<64><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                             ri, rp, desc->q_heads, o, lse, P.err);
+                                             pl.seg_chunks, ri, rp, desc->q_heads, o, lse, P.err);
     return rc_host::launch_status(cudaGetLastError());
 }
 

@@ -72,6 +72,7 @@ extern "C" rc_status attn_extend(const rc_attn_desc* desc, const void* q, const 
     p.table = kv->slots;
     p.start = kv->start;
     p.len = kv->len;
+    p.table_len = kv->table_len;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
     const int G = desc->q_heads / P.kv_heads;

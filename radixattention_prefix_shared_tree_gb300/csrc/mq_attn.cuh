@@ -31,6 +31,7 @@ struct MQParams {
     const int32_t* table;
     const int32_t* start;
     const int32_t* len;
+    int64_t table_len;
     __nv_bfloat16* out;
     float* lse;
     // cascade: rows are the requests sharing segment blockIdx.z
@@ -38,17 +39,21 @@ struct MQParams {
     const int32_t* seg_indptr;
     const int32_t* seg_row_indptr;
     const int32_t* seg_rows;
-    float* part_o;    // [total_seg_rows][q_heads][D]
-    float* part_lse;  // [total_seg_rows][q_heads], log2 units
+    float* part_o;    // [total_seg_rows][q_heads][seg_chunks][D]
+    float* part_lse;  // [total_seg_rows][q_heads][seg_chunks], log2 units (-inf: empty chunk)
+    int32_t seg_chunk;   // keys per cascade CTA
+    int32_t seg_chunks;  // chunks per segment (grid z = segment * seg_chunks + chunk)
 };
 
 constexpr int kMQRows = 64;
 constexpr int kMQKeys = 64;
 constexpr int kMQStages = 3;
 
+constexpr int kMQSlotRing = 4;  // tiles of slot ids: written 4 ahead into the entry of the tile issued 2 iterations ago
+
 template <int D>
-constexpr int mq_smem_bytes() {
-    return kMQRows * D * 2 + kMQStages * 2 * kMQKeys * D * 2;
+__host__ __device__ constexpr int mq_smem_bytes() {
+    return kMQRows * D * 2 + kMQStages * 2 * kMQKeys * D * 2 + kMQSlotRing * kMQKeys * 4;
 }
 
 template <int D, int G, MQMode MODE>
@@ -80,50 +85,66 @@ __global__ void __launch_bounds__(128, 2) mq_attn_kernel(const MQParams p) {
         n_rows_tok = p.qo_indptr[z + 1] - qo0;
         const int L = p.len[z];
         prefix = L - n_rows_tok;
-        keys = p.table + p.start[z];
+        const int64_t row0 = p.start[z];
         if (tok0 >= n_rows_tok) return;
+        if (row0 < 0 || prefix < 0 || row0 + L > p.table_len) {  // row outside the table: read nothing
+            if (tid == 0) flag_error(p.err, kErrBadSlot);
+            return;
+        }
+        keys = p.table + row0;
         const int last = min(n_rows_tok, tok0 + TPC) - 1;
         key_count = prefix + last + 1;
     } else {
-        const int r0 = p.seg_row_indptr[z];
-        n_rows_tok = p.seg_row_indptr[z + 1] - r0;
+        const int seg = z / p.seg_chunks;
+        const int chunk = z % p.seg_chunks;
+        const int r0 = p.seg_row_indptr[seg];
+        n_rows_tok = p.seg_row_indptr[seg + 1] - r0;
         qo0 = r0;
-        keys = p.seg_slots + p.seg_indptr[z];
-        key_count = p.seg_indptr[z + 1] - p.seg_indptr[z];
+        const int k0 = chunk * p.seg_chunk;
+        keys = p.seg_slots + p.seg_indptr[seg] + k0;
+        key_count = min(p.seg_indptr[seg + 1] - p.seg_indptr[seg] - k0, p.seg_chunk);
         if (tok0 >= n_rows_tok) return;
-    }
-
-    // ---- load Q rows (zero for rows past the end)
-    for (int i = tid; i < kMQRows * CH; i += 128) {
-        const int r = i / CH, c = i % CH;
-        const int tk = tok0 + r / G;
-        const int h = kvh * G + (r % G);
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (tk < n_rows_tok) {
-            int64_t qrow;
-            if constexpr (MODE == MQMode::kExtend) qrow = (int64_t)(qo0 + tk) * p.q_heads + h;
-            else qrow = (int64_t)p.seg_rows[qo0 + tk] * p.q_heads + h;
-            v = *reinterpret_cast<const uint4*>(p.q + qrow * D + c * 8);
+        if (key_count <= 0) {  // segment shorter than this chunk: an empty partial
+            for (int r = tid; r < kMQRows; r += 128) {
+                const int tk = tok0 + r / G;
+                if (tk < n_rows_tok)
+                    p.part_lse[((int64_t)(qo0 + tk) * p.q_heads + kvh * G + (r % G)) * p.seg_chunks + chunk] =
+                        -INFINITY;
+            }
+            return;
         }
-        *reinterpret_cast<uint4*>(sQ + swz<CH>(r, c)) = v;
     }
 
-    // ---- tile loader: keys [kt*64, kt*64+64) into stage st
-    auto load_tile = [&](int kt, int st) {
-        unsigned char* sK = sKV + st * 2 * TILE_BYTES;
+    int32_t* sSlot = reinterpret_cast<int32_t*>(sKV + kMQStages * 2 * TILE_BYTES);  // [ring][64]
+    const int n_tiles = (key_count + kMQKeys - 1) / kMQKeys;
+
+    // Slot ids travel through the cp.async pipeline: the group committed at
+    // iteration kt holds K/V of tile kt+2 and the slot ids of tile kt+4, so a
+    // gather never waits on the load of its own ids.
+    auto copy_slots = [&](int kt) {
+        if (tid < kMQKeys) {
+            const int key = kt * kMQKeys + tid;
+            const bool ok = kt < n_tiles && key < key_count;
+            cp_async4(smem_u32(sSlot + (kt % kMQSlotRing) * kMQKeys + tid), ok ? keys + key : keys, ok ? 4u : 0u);
+        }
+    };
+    auto load_tile = [&](int kt) {
+        if (kt >= n_tiles) return;
+        unsigned char* sK = sKV + (kt % kMQStages) * 2 * TILE_BYTES;
         unsigned char* sV = sK + TILE_BYTES;
+        const int32_t* ring = sSlot + (kt % kMQSlotRing) * kMQKeys;
         constexpr int PER = kMQKeys * CH / 128;  // chunks per thread per matrix
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int lin = i * 128 + tid;
             const int r = lin / CH, c = lin % CH;
-            const int key = kt * kMQKeys + r;
-            int slot = 0;
-            uint32_t bytes = 0;
-            if (key < key_count) {
-                slot = __ldg(keys + key);
-                if (slot >= 0 && (int64_t)slot < p.n_slots) bytes = 16;
-                else { slot = 0; flag_error(p.err, kErrBadSlot); }
+            int slot = ring[r];
+            uint32_t bytes = 16;
+            if (kt * kMQKeys + r >= key_count) { slot = 0; bytes = 0; }
+            else if (slot < 0 || (int64_t)slot >= p.n_slots) {
+                flag_error(p.err, kErrBadSlot);
+                slot = 0;
+                bytes = 0;
             }
             const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
             cp_async16(smem_u32(sK + swz<CH>(r, c)), p.pool_k + roff, bytes);
@@ -131,12 +152,28 @@ __global__ void __launch_bounds__(128, 2) mq_attn_kernel(const MQParams p) {
         }
     };
 
-    const int n_tiles = (key_count + kMQKeys - 1) / kMQKeys;
+    // prologue: slot ids of tiles 0..3; then Q rows (zero past the end) + tile 0; tile 1
 #pragma unroll
-    for (int s = 0; s < kMQStages - 1; ++s) {
-        if (s < n_tiles) load_tile(s, s);
-        cp_async_commit();
+    for (int t = 0; t < 4; ++t) copy_slots(t);
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int i = tid; i < kMQRows * CH; i += 128) {
+        const int r = i / CH, c = i % CH;
+        const int tk = tok0 + r / G;
+        const int h = kvh * G + (r % G);
+        int64_t qrow = 0;
+        if (tk < n_rows_tok) {
+            if constexpr (MODE == MQMode::kExtend) qrow = (int64_t)(qo0 + tk) * p.q_heads + h;
+            else qrow = (int64_t)p.seg_rows[qo0 + tk] * p.q_heads + h;
+        }
+        cp_async16(smem_u32(sQ + swz<CH>(r, c)), p.q + qrow * D + c * 8, tk < n_rows_tok ? 16u : 0u);
     }
+    load_tile(0);
+    cp_async_commit();
+    load_tile(1);
+    cp_async_commit();
+    cp_async_wait<1>();
     __syncthreads();
 
     // ---- Q fragments of this warp's 16 rows
@@ -165,9 +202,12 @@ __global__ void __launch_bounds__(128, 2) mq_attn_kernel(const MQParams p) {
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     for (int kt = 0; kt < n_tiles; ++kt) {
-        cp_async_wait<kMQStages - 2>();
-        __syncthreads();
-        if (kt + kMQStages - 1 < n_tiles) load_tile(kt + kMQStages - 1, (kt + kMQStages - 1) % kMQStages);
+        if (kt > 0) {
+            cp_async_wait<1>();
+            __syncthreads();
+        }
+        load_tile(kt + 2);
+        copy_slots(kt + 4);
         cp_async_commit();
         const unsigned char* sK = sKV + (kt % kMQStages) * 2 * TILE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
@@ -271,7 +311,7 @@ __global__ void __launch_bounds__(128, 2) mq_attn_kernel(const MQParams p) {
             }
             if (p.lse && t_lane == 0) p.lse[row] = lse2 * kLn2;
         } else {
-            const int64_t row = (int64_t)(qo0 + tk) * p.q_heads + h;
+            const int64_t row = ((int64_t)(qo0 + tk) * p.q_heads + h) * p.seg_chunks + (z % p.seg_chunks);
             float* dst = p.part_o + row * D;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {

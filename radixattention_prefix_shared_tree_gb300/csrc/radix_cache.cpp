@@ -329,7 +329,7 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     if (pin) c->pin(c->path);
     if (out_slots) {
         if (m) std::memcpy(out_slots, have.data(), (size_t)m * 4);
-        if (n > m) std::memcpy(out_slots + m, slots + m, (size_t)(n - m) * 4);
+        if (n > m && out_slots != slots) std::memmove(out_slots + m, slots + m, (size_t)(n - m) * 4);
     }
     *already_present = m;
     *out_node = c->recs[(size_t)c->path.back()].id;
@@ -429,6 +429,82 @@ rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, co
             key[(size_t)i] = {-c->descend(prompts[i], lens[i], false, nullptr, nullptr), i};
         std::sort(key.begin(), key.end());  // (-match, index): longest first, then arrival
         for (int32_t i = 0; i < n; ++i) out_order[i] = key[(size_t)i].second;
+    }
+    return RC_OK;
+}
+
+rc_status rc_admit(rc_cache* c, int policy, rc_request* reqs, int32_t n, int32_t max_batch, int32_t* out_order,
+                   int32_t* n_admitted) {
+    if (!c || n < 0 || (n > 0 && (!reqs || !out_order)) || !n_admitted) return RC_ERR_ARG;
+    *n_admitted = 0;
+    if (n == 0) return RC_OK;
+    std::vector<const int32_t*> prompts((size_t)n);
+    std::vector<int64_t> lens((size_t)n);
+    for (int32_t i = 0; i < n; ++i) {
+        const rc_request& r = reqs[i];
+        if (r.prompt_len < 0 || r.max_new < 0 || (r.prompt_len > 0 && !r.tokens) || !r.slots ||
+            (r.max_new > 0 && r.prompt_len == 0))
+            return RC_ERR_ARG;
+        prompts[(size_t)i] = r.tokens;
+        lens[(size_t)i] = r.prompt_len;
+        reqs[i].admitted = 0;
+        reqs[i].node = -1;
+    }
+    std::vector<int32_t> order((size_t)n);
+    rc_status st = sched_order(c, policy, prompts.data(), lens.data(), n, order.data());
+    if (st != RC_OK) return st;
+    std::vector<int32_t> mslots;
+    int32_t count = 0;
+    for (int32_t k = 0; k < n; ++k) {
+        if (max_batch > 0 && count >= max_batch) break;
+        rc_request& r = reqs[order[(size_t)k]];
+        mslots.resize((size_t)std::max<int64_t>(r.prompt_len, 1));
+        int64_t m = 0;
+        rc_node node = 0;
+        st = rc_match_prefix(c, r.tokens, r.prompt_len, 1, &m, mslots.data(), &node);
+        if (st != RC_OK) return st;
+        const int64_t first = r.max_new > 0 ? std::min(m, r.prompt_len - 1) : m;
+        const int64_t need = r.prompt_len - first + r.max_new;
+        int32_t* dst = r.slots + first;
+        st = rc_alloc(c, need, dst);
+        if (st == RC_ERR_NOMEM) {
+            int64_t freed = 0, cnt = 0;
+            st = rc_evict(c, need - c->n_free, &freed, nullptr, 0, &cnt);
+            if (st != RC_OK) return st;
+            st = rc_alloc(c, need, dst);
+        }
+        if (st != RC_OK) {
+            if (st != RC_ERR_NOMEM) return st;
+            rc_status rs = rc_release(c, node);
+            if (rs != RC_OK) return rs;
+            break;  // the first request that does not fit stops the round
+        }
+        if (first) std::memcpy(r.slots, mslots.data(), (size_t)first * 4);
+        r.matched = m;
+        r.first = first;
+        r.node = node;
+        r.admitted = 1;
+        out_order[count++] = order[(size_t)k];
+    }
+    *n_admitted = count;
+    return RC_OK;
+}
+
+rc_status rc_commit(rc_cache* c, rc_request* reqs, const int32_t* idx, int32_t n, int mode) {
+    if (!c || n < 0 || (n > 0 && (!reqs || !idx)) || (mode != RC_COMMIT_PREFILL && mode != RC_COMMIT_FINISH))
+        return RC_ERR_ARG;
+    for (int32_t k = 0; k < n; ++k) {
+        rc_request& r = reqs[idx[k]];
+        if (mode == RC_COMMIT_FINISH && r.max_new == 0) continue;
+        const int64_t len = mode == RC_COMMIT_PREFILL ? r.prompt_len : r.prompt_len + r.max_new;
+        const int pin = mode == RC_COMMIT_PREFILL && r.max_new > 0;
+        int64_t present = 0;
+        rc_node node = -1;
+        rc_status st = rc_insert(c, r.tokens, r.slots, len, pin, &present, &node, r.slots);
+        if (st != RC_OK) return st;
+        st = rc_release(c, r.node);
+        if (st != RC_OK) return st;
+        r.node = pin ? node : -1;
     }
     return RC_OK;
 }

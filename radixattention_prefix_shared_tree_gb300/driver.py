@@ -24,12 +24,14 @@ launches; PyTorch only provides device memory and the stream.
 """
 from __future__ import annotations
 
+import ctypes as C
 from dataclasses import dataclass, field
 
 import numpy as np
 
-from . import (RC_ERR_NOMEM, RC_FCFS, RC_LPM, RC_OK, attn_decode, attn_decode_workspace, attn_extend,
-               kv_store, make_attn_desc, make_cascade, make_kv_table, make_pool_desc)
+from . import (RC_COMMIT_FINISH, RC_COMMIT_PREFILL, RC_ERR_NOMEM, RC_FCFS, RC_LPM, RC_OK, RCError, attn_decode,
+               attn_decode_workspace, attn_extend, kv_store, lib, make_attn_desc, make_cascade, make_kv_table,
+               make_pool_desc, rc_request)
 
 
 @dataclass
@@ -56,6 +58,16 @@ class SchedulerError(RuntimeError):
     pass
 
 
+_REQ_DTYPE = np.dtype([("tokens", "u8"), ("prompt_len", "i8"), ("max_new", "i8"), ("slots", "u8"),
+                       ("matched", "i8"), ("first", "i8"), ("node", "i8"), ("admitted", "i4"), ("_pad", "i4")])
+
+
+def _req_view(arr):
+    """Numpy view of a ctypes rc_request array (fields read without Python loops)."""
+    assert C.sizeof(rc_request) == _REQ_DTYPE.itemsize
+    return np.frombuffer(arr, dtype=_REQ_DTYPE)
+
+
 def _ok(st, what):
     if st != RC_OK:
         raise SchedulerError(f"{what} returned {st}")
@@ -72,10 +84,15 @@ class Scheduler:
         if self.log is not None:
             self.log.append(item)
 
+    def _native(self) -> bool:
+        return self.log is None and hasattr(self.cache, "admit_batch")
+
     def admit(self, pending: list, policy: int = RC_LPM, max_batch: int | None = None):
         """Admit requests in scheduling order; returns (admitted, still pending)."""
         if not pending:
             return [], []
+        if self._native():
+            return self._admit_native(pending, policy, max_batch)
         st, order = self.cache.sched_order(policy, [r.prompt for r in pending])
         _ok(st, "sched_order")
         self._rec("order", tuple(int(i) for i in order))
@@ -110,8 +127,49 @@ class Scheduler:
             admitted.append(r)
         return admitted, waiting
 
+    # ---- native batch path: the same rules, one C call per round
+    def _admit_native(self, pending, policy, max_batch):
+        n = len(pending)
+        arr = (rc_request * n)()
+        for i, r in enumerate(pending):
+            if r.tokens.dtype != np.int32 or not r.tokens.flags.c_contiguous:
+                r.tokens = np.ascontiguousarray(r.tokens, np.int32)
+            r.slots = np.empty(r.prompt_len + r.max_new, np.int32)
+            c = arr[i]
+            c.tokens = r.tokens.ctypes.data
+            c.prompt_len, c.max_new = r.prompt_len, r.max_new
+            c.slots = r.slots.ctypes.data
+        order = np.empty(n, np.int32)
+        st, cnt = self.cache.admit_batch(policy, arr, n, max_batch or 0, order)
+        _ok(st, "rc_admit")
+        view = _req_view(arr)
+        admitted = []
+        for k in range(cnt):
+            i = int(order[k])
+            r = pending[i]
+            r.matched, r.first, r.node = int(view["matched"][i]), int(view["first"][i]), int(view["node"][i])
+            r._batch = (arr, i)
+            admitted.append(r)
+        took = set(int(i) for i in order[:cnt])
+        waiting = [r for i, r in enumerate(pending) if i not in took]
+        return admitted, waiting
+
+    def _commit_native(self, batch, mode):
+        groups = {}
+        for r in batch:
+            arr, i = r._batch
+            groups.setdefault(id(arr), (arr, []))[1].append(i)
+        for arr, idx in groups.values():
+            _ok(self.cache.commit_batch(arr, idx, mode), "rc_commit")
+            view = _req_view(arr)
+            for r in batch:
+                if r._batch[0] is arr:
+                    r.node = int(view["node"][r._batch[1]])
+
     def commit_prompts(self, batch: list):
         """After prefill: insert each prompt, keep it pinned, drop the admission pin."""
+        if self._native() and all(hasattr(r, "_batch") for r in batch):
+            return self._commit_native(batch, RC_COMMIT_PREFILL)
         for r in batch:
             L = r.prompt_len
             st, present, node, canon = self.cache.insert(r.prompt, r.slots[:L], r.max_new > 0)
@@ -123,6 +181,8 @@ class Scheduler:
 
     def finish(self, batch: list):
         """After decode: insert prompt + generated tokens, unpin."""
+        if self._native() and all(hasattr(r, "_batch") for r in batch):
+            return self._commit_native(batch, RC_COMMIT_FINISH)
         for r in batch:
             if r.max_new == 0:
                 continue
@@ -219,6 +279,14 @@ class DeviceEngine:
             self._ws = self.torch.empty(int(nbytes * 1.25) + 256, dtype=self.torch.uint8, device=self.device)
         return self._ws
 
+    def pinned(self, arr):
+        """Host array -> pinned host tensor (from torch's caching host allocator,
+        which keeps the block until the asynchronous copy that reads it is done)."""
+        return self.torch.from_numpy(np.ascontiguousarray(arr)).pin_memory()
+
+    def to_device(self, arr):
+        return self.pinned(arr).to(self.device, non_blocking=True)
+
     def upload_batch(self, batch: list, cascade: bool):
         """Slot rows of the batch -> device table; returns the batch's device layout."""
         torch = self.torch
@@ -230,7 +298,7 @@ class DeviceEngine:
         if total > self.table.numel():
             self.table = torch.zeros(total, dtype=torch.int32, device=self.device)
         flat = np.concatenate([r.slots for r in batch]).astype(np.int32) if batch else np.zeros(0, np.int32)
-        self.table[:total].copy_(torch.from_numpy(flat), non_blocking=False)
+        self.table[:total].copy_(self.pinned(flat), non_blocking=True)
         lay = BatchLayout(self, batch, starts, cascade)
         return lay
 
@@ -244,6 +312,51 @@ class DeviceEngine:
         kv = lay.extend_table
         self._call("attn_extend", 1, ("extend", lay),
                    lambda: attn_extend(self.desc, q, lay.qo_indptr, kv, lay.batch_size, lay.max_q, out, lse))
+
+    # ---- decode loop: per-step arguments built once per batch, two C calls per step
+    def prepare_decode(self, lay):
+        T, B = lay.max_new, lay.batch_size
+        casc = lay.casc if lay.use_cascade else None
+        lay.kv_tables = [make_kv_table(self.table, lay.dec_start, lay.dec_len[t], int(lay.dec_max[t]))
+                         for t in range(T)]
+        sizes = {}
+        for kv in lay.kv_tables:
+            if kv.max_len not in sizes:
+                sizes[kv.max_len] = attn_decode_workspace(self.desc, B, kv.max_len, casc)
+        lay.ws_bytes = max(sizes.values()) if sizes else 256
+        lay.ws = self.workspace(lay.ws_bytes)
+        lay.casc_ref = C.byref(casc) if casc is not None else None
+        lay.slot_ptrs = [lay.decode_slots[t].data_ptr() for t in range(T)]
+        # kernels per step: cascade (if any) + table pass + merge when a row is split
+        sms = self.torch.cuda.get_device_properties(self.device).multi_processor_count
+        split = B * self.shape.kv_heads < 8 * sms
+        lay.decode_kernels = (1 if casc is not None else 0) + 1 + (1 if split else 0)
+        lay.stream = C.c_void_p(self.torch.cuda.current_stream(self.device).cuda_stream)
+
+    def decode_step(self, lay, t: int, q, k, v, out, lse=None):
+        L = lib()
+        B = lay.batch_size
+        ev = None
+        if self.timing:
+            ev = (self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True),
+                  self.torch.cuda.Event(enable_timing=True))
+            ev[0].record()
+        st = L.kv_store(C.byref(self.pool), lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
+                        B, None, None, lay.stream)
+        if st != RC_OK:
+            raise RCError("kv_store", st)
+        if ev:
+            ev[1].record()
+        st = L.attn_decode(C.byref(self.desc), q.data_ptr(), C.byref(lay.kv_tables[t]), B, lay.casc_ref,
+                           out.data_ptr(), lse.data_ptr() if lse is not None else None, lay.ws.data_ptr(),
+                           lay.ws_bytes, lay.stream)
+        if st != RC_OK:
+            raise RCError("attn_decode", st)
+        if ev:
+            ev[2].record()
+            self.events.setdefault("kv_store", []).append((ev[0], ev[1], ("store", B)))
+            self.events.setdefault("attn_decode", []).append((ev[1], ev[2], ("decode", lay, t)))
+        self.launches += 1 + lay.decode_kernels
 
     def decode(self, lay, t: int, q, out, lse=None):
         kv, casc = lay.decode_table(t)
@@ -272,7 +385,7 @@ class BatchLayout:
         qo[1:] = np.cumsum(n_new)
         self.qo_host = qo
         self.max_q = int(n_new.max()) if B else 0
-        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+        i32 = lambda a: eng.to_device(np.asarray(a, dtype=np.int32))
         self.qo_indptr = i32(qo)
         self.start_dev = i32(starts)
         self.len_prompt = i32(L)
@@ -312,7 +425,8 @@ class BatchLayout:
                 req_pos = np.concatenate([np.asarray(x, np.int64) for x in pos_of]) if len(seg_rows) else np.zeros(0)
                 self._casc_arrays = [i32(seg_slots), i32(seg_indptr), i32(seg_row_indptr), i32(seg_rows),
                                      i32(req_indptr), i32(req_pos)]
-                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=max(len(rw) for rw in rows))
+                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=max(len(rw) for rw in rows),
+                                         max_seg_len=max(len(sg) for sg, _ in segs))
             else:
                 self.use_cascade = False
         self.dec_start = i32(starts + self.private)

@@ -36,6 +36,8 @@ class Runner:
         self.extend_out = {}   # rid -> (positions, out bf16 [n, Hq, dv], lse [n, Hq])
         self.decode_out = {}   # rid -> list of (position, out [Hq, dv], lse [Hq])
         self.next_rid = 0
+        self.on_decode = None   # optional callback(out) after each decode step
+        self.on_extend = None   # optional callback(out) after the prefill
 
     def request(self, prompt, max_new: int) -> Request:
         r = new_request(self.model, self.next_rid, prompt, max_new)
@@ -68,6 +70,8 @@ class Runner:
         out = torch.empty(total, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
         lse = torch.empty(total, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
         eng.extend(lay, inp["q"], out, lse)
+        if self.on_extend is not None:
+            self.on_extend(out)
         if self.collect:
             o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
             for i, r in enumerate(batch):
@@ -82,10 +86,12 @@ class Runner:
         B = len(batch)
         out = torch.empty(B, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
         lse = torch.empty(B, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
+        eng.prepare_decode(lay)
         for t in range(lay.max_new):
             inp = self.model.decode_inputs(batch, t)
-            eng.store(lay.decode_slots[t], inp["k"], inp["v"])
-            eng.decode(lay, t, inp["q"], out, lse)
+            eng.decode_step(lay, t, inp["q"], inp["k"], inp["v"], out, lse)
+            if self.on_decode is not None:
+                self.on_decode(out)
             if self.collect:
                 o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
                 for i, r in enumerate(batch):

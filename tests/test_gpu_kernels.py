@@ -216,7 +216,8 @@ def test_cascade_equals_flat_and_oracle(cuda, Hq, Hkv, D):
     req_pos = np.concatenate([np.asarray(x, np.int32) for x in pos_of])
     T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(cuda)
     arrs = [T(seg_slots), T(seg_indptr), T(seg_row_indptr), T(seg_rows), T(req_indptr), T(req_pos)]
-    casc = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs))
+    casc = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs),
+                           max_seg_len=max(len(x) for x, _ in segs))
     pstart = T(start.cpu().numpy() + private)
     plen = T(np.asarray(lens) - private)
     kv2 = ra.make_kv_table(table, pstart, plen, int((np.asarray(lens) - private).max()))
@@ -243,3 +244,49 @@ def test_decode_reports_len_above_max_len(cuda):
     out = torch.empty(2, 32, 128, dtype=torch.bfloat16, device=cuda)
     ra.attn_decode(desc, q, kv, 2, out, None, ws)
     assert ra.rc_sync(pool.err) == ra.RC_ERR_DEVICE
+
+
+def test_cascade_fused_path_with_empty_tails(cuda):
+    """Enough rows that each (row, KV head) is one CTA (merge fused into it);
+    some rows have every key in shared segments (empty private part)."""
+    Hq, Hkv, D = 32, 8, 128
+    n_slots = 30000
+    pool = Pool(n_slots, Hkv, D, cuda, 5)
+    rng = np.random.default_rng(21)
+    perm = rng.permutation(n_slots).astype(np.int32)
+    root = perm[:1500]
+    mids = [perm[1500:1700], perm[1700:1990]]
+    off = 1990
+    rows, private = [], []
+    B = 48
+    for b in range(B):
+        mid = mids[b % 2]
+        tail_len = 0 if b % 5 == 0 else int(rng.integers(1, 200))
+        tail = perm[off:off + tail_len]
+        off += tail_len
+        rows.append(np.concatenate([root, mid, tail]).astype(np.int32))
+        private.append(len(root) + len(mid))
+    lens = [len(r) for r in rows]
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(cuda)
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    table = T(np.concatenate(rows))
+    segs = [(root, list(range(B))), (mids[0], list(range(0, B, 2))), (mids[1], list(range(1, B, 2)))]
+    seg_rows = np.concatenate([np.asarray(r, np.int32) for _, r in segs])
+    pos_of = [[p for p, b in enumerate(seg_rows) if b == bb] for bb in range(B)]
+    arrs = [T(np.concatenate([s for s, _ in segs])), T(np.concatenate([[0], np.cumsum([len(s) for s, _ in segs])])),
+            T(np.concatenate([[0], np.cumsum([len(r) for _, r in segs])])), T(seg_rows),
+            T(np.concatenate([[0], np.cumsum([len(x) for x in pos_of])])), T(np.concatenate(pos_of))]
+    casc = ra.make_cascade(*arrs, max_seg_rows=B, max_seg_len=len(root))
+    private = np.asarray(private)
+    plen = np.asarray(lens) - private
+    kv = ra.make_kv_table(table, T(starts + private), T(plen), int(plen.max()))
+    g = torch.Generator().manual_seed(9)
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    desc = ra.make_attn_desc(pool.desc, Hq, 1.0 / np.sqrt(D))
+    ws = torch.empty(ra.attn_decode_workspace(desc, B, kv.max_len, casc), dtype=torch.uint8, device=cuda)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_decode(desc, q, kv, B, out, lse, ws, cascade=casc)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    ref, ref_lse = _oracle_rows(pool, rows, bits(q), lens, Hq, Hkv, D, 1.0 / np.sqrt(D))
+    check(bits(out), ref, lse.cpu().numpy(), ref_lse)

@@ -128,3 +128,36 @@ def test_full_chat_host_trace_bit_exact(built):
         outs.append((log, cache.stats(), rounds))
     assert outs[0] == outs[1]
     assert outs[1][1]["evicted_tokens"] > 0
+
+
+def _native_vs_per_call(trace_fn, runner_fn, pool):
+    """The scheduler's native batch path (rc_admit / rc_commit) against its
+    per-call path (which the tests above pin to the oracle)."""
+    out = []
+    for log in (None, []):
+        tr = trace_fn()
+        cache = ra.RadixCache(pool(tr))
+        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=log)
+        res = runner_fn(runner, tr)
+        reqs = res[0] if isinstance(res, tuple) else res
+        rows = sorted((r.rid, r.matched, r.first, tuple(int(x) for x in r.slots)) for r in reqs)
+        out.append((cache.dump(), cache.stats(), rows))
+    assert out[0] == out[1]
+
+
+def test_native_batch_scheduler_equals_per_call_few_shot(built):
+    _native_vs_per_call(lambda: traces.few_shot(n_questions=40, max_new=8), wl.run_few_shot, lambda tr: 1 << 15)
+
+
+def test_native_batch_scheduler_equals_per_call_chat_with_eviction(built):
+    def small():
+        tr = traces.chat(n_sessions=20, n_turns=4, umin=16, umax=64, max_new=16)
+        tr.max_batch = 7
+        return tr
+    _native_vs_per_call(small, wl.run_chat, lambda tr: tr.pool_slots)
+
+
+def test_native_batch_scheduler_equals_per_call_tiny_and_agent(built):
+    _native_vs_per_call(traces.tiny, wl.run_tiny, lambda tr: tr.pool_slots)
+    _native_vs_per_call(lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8), wl.run_agent,
+                        lambda tr: 4096)

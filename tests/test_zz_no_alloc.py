@@ -58,7 +58,8 @@ def _case(dev, seed, Hq, Hkv, D, lens, n_slots=12000):
             T(np.concatenate([[0], np.cumsum([len(r) for _, r in segs])])), T(seg_rows),
             T(np.concatenate([[0], np.cumsum([len(x) for x in pos_of])])), T(np.concatenate(pos_of))]
     state["casc_arrays"] = arrs
-    state["casc"] = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs))
+    state["casc"] = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs),
+                           max_seg_len=max(len(x) for x, _ in segs))
     state["pstart"], state["plen"] = T(starts + private), T(np.asarray(full) - private)
     state["kv_tail"] = ra.make_kv_table(state["table"], state["pstart"], state["plen"],
                                         int((np.asarray(full) - private).max()))
@@ -117,11 +118,17 @@ def test_static_scratch_refuses_oversized_batch():
     __graft_entry__.build()
     dev = torch.device("cuda:0")
     st = _case(dev, 3, 32, 8, 128, [10, 10])
-    # a batch whose partials exceed the fixed area: refused before any launch
+    # a batch whose partials exceed the fixed area (4096 rows reading one
+    # shared segment): refused before any launch
     big_b = 4096
-    kv = ra.make_kv_table(st["table"], st["start"], st["len"], 1 << 15)
-    need = ra.attn_decode_workspace(st["desc"], big_b, 1 << 15)
+    kv = ra.make_kv_table(st["table"], st["start"], st["len"], 64)
+    casc = ra.rc_cascade()
+    casc.n_seg, casc.max_seg_len, casc.max_seg_rows, casc.total_seg_rows = 1, 1000, big_b, big_b
+    for name, t in zip(("seg_slots", "seg_indptr", "seg_row_indptr", "seg_rows", "req_seg_indptr", "req_seg_pos"),
+                       st["casc_arrays"]):
+        setattr(casc, name, t.data_ptr())
+    need = ra.attn_decode_workspace(st["desc"], big_b, 64, casc)
     assert need > ra.RC_STATIC_SCRATCH_BYTES
     out = torch.empty(1, dtype=torch.bfloat16, device=dev)
-    assert ra.attn_decode_static(st["desc"], st["q"], kv, big_b, out) == ra.RC_ERR_SCRATCH
+    assert ra.attn_decode_static(st["desc"], st["q"], kv, big_b, out, cascade=casc) == ra.RC_ERR_SCRATCH
     assert "scratch" in ra.rc_strerror(ra.RC_ERR_SCRATCH)
