@@ -142,9 +142,9 @@ class ReplayModel:
         ext = self.base.rows(ext_h)
         dec = self.base.rows(dec_h.reshape(-1))
         B = len(reqs)
-        entry = {"ext": ext, "dec": {k: (v.view(T, B, *v.shape[1:]) if v is not None else None)
-                                     for k, v in dec.items()},
-                 "first": first}
+        dec = {k: (v.view(T, B, *v.shape[1:]) if v is not None else None) for k, v in dec.items()}
+        entry = {"ext": ext, "dec": dec, "first": first,
+                 "dec_steps": [{k: (v[t] if v is not None else None) for k, v in dec.items()} for t in range(T)]}
         self.ready[tuple(r.rid for r in reqs)] = entry
         return entry
 
@@ -158,6 +158,7 @@ class ReplayModel:
         e["dec_dev"] = {k: (torch_empty_like(self.torch, v[0]) if v is not None else None)
                         for k, v in e["dec"].items()}
         e["dec"] = None
+        e["dec_steps"] = None
 
     def _entry(self, batch):
         key = tuple(r.rid for r in batch)
@@ -185,7 +186,7 @@ class ReplayModel:
                     self.h2d_bytes += v.numel() * v.element_size()
                 out[k] = v
             return out
-        return {k: (v[t] if v is not None else None) for k, v in e["dec"].items()}
+        return e["dec_steps"][t]
 
 
 def torch_empty_like(torch, t):
@@ -352,8 +353,7 @@ def main():
     assert ra.rc_sync(eng.err) == ra.RC_OK
 
     # ---------------------------------------------------------- timed region
-    eng.events.clear()
-    eng.timing = True
+    eng.start_timing(4 * (args.steps * (args.max_new * 3 + 8)) + 64)
     launches0 = eng.launches
     st0 = cache.stats()
     clocks = ClockSampler(local)

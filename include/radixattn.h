@@ -178,6 +178,26 @@ rc_status rc_admit(rc_cache* cache, int policy, rc_request* reqs, int32_t n, int
 #define RC_COMMIT_FINISH  1
 rc_status rc_commit(rc_cache* cache, rc_request* reqs, const int32_t* idx, int32_t n, int mode);
 
+/* Cascade segments of a running batch, read off the tree [N49 s.1: the
+ * shared parts of layered prompts form a tree]: every node on the pinned path
+ * of at least two of the n requests (nodes[i] = request i's pinned node) is a
+ * segment, read once for all of them.  Request i's own keys start after the
+ * last shared node on its path (a node shared by several requests is shared
+ * in full: their matches split edges at every divergence).
+ * Outputs (caller buffers): seg_slots (cap seg_slots_cap), seg_indptr (n_seg+1),
+ * seg_row_indptr (n_seg+1), seg_rows and req_seg_pos (cap rows_cap),
+ * req_seg_indptr (n+1), private_start (n); *n_seg, *n_seg_slots, *total_rows,
+ * *max_seg_len, *max_seg_rows.  Segments come in depth-first order of first
+ * appearance; rows within a segment ascend.  seg_cap bounds n_seg.
+ * Errors: RC_ERR_ARG (bad pointers), RC_ERR_STATE (unknown node),
+ * RC_ERR_NOMEM (a buffer is too small). */
+rc_status rc_cascade_plan(rc_cache* cache, const rc_node* nodes, int32_t n, int32_t* seg_slots,
+                          int64_t seg_slots_cap, int32_t* seg_indptr, int32_t* seg_row_indptr,
+                          int32_t* seg_rows, int32_t* req_seg_indptr, int32_t* req_seg_pos,
+                          int64_t rows_cap, int64_t* private_start, int32_t seg_cap, int32_t* n_seg,
+                          int64_t* n_seg_slots, int32_t* total_rows, int32_t* max_seg_len,
+                          int32_t* max_seg_rows);
+
 typedef struct rc_stats_t {
     int64_t pool_slots, free_slots, caller_slots, tree_tokens, nodes;
     int64_t match_calls, match_tokens, match_hits, match_hit_tokens;

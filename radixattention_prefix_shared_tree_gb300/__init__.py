@@ -80,6 +80,8 @@ SIGNATURES = {
     "rc_stats": (I32, [VP, P(rc_stats_t)]),
     "rc_admit": (I32, [VP, C.c_int, VP, I32, I32, VP, P(I32)]),
     "rc_commit": (I32, [VP, VP, VP, I32, C.c_int]),
+    "rc_cascade_plan": (I32, [VP, VP, I32, VP, I64, VP, VP, VP, VP, VP, I64, VP, I32, P(I32), P(I64), P(I32),
+                              P(I32), P(I32)]),
     "rc_dump": (I32, [VP, C.c_char_p, I64, P(I64)]),
     "kv_store": (I32, [P(rc_pool_desc), VP, VP, VP, I32, VP, VP, VP]),
     "attn_decode_workspace": (I32, [P(rc_attn_desc), I32, I32, P(rc_cascade), P(C.c_size_t)]),
@@ -223,6 +225,36 @@ def rc_admit(handle, policy: int, reqs, n: int, max_batch: int, out_order):
     return st, cnt.value
 
 
+def rc_cascade_plan(handle, nodes):
+    """Cascade segments of the requests pinned at `nodes` (see the header).
+    Returns a dict of numpy arrays and bounds."""
+    nodes = np.ascontiguousarray(nodes, dtype=np.int64)
+    n = len(nodes)
+    cap_slots, cap_rows, cap_seg = 1 << 16, 1 << 12, 1 << 10
+    while True:
+        seg_slots = np.empty(cap_slots, np.int32)
+        seg_indptr = np.empty(cap_seg + 1, np.int32)
+        seg_row_indptr = np.empty(cap_seg + 1, np.int32)
+        seg_rows = np.empty(cap_rows, np.int32)
+        req_seg_pos = np.empty(cap_rows, np.int32)
+        req_seg_indptr = np.empty(n + 1, np.int32)
+        private = np.empty(max(n, 1), np.int64)
+        ns, nsl, tot, mlen, mrows = I32(0), I64(0), I32(0), I32(0), I32(0)
+        st = lib().rc_cascade_plan(handle, _np_ptr(nodes), n, _np_ptr(seg_slots), cap_slots, _np_ptr(seg_indptr),
+                                   _np_ptr(seg_row_indptr), _np_ptr(seg_rows), _np_ptr(req_seg_indptr),
+                                   _np_ptr(req_seg_pos), cap_rows, _np_ptr(private), cap_seg, C.byref(ns),
+                                   C.byref(nsl), C.byref(tot), C.byref(mlen), C.byref(mrows))
+        if st == RC_ERR_NOMEM:
+            cap_slots, cap_rows, cap_seg = cap_slots * 8, cap_rows * 8, cap_seg * 8
+            continue
+        _check("rc_cascade_plan", st)
+        k = ns.value
+        return dict(n_seg=k, seg_slots=seg_slots[:nsl.value], seg_indptr=seg_indptr[:k + 1],
+                    seg_row_indptr=seg_row_indptr[:k + 1], seg_rows=seg_rows[:tot.value],
+                    req_seg_indptr=req_seg_indptr, req_seg_pos=req_seg_pos[:tot.value], private=private[:n],
+                    max_seg_len=mlen.value, max_seg_rows=mrows.value)
+
+
 def rc_commit(handle, reqs, idx, mode: int):
     idx = _i32(idx)
     return lib().rc_commit(handle, C.cast(reqs, VP), _np_ptr(idx), len(idx), int(mode))
@@ -276,6 +308,9 @@ class RadixCache:
 
     def commit_batch(self, reqs, idx, mode):
         return rc_commit(self._h, reqs, idx, mode)
+
+    def cascade_plan(self, nodes):
+        return rc_cascade_plan(self._h, nodes)
 
     def stats(self) -> dict:
         return {_STAT_RENAME.get(k, k): v for k, v in rc_stats(self._h).items()}

@@ -279,40 +279,85 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
             n_parts = (p.req_seg_indptr[b + 1] - e0) * p.seg_chunks;
         }
         const int sc = p.seg_chunks;
-        auto part_row = [&](int j) -> int64_t {
-            return (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc);
-        };
+        // partial j of head h is row part_row(j) + h_off; resolved into a
+        // per-warp table (batches of 32) so the element loop has no chains
+        constexpr int kPB = 32;
+        int64_t* sRow = reinterpret_cast<int64_t*>(sOwn + 8);   // [kPB]
+        float* sW = reinterpret_cast<float*>(sRow + kPB);        // [G][kPB]
+        float* sHead = sW + G * kPB;                             // [G][2]: final max, 1/weight sum
+        // pass 1: final max and weight sum per head over all partials
         for (int h = 0; h < G; ++h) {
-            const int head = kvh * G + h;
-            const int64_t hoff = (int64_t)head * sc;
-            const float own = sOwn[h];
-            float m = own;
-            for (int j = lane; j < n_parts; j += 32) m = fmaxf(m, p.seg_lse[part_row(j) + hoff]);
+            const int64_t hoff = (int64_t)(kvh * G + h) * sc;
+            float m = sOwn[h];
+            for (int j = lane; j < n_parts; j += 32) {
+                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc) + hoff;
+                m = fmaxf(m, p.seg_lse[row]);
+            }
 #pragma unroll
             for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
             float w = 0.f;
             for (int j = lane; j < n_parts; j += 32) {
-                const float l2 = p.seg_lse[part_row(j) + hoff];
+                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc) + hoff;
+                const float l2 = p.seg_lse[row];
                 w += l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m);
             }
 #pragma unroll
             for (int k = 16; k > 0; k >>= 1) w += __shfl_xor_sync(0xffffffffu, w, k);
-            const float wo = own == -INFINITY ? 0.f : rc::fast_exp2(own - m);
-            w += wo;
-            const float invw = w > 0.f ? 1.f / w : 0.f;
-            const int64_t orow = (int64_t)b * p.q_heads + head;
-            for (int d = lane; d < D; d += 32) {
-                float acc = wo * sE[h * D + d];
-#pragma unroll 4
-                for (int j = 0; j < n_parts; ++j) {
-                    const int64_t row = part_row(j) + hoff;
-                    const float l2 = p.seg_lse[row];
-                    const float v = p.seg_o[row * D + d];
-                    acc += l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m) * v;
-                }
-                p.out[orow * D + d] = __float2bfloat16_rn(acc * invw);
+            const float own = sOwn[h];
+            w += own == -INFINITY ? 0.f : rc::fast_exp2(own - m);
+            if (lane == 0) {
+                sHead[2 * h] = m;
+                sHead[2 * h + 1] = w > 0.f ? 1.f / w : 0.f;
             }
-            if (p.lse && lane == 0) p.lse[orow] = w > 0.f ? (m + log2f(w)) * rc::kLn2 : -INFINITY;
+        }
+        __syncwarp();
+        // pass 2: own part, then the partials batch by batch
+        float acc[G][D / 32];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float own = sOwn[h];
+            const float wo = own == -INFINITY ? 0.f : rc::fast_exp2(own - sHead[2 * h]) * sHead[2 * h + 1];
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) acc[h][k] = wo * sE[h * D + lane + 32 * k];
+        }
+        for (int j0 = 0; j0 < n_parts; j0 += kPB) {
+            const int nb = min(kPB, n_parts - j0);
+            if (lane < nb) {
+                const int j = j0 + lane;
+                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc);
+                sRow[lane] = row;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float l2 = p.seg_lse[row + (int64_t)(kvh * G + h) * sc];
+                    sW[h * kPB + lane] =
+                        l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - sHead[2 * h]) * sHead[2 * h + 1];
+                }
+            }
+            __syncwarp();
+            for (int jj = 0; jj < nb; ++jj) {
+                const int64_t row = sRow[jj];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float w = sW[h * kPB + jj];
+                    const float* src = p.seg_o + (row + (int64_t)(kvh * G + h) * sc) * D + lane;
+#pragma unroll
+                    for (int k = 0; k < D / 32; ++k) {
+                        const float v = src[32 * k];
+                        acc[h][k] += w == 0.f ? 0.f : w * v;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const int64_t orow = (int64_t)b * p.q_heads + kvh * G + h;
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k)
+                p.out[orow * D + lane + 32 * k] = __float2bfloat16_rn(acc[h][k]);
+            if (p.lse && lane == 0)
+                p.lse[orow] = sHead[2 * h + 1] > 0.f ? (sHead[2 * h] - log2f(sHead[2 * h + 1])) * rc::kLn2
+                                                     : -INFINITY;
         }
     }
 }

@@ -509,6 +509,81 @@ rc_status rc_commit(rc_cache* c, rc_request* reqs, const int32_t* idx, int32_t n
     return RC_OK;
 }
 
+rc_status rc_cascade_plan(rc_cache* c, const rc_node* nodes, int32_t n, int32_t* seg_slots, int64_t seg_slots_cap,
+                          int32_t* seg_indptr, int32_t* seg_row_indptr, int32_t* seg_rows, int32_t* req_seg_indptr,
+                          int32_t* req_seg_pos, int64_t rows_cap, int64_t* private_start, int32_t seg_cap,
+                          int32_t* n_seg, int64_t* n_seg_slots, int32_t* total_rows, int32_t* max_seg_len,
+                          int32_t* max_seg_rows) {
+    if (!c || n < 0 || (n > 0 && !nodes) || !seg_indptr || !seg_row_indptr || !req_seg_indptr || !private_start ||
+        !n_seg || !n_seg_slots || !total_rows || !max_seg_len || !max_seg_rows || seg_cap < 0)
+        return RC_ERR_ARG;
+    // paths root..node (root excluded), as record indices
+    std::vector<std::vector<int32_t>> paths((size_t)n);
+    std::unordered_map<int32_t, int32_t> uses;
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = c->by_id.find(nodes[i]);
+        if (it == c->by_id.end()) return RC_ERR_STATE;
+        for (int32_t k = it->second; k > 0; k = c->recs[(size_t)k].parent) paths[(size_t)i].push_back(k);
+        std::reverse(paths[(size_t)i].begin(), paths[(size_t)i].end());
+        for (int32_t k : paths[(size_t)i]) uses[k] += 1;
+    }
+    // segments in order of first appearance along the requests' paths
+    std::unordered_map<int32_t, int32_t> seg_of;
+    std::vector<int32_t> seg_rec;
+    for (int32_t i = 0; i < n; ++i)
+        for (int32_t k : paths[(size_t)i]) {
+            if (uses[k] < 2) break;
+            if (seg_of.emplace(k, (int32_t)seg_rec.size()).second) seg_rec.push_back(k);
+        }
+    const int32_t ns = (int32_t)seg_rec.size();
+    if (ns > seg_cap) return RC_ERR_NOMEM;
+    std::vector<std::vector<int32_t>> rows_of((size_t)ns);
+    req_seg_indptr[0] = 0;
+    int64_t pos_total = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        int64_t priv = 0;
+        for (int32_t k : paths[(size_t)i]) {
+            if (uses[k] < 2) break;
+            rows_of[(size_t)seg_of[k]].push_back(i);
+            priv += c->recs[(size_t)k].len;
+            pos_total += 1;
+        }
+        private_start[i] = priv;
+    }
+    if (pos_total > rows_cap || (pos_total > 0 && (!seg_rows || !req_seg_pos))) return RC_ERR_NOMEM;
+    int64_t nslots = 0;
+    int32_t mlen = 0, mrows = 0, rpos = 0;
+    seg_indptr[0] = 0;
+    seg_row_indptr[0] = 0;
+    std::vector<std::vector<int32_t>> pos_of((size_t)n);
+    for (int32_t s = 0; s < ns; ++s) {
+        const Rec& r = c->recs[(size_t)seg_rec[(size_t)s]];
+        if (nslots + r.len > seg_slots_cap || !seg_slots) return RC_ERR_NOMEM;
+        std::memcpy(seg_slots + nslots, c->slot_arena.data() + r.off, (size_t)r.len * 4);
+        nslots += r.len;
+        seg_indptr[s + 1] = (int32_t)nslots;
+        mlen = std::max(mlen, r.len);
+        const auto& rw = rows_of[(size_t)s];
+        mrows = std::max(mrows, (int32_t)rw.size());
+        for (int32_t b : rw) {
+            pos_of[(size_t)b].push_back(rpos);
+            seg_rows[rpos++] = b;
+        }
+        seg_row_indptr[s + 1] = rpos;
+    }
+    int32_t q = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        for (int32_t p2 : pos_of[(size_t)i]) req_seg_pos[q++] = p2;
+        req_seg_indptr[i + 1] = q;
+    }
+    *n_seg = ns;
+    *n_seg_slots = nslots;
+    *total_rows = rpos;
+    *max_seg_len = mlen;
+    *max_seg_rows = mrows;
+    return RC_OK;
+}
+
 rc_status rc_stats(rc_cache* c, rc_stats_t* o) {
     if (!c || !o) return RC_ERR_ARG;
     o->pool_slots = c->pool;

@@ -236,6 +236,26 @@ def plan_cascade(rows: list):
     return segs, private
 
 
+def plan_from_rows(rows: list) -> dict:
+    """plan_cascade in the dictionary form of rc_cascade_plan."""
+    segs, private = plan_cascade(rows)
+    B = len(rows)
+    if not segs:
+        return dict(n_seg=0, private=private)
+    seg_rows = np.concatenate([np.asarray(rw, np.int64) for _, rw in segs])
+    pos_of = [[] for _ in range(B)]
+    for p_, b in enumerate(seg_rows):
+        pos_of[int(b)].append(p_)
+    return dict(n_seg=len(segs), seg_slots=np.concatenate([sg for sg, _ in segs]).astype(np.int32),
+                seg_indptr=np.concatenate([[0], np.cumsum([len(sg) for sg, _ in segs])]).astype(np.int32),
+                seg_row_indptr=np.concatenate([[0], np.cumsum([len(rw) for _, rw in segs])]).astype(np.int32),
+                seg_rows=seg_rows.astype(np.int32),
+                req_seg_indptr=np.concatenate([[0], np.cumsum([len(x) for x in pos_of])]).astype(np.int32),
+                req_seg_pos=np.concatenate([np.asarray(x, np.int64) for x in pos_of]).astype(np.int32),
+                private=private, max_seg_len=max(len(sg) for sg, _ in segs),
+                max_seg_rows=max(len(rw) for _, rw in segs))
+
+
 # ------------------------------------------------------------------- device
 class DeviceEngine:
     """KV pool + slot tables in HBM and the kernel launches of one batch."""
@@ -260,12 +280,27 @@ class DeviceEngine:
         self.timing = False          # record CUDA events around every device call
         self.events = {}             # call name -> [(start, end, info)]
         self.launches = 0            # kernels launched by the library (counted per call)
+        self._ev_pool = []
+
+    def start_timing(self, n_events: int = 4096):
+        """Record CUDA events around device calls, from a pool made up front."""
+        self.events = {}
+        self._ev_pool = [self.torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+        self._ev_next = 0
+        self.timing = True
+
+    def _event(self):
+        if self._ev_next < len(self._ev_pool):
+            e = self._ev_pool[self._ev_next]
+            self._ev_next += 1
+            return e
+        return self.torch.cuda.Event(enable_timing=True)
 
     def _call(self, name, kernels, info, fn):
         if self.timing:
             st = self.torch.cuda.current_stream()
-            a = self.torch.cuda.Event(enable_timing=True)
-            b = self.torch.cuda.Event(enable_timing=True)
+            a = self._event()
+            b = self._event()
             a.record(st)
             fn()
             b.record(st)
@@ -287,7 +322,7 @@ class DeviceEngine:
     def to_device(self, arr):
         return self.pinned(arr).to(self.device, non_blocking=True)
 
-    def upload_batch(self, batch: list, cascade: bool):
+    def upload_batch(self, batch: list, cascade: bool, planner=None):
         """Slot rows of the batch -> device table; returns the batch's device layout."""
         torch = self.torch
         lens = np.asarray([len(r.slots) for r in batch], np.int64)
@@ -299,7 +334,7 @@ class DeviceEngine:
             self.table = torch.zeros(total, dtype=torch.int32, device=self.device)
         flat = np.concatenate([r.slots for r in batch]).astype(np.int32) if batch else np.zeros(0, np.int32)
         self.table[:total].copy_(self.pinned(flat), non_blocking=True)
-        lay = BatchLayout(self, batch, starts, cascade)
+        lay = BatchLayout(self, batch, starts, cascade, planner)
         return lay
 
     # -- kernels
@@ -338,8 +373,7 @@ class DeviceEngine:
         B = lay.batch_size
         ev = None
         if self.timing:
-            ev = (self.torch.cuda.Event(enable_timing=True), self.torch.cuda.Event(enable_timing=True),
-                  self.torch.cuda.Event(enable_timing=True))
+            ev = (self._event(), self._event(), self._event())
             ev[0].record()
         st = L.kv_store(C.byref(self.pool), lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
                         B, None, None, lay.stream)
@@ -369,7 +403,7 @@ class DeviceEngine:
 class BatchLayout:
     """Device-side index arrays of one admitted batch."""
 
-    def __init__(self, eng: DeviceEngine, batch: list, starts: np.ndarray, cascade: bool):
+    def __init__(self, eng: DeviceEngine, batch: list, starts: np.ndarray, cascade: bool, planner=None):
         torch = eng.torch
         dev = eng.device
         self.eng = eng
@@ -406,27 +440,21 @@ class BatchLayout:
         self.private = np.zeros(B, np.int64)
         self.casc = None
         if self.use_cascade:
-            segs, private = plan_cascade([r.slots[:r.prompt_len] for r in batch])
-            if segs:
-                self.private = private
-                self.segments = segs
-                seg_slots = np.concatenate([s for s, _ in segs]).astype(np.int32)
-                seg_indptr = np.zeros(len(segs) + 1, np.int64)
-                seg_indptr[1:] = np.cumsum([len(s) for s, _ in segs])
-                rows = [rw for _, rw in segs]
-                seg_row_indptr = np.zeros(len(segs) + 1, np.int64)
-                seg_row_indptr[1:] = np.cumsum([len(rw) for rw in rows])
-                seg_rows = np.concatenate([np.asarray(rw, np.int64) for rw in rows])
-                pos_of = [[] for _ in range(B)]
-                for p, b in enumerate(seg_rows):
-                    pos_of[int(b)].append(p)
-                req_indptr = np.zeros(B + 1, np.int64)
-                req_indptr[1:] = np.cumsum([len(x) for x in pos_of])
-                req_pos = np.concatenate([np.asarray(x, np.int64) for x in pos_of]) if len(seg_rows) else np.zeros(0)
-                self._casc_arrays = [i32(seg_slots), i32(seg_indptr), i32(seg_row_indptr), i32(seg_rows),
-                                     i32(req_indptr), i32(req_pos)]
-                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=max(len(rw) for rw in rows),
-                                         max_seg_len=max(len(sg) for sg, _ in segs))
+            plan = None
+            if planner is not None and all(r.node >= 0 for r in batch):
+                plan = planner(np.asarray([r.node for r in batch], np.int64))   # read off the tree
+            else:
+                plan = plan_from_rows([r.slots[:r.prompt_len] for r in batch])
+            if plan["n_seg"] > 0:
+                self.private = plan["private"].astype(np.int64)
+                ip = plan["seg_indptr"]
+                self.segments = [(plan["seg_slots"][ip[k]:ip[k + 1]],
+                                  plan["seg_rows"][plan["seg_row_indptr"][k]:plan["seg_row_indptr"][k + 1]])
+                                 for k in range(plan["n_seg"])]
+                self._casc_arrays = [i32(plan[k]) for k in ("seg_slots", "seg_indptr", "seg_row_indptr", "seg_rows",
+                                                            "req_seg_indptr", "req_seg_pos")]
+                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=plan["max_seg_rows"],
+                                         max_seg_len=plan["max_seg_len"])
             else:
                 self.use_cascade = False
         self.dec_start = i32(starts + self.private)

@@ -80,7 +80,8 @@ class Runner:
 
     def _decode(self, batch):
         eng, torch = self.engine, self.engine.torch
-        lay = eng.upload_batch(batch, cascade=self.cascade)
+        planner = getattr(self.cache, "cascade_plan", None)
+        lay = eng.upload_batch(batch, cascade=self.cascade, planner=planner)
         self.last_layout = lay
         sh = eng.shape
         B = len(batch)

@@ -161,3 +161,39 @@ def test_native_batch_scheduler_equals_per_call_tiny_and_agent(built):
     _native_vs_per_call(traces.tiny, wl.run_tiny, lambda tr: tr.pool_slots)
     _native_vs_per_call(lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8), wl.run_agent,
                         lambda tr: 4096)
+
+
+@pytest.mark.parametrize("which", ["few_shot", "agent"])
+def test_tree_cascade_plan_equals_slot_row_plan(built, which):
+    """rc_cascade_plan (read off the pinned paths of the tree) finds the same
+    segments, rows and private starts as the compressed trie of slot rows."""
+    from radixattention_prefix_shared_tree_gb300.driver import plan_cascade
+    if which == "few_shot":
+        tr = traces.few_shot(n_questions=30, max_new=4)
+        cache = ra.RadixCache(1 << 15)
+        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"))
+        runner.serve([runner.request(tr.warm, 0)])
+        reqs = [runner.request(tr.prompt(i), tr.max_new) for i in range(30)]
+    else:
+        tr = traces.agent_tree(root_len=96, branch_len=16, max_new=4)
+        cache = ra.RadixCache(8192)
+        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"))
+        runner.serve([runner.request(tr.root, 0)])
+        for lvl in (1, 2):
+            runner.serve([runner.request(tr.prompt(p), 0) for p in sorted({lf[:lvl] for lf in tr.leaves})])
+        reqs = [runner.request(tr.prompt(lf), tr.max_new) for lf in tr.leaves]
+    admitted, _ = runner.sched.admit(reqs)
+    runner.sched.commit_prompts(admitted)
+    plan = cache.cascade_plan([r.node for r in admitted])
+    segs, private = plan_cascade([r.slots[:r.prompt_len] for r in admitted])
+    got = set()
+    ip, rp = plan["seg_indptr"], plan["seg_row_indptr"]
+    for k in range(plan["n_seg"]):
+        got.add((tuple(int(x) for x in plan["seg_slots"][ip[k]:ip[k + 1]]),
+                 tuple(int(x) for x in plan["seg_rows"][rp[k]:rp[k + 1]])))
+    want = {(tuple(int(x) for x in s), tuple(int(x) for x in r)) for s, r in segs}
+    assert got == want and len(got) == (1 if which == "few_shot" else 1 + 4 + 16)
+    assert (plan["private"] == private).all()
+    for b in range(len(admitted)):   # the inverse map lists row b's entries
+        pos = plan["req_seg_pos"][plan["req_seg_indptr"][b]:plan["req_seg_indptr"][b + 1]]
+        assert all(plan["seg_rows"][p] == b for p in pos)
