@@ -529,6 +529,12 @@ cudaError_t dispatch_group(int G, const DecParams& dp, const rc::MQParams& mp, c
 extern "C" rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t batch, int32_t max_len,
                                            const rc_cascade* cascade, size_t* bytes) {
     if (!bytes) return RC_ERR_ARG;
+    if (desc && desc->pool.mla) {
+        if (batch < 0 || max_len < 0 || desc->q_heads <= 0) return RC_ERR_ARG;
+        if (cascade && cascade->n_seg > 0) return RC_ERR_UNSUPPORTED;
+        *bytes = rc_host::mla_workspace(batch, desc->q_heads, max_len);
+        return RC_OK;
+    }
     DecodePlan pl;
     rc_status s = plan_decode(desc, batch, max_len, cascade, &pl);
     if (s != RC_OK) return s;
@@ -543,6 +549,11 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     if (batch == 0) return RC_OK;
     if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
     const bool use_casc = casc && casc->n_seg > 0;
+    if (desc->pool.mla) {  // one latent KV head: its own kernel (attn_decode_mla.cu)
+        if (use_casc) return RC_ERR_UNSUPPORTED;
+        if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return RC_ERR_ARG;
+        return rc_host::mla_decode(desc, q, kv, batch, out, lse, ws, ws_bytes, (cudaStream_t)stream);
+    }
     DecodePlan pl;
     rc_status s = plan_decode(desc, batch, kv->max_len, use_casc ? casc : nullptr, &pl);
     if (s != RC_OK) return s;

@@ -95,6 +95,10 @@ RC_DEV uint32_t swz(int r, int c) {
 // Host-side launch helpers.
 namespace rc_host {
 int sm_count();
+// latent (MLA) decode, attn_decode_mla.cu
+size_t mla_workspace(int32_t batch, int32_t q_heads, int32_t max_len);
+rc_status mla_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv, int32_t batch, void* out,
+                     float* lse, void* ws, size_t ws_bytes, cudaStream_t st);
 inline rc_status launch_status(cudaError_t e) { return e == cudaSuccess ? RC_OK : RC_ERR_CUDA; }
 
 // Raise a kernel's dynamic shared-memory limit once per device (one flag

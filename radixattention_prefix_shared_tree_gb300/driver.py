@@ -363,8 +363,15 @@ class DeviceEngine:
         lay.casc_ref = C.byref(casc) if casc is not None else None
         lay.slot_ptrs = [lay.decode_slots[t].data_ptr() for t in range(T)]
         # kernels per step: cascade (if any) + table pass + merge when a row is split
+        # (the same thresholds as the library's plan)
         sms = self.torch.cuda.get_device_properties(self.device).multi_processor_count
-        split = B * self.shape.kv_heads < 8 * sms
+        if self.shape.mla:
+            base = B * (self.shape.q_heads // 16)
+            max_len = max(kv.max_len for kv in lay.kv_tables) if lay.kv_tables else 0
+            splits = min(max(-(-4 * sms // max(base, 1)), 1), max(-(-max_len // 1024), 1))
+            split = splits > 1
+        else:
+            split = B * self.shape.kv_heads < 8 * sms
         lay.decode_kernels = (1 if casc is not None else 0) + 1 + (1 if split else 0)
         lay.stream = C.c_void_p(self.torch.cuda.current_stream(self.device).cuda_stream)
 

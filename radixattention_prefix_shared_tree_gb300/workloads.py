@@ -62,10 +62,12 @@ class Runner:
         total = int(lay.qo_host[-1])
         if total == 0:
             return
+        if not self.prefill_attention:   # store K/V only (no queries needed)
+            inp = self.model.extend_kv(batch)
+            eng.store(lay.extend_slots, inp["k"], inp["v"])
+            return
         inp = self.model.extend_inputs(batch)
         eng.store(lay.extend_slots, inp["k"], inp["v"])
-        if not self.prefill_attention:
-            return
         sh = eng.shape
         out = torch.empty(total, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
         lse = torch.empty(total, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
@@ -173,6 +175,18 @@ def run_agent(runner: Runner, trace):
         admitted, waiting = runner.serve(reqs)
         assert not waiting
     reqs = [runner.request(trace.prompt(leaf), trace.max_new) for leaf in trace.leaves]
+    admitted, waiting = runner.serve(reqs)
+    assert not waiting
+    return admitted
+
+
+def run_mla(runner: Runner, trace, n_requests: int | None = None):
+    """Latent-attention long-context decode: the shared prefix and every
+    request's private context are stored (kv_store, no prefill attention),
+    then all requests decode trace.steps tokens together."""
+    runner.serve([runner.request(trace.shared, 0)])
+    n = len(trace.private) if n_requests is None else n_requests
+    reqs = [runner.request(trace.prompt(i), trace.steps) for i in range(n)]
     admitted, waiting = runner.serve(reqs)
     assert not waiting
     return admitted

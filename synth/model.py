@@ -73,6 +73,12 @@ class SynthModel:
         h = np.concatenate(hs) if hs else np.zeros(0, np.uint64)
         return self.rows(h)
 
+    def extend_kv(self, batch):
+        """K/V rows only (a prefill that stores K/V without attention)."""
+        hs = [self._hashes[r.rid][r.first:r.prompt_len] for r in batch]
+        h = np.concatenate(hs) if hs else np.zeros(0, np.uint64)
+        return self.rows(h, kinds=("k", "v"))
+
     def decode_inputs(self, batch, t: int):
         h = np.asarray([self._hashes[r.rid][r.prompt_len + t] for r in batch], np.uint64)
         return self.rows(h)
