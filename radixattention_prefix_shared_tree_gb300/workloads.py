@@ -36,6 +36,7 @@ class Runner:
         self.extend_out = {}   # rid -> (positions, out bf16 [n, Hq, dv], lse [n, Hq])
         self.decode_out = {}   # rid -> list of (position, out [Hq, dv], lse [Hq])
         self.next_rid = 0
+        self.collect_rids = None  # collect only these requests' outputs (None: all)
         self.on_decode = None   # optional callback(out) after each decode step
         self.on_extend = None   # optional callback(out) after the prefill
 
@@ -75,10 +76,12 @@ class Runner:
         if self.on_extend is not None:
             self.on_extend(out)
         if self.collect:
-            o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
             for i, r in enumerate(batch):
+                if self.collect_rids is not None and r.rid not in self.collect_rids:
+                    continue
                 a, b = int(lay.qo_host[i]), int(lay.qo_host[i + 1])
-                self.extend_out[r.rid] = (np.arange(r.first, r.prompt_len), o[a:b], l[a:b])
+                o = out[a:b].view(torch.int16).cpu().numpy().view(np.uint16)
+                self.extend_out[r.rid] = (np.arange(r.first, r.prompt_len), o, lse[a:b].cpu().numpy())
 
     def _decode(self, batch):
         eng, torch = self.engine, self.engine.torch
@@ -96,9 +99,16 @@ class Runner:
             if self.on_decode is not None:
                 self.on_decode(out)
             if self.collect:
-                o, l = out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
-                for i, r in enumerate(batch):
-                    self.decode_out.setdefault(r.rid, []).append((r.prompt_len + t, o[i].copy(), l[i].copy()))
+                if self.collect_rids is None:
+                    idx = list(range(B))
+                else:
+                    idx = [i for i, r in enumerate(batch) if r.rid in self.collect_rids]
+                if idx:
+                    sel = torch.as_tensor(idx, device=out.device)
+                    o = out.index_select(0, sel).view(torch.int16).cpu().numpy().view(np.uint16)
+                    l = lse.index_select(0, sel).cpu().numpy()
+                    for j, i in enumerate(idx):
+                        self.decode_out.setdefault(batch[i].rid, []).append((batch[i].prompt_len + t, o[j], l[j]))
 
 
 # ------------------------------------------------------------------ workloads
