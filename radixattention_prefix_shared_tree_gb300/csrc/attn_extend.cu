@@ -5,24 +5,25 @@
 // of request b sits at position len[b] - n_b + i of its slot-table row and
 // attends causally to positions 0..itself, prefix included.
 //
-// The kernel body is mq_attn.cuh: a CTA owns 64 query rows = (64/G new tokens)
-// x (the G query heads of one KV head), so each gathered K/V row serves every
-// head of its group; tensor-core products, online softmax, bf16 output written
-// directly (no split, no workspace).
+// The kernel body is attn_tc.cuh: a CTA owns 128 query rows = (128/G new
+// tokens) x (the G query heads of one KV head), so each gathered K/V row
+// serves every head of its group; both products run on tcgen05 with the
+// accumulators in TMEM; online softmax; bf16 output written directly (no
+// split, no workspace).
 
+#include "attn_tc.cuh"
 #include "common.cuh"
-#include "mq_attn.cuh"
 
 namespace {
 
 template <int D, int G>
 cudaError_t launch_extend(const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st) {
-    constexpr int smem = rc::mq_smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<rc::mq_attn_kernel<D, G, rc::MQMode::kExtend>>(smem);
+    constexpr int smem = rc_tc::smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<rc_tc::attn_tc_kernel<D, G, rc::MQMode::kExtend>>(smem);
     if (e != cudaSuccess) return e;
-    constexpr int TPC = rc::kMQRows / G;
+    constexpr int TPC = rc_tc::TM / G;
     dim3 grid((max_q + TPC - 1) / TPC, kv_heads, batch);
-    rc::mq_attn_kernel<D, G, rc::MQMode::kExtend><<<grid, 128, smem, st>>>(p);
+    rc_tc::attn_tc_kernel<D, G, rc::MQMode::kExtend><<<grid, 128, smem, st>>>(p);
     return cudaGetLastError();
 }
 
