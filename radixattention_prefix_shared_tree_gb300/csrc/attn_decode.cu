@@ -19,7 +19,7 @@
 //     (request, head) and segment.
 //  3. merge pass: per (request, head), combine all partials by log-sum-exp.
 
-#include "attn_tc.cuh"
+#include "attn_tc2.cuh"
 #include "common.cuh"
 
 namespace {
@@ -457,14 +457,14 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     pl->seg_chunks = 1;
     if (casc && casc->n_seg > 0 && casc->max_seg_len > 0) {
         const int G = d->q_heads / hkv;
-        const int64_t row_blocks = (casc->max_seg_rows * (int64_t)G + rc_tc::TM - 1) / rc_tc::TM;
+        const int64_t row_blocks = (casc->max_seg_rows * (int64_t)G + rc_tc2::ROWS - 1) / rc_tc2::ROWS;
         const int64_t cbase = (int64_t)casc->n_seg * row_blocks * hkv;
-        int64_t sc = cbase > 0 ? (3 * sms + cbase - 1) / cbase : 1;
+        int64_t sc = cbase > 0 ? (sms + cbase - 1) / cbase : 1;   // about one CTA per SM
         const int64_t sc_max = (casc->max_seg_len + 255) / 256;
         if (sc > sc_max) sc = sc_max;
         if (sc < 1) sc = 1;
         int64_t len = (casc->max_seg_len + sc - 1) / sc;
-        len = (len + rc_tc::TN - 1) / rc_tc::TN * rc_tc::TN;
+        len = (len + rc_tc2::TN - 1) / rc_tc2::TN * rc_tc2::TN;
         pl->seg_chunk = (int)len;
         pl->seg_chunks = (int)((casc->max_seg_len + len - 1) / len);
     }
@@ -492,12 +492,12 @@ cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream
 
 template <int D, int G>
 cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_heads, cudaStream_t st) {
-    constexpr int smem = rc_tc::smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<rc_tc::attn_tc_kernel<D, G, rc::MQMode::kCascade>>(smem);
+    constexpr int smem = rc_tc2::smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade>>(smem);
     if (e != cudaSuccess) return e;
-    constexpr int TPC = rc_tc::TM / G;
+    constexpr int TPC = rc_tc2::ROWS / G;
     dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
-    rc_tc::attn_tc_kernel<D, G, rc::MQMode::kCascade><<<grid, 128, smem, st>>>(p);
+    rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade><<<grid, rc_tc2::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -5,25 +5,26 @@
 // of request b sits at position len[b] - n_b + i of its slot-table row and
 // attends causally to positions 0..itself, prefix included.
 //
-// The kernel body is attn_tc.cuh: a CTA owns 128 query rows = (128/G new
-// tokens) x (the G query heads of one KV head), so each gathered K/V row
-// serves every head of its group; both products run on tcgen05 with the
-// accumulators in TMEM; online softmax; bf16 output written directly (no
-// split, no workspace).
+// The kernel body is attn_tc2.cuh: a CTA owns 256 query rows = (256/G new
+// tokens) x (the G query heads of one KV head) in two M=128 tiles, so each
+// gathered K/V row serves every head of its group and both tiles; both
+// products run on tcgen05 with the accumulators in TMEM, with producer,
+// MMA and softmax warps; bf16 output written directly (no split, no
+// workspace).
 
-#include "attn_tc.cuh"
+#include "attn_tc2.cuh"
 #include "common.cuh"
 
 namespace {
 
 template <int D, int G>
 cudaError_t launch_extend(const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st) {
-    constexpr int smem = rc_tc::smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<rc_tc::attn_tc_kernel<D, G, rc::MQMode::kExtend>>(smem);
+    constexpr int smem = rc_tc2::smem_bytes<D>();
+    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend>>(smem);
     if (e != cudaSuccess) return e;
-    constexpr int TPC = rc_tc::TM / G;
+    constexpr int TPC = rc_tc2::ROWS / G;
     dim3 grid((max_q + TPC - 1) / TPC, kv_heads, batch);
-    rc_tc::attn_tc_kernel<D, G, rc::MQMode::kExtend><<<grid, 128, smem, st>>>(p);
+    rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend><<<grid, rc_tc2::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
