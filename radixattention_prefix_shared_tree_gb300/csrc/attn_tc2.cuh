@@ -7,18 +7,23 @@
 // tokens or requests) x (the G query heads of that KV head) -- so every K/V
 // tile it gathers feeds both.  Eleven warps with fixed roles:
 //   warps 0-3 and 4-7  softmax of query tile 0 and 1: one thread per row /
-//                      TMEM lane; read S, write P (bf16) to shared memory,
-//                      rescale the row's O in TMEM when its max grows > 2^8;
+//                      TMEM lane; read S from TMEM, write P (bf16) back over
+//                      it, rescale the row's O in TMEM when its max grows by
+//                      more than 2^8;
 //   warps 8, 9         producers of the even and odd tiles: gather K/V rows
-//                      by slot id with cp.async into a 4-stage ring
+//                      by slot id with cp.async into a 5-stage ring
 //                      (no-swizzle operand layout);
 //   warp 10            issues every MMA (one thread) and owns TMEM.
 // Per 64-key tile and query tile q:  S_q = Q_q K^T (M=128, N=64, K=D) into
-// one of two S buffers, O_q += P_q V (M=128, N=D, K=64).  The next tile's S
-// products are issued before this tile's P.V, so the tensor core works while
-// the softmax warps run.  TMEM: query tile q uses columns [256q, 256q+256):
-// S buffers at +0 and +64, O at +128.  All hand-offs are mbarriers; every
-// wait is bounded and a wait that gives up flags RC_ERR_TIMEOUT.
+// one of two S buffers, O_q += P_q V (M=128, N=D, K=64) with P read from
+// tensor memory.  The next tile's S products are issued before this tile's
+// P.V, so the tensor core works while the softmax warps run, and the softmax
+// of tile t+1 does not wait for P.V of tile t (only a rescale of O does).
+// TMEM: query tile q uses columns [256q, 256q+256): S buffers at +0 and +64
+// (P over their first 32 columns), O at +128.  The tensor core runs one
+// thread's MMAs in issue order, so S(t+2) overwrites P(t) only after P(t).V
+// has read it.  All hand-offs are mbarriers; every wait is bounded and a wait
+// that gives up flags RC_ERR_TIMEOUT.
 #pragma once
 
 #include "mq_attn.cuh"
@@ -30,18 +35,50 @@ constexpr int QT = 2;          // query tiles per CTA
 constexpr int TM = 128;        // rows per query tile
 constexpr int ROWS = QT * TM;  // query rows per CTA
 constexpr int TN = 64;         // keys per tile
-constexpr int NS = 4;          // K/V stages
+constexpr int NS = 5;          // K/V stages
 constexpr int THREADS = 352;
 constexpr uint32_t kWaitIter = 1u << 24;
+constexpr int kBars = 1 + 2 * NS + 4 + 4 + 2;
 
 template <int D>
 __host__ __device__ constexpr int smem_bytes() {
-    return QT * TM * D * 2 + NS * 2 * TN * D * 2 + QT * TM * TN * 2 + 18 * 8 + 16;
+    return QT * TM * D * 2 + NS * 2 * TN * D * 2 + kBars * 8 + 16;
 }
 
 RC_DEV void mbar_arrive(uint64_t* mbar) {
     asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}\n" ::"r"(rc::smem_u32(mbar))
                  : "memory");
+}
+
+RC_DEV float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+RC_DEV float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// (a.x*b + c, a.y*b + c) in one packed instruction
+RC_DEV float2 ffma2(float2 a, float b, float c) {
+    uint64_t r, x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
+}
+RC_DEV float2 fadd2(float2 a, float2 b) {
+    uint64_t r, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    float2 o;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
+    return o;
 }
 
 template <int D, int G, rc::MQMode MODE>
@@ -55,15 +92,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* sQ = smem;                                  // [QT][128 rows][D]
     unsigned char* sKV = sQ + QT * TM * D * 2;                 // [NS][K, V]
-    unsigned char* sP = sKV + NS * 2 * KV_BYTES;               // [QT][128 rows][64 keys]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sP + QT * TM * TN * 2);
-    uint64_t* q_full = bar + 0;          // count 256 (softmax threads)
-    uint64_t* kv_full = bar + 1;         // [NS], count 32 (the lanes of the tile's producer warp)
-    uint64_t* kv_empty = bar + 5;        // [NS], count 1 (MMA commit)
-    uint64_t* s_full = bar + 9;          // [QT][2], count 1
-    uint64_t* p_full = bar + 13;         // [QT], count 128
-    uint64_t* o_done = bar + 15;         // [QT], count 1
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 18);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + NS * 2 * KV_BYTES);
+    uint64_t* q_full = bar + 0;              // count 8 (softmax warps)
+    uint64_t* kv_full = bar + 1;             // [NS], count 32 (the lanes of the tile's producer warp)
+    uint64_t* kv_empty = bar + 1 + NS;       // [NS], count 1 (MMA commit)
+    uint64_t* s_full = bar + 1 + 2 * NS;     // [QT][2], count 1
+    uint64_t* p_full = s_full + 4;           // [QT][2] (one per S buffer), count 4 (the tile's softmax warps)
+    uint64_t* o_done = p_full + 4;           // [QT], count 1
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kBars);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = blockIdx.y, z = blockIdx.z, blk = blockIdx.x;
@@ -104,19 +140,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             return;
         }
     }
+    // a wait gave up in an earlier CTA: the results are void, leave at once
+    if (p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout)) return;
     const int n_tiles = (key_count + TN - 1) / TN;
     // query tiles with at least one valid row
     const int n_qt = min(QT, ((min(n_rows_tok - tok0, TPC) * G) + TM - 1) / TM);
 
     if (tid == 0) {
-        tc::mbar_init(q_full, QT * TM);
+        tc::mbar_init(q_full, 8);
         for (int s = 0; s < NS; ++s) {
             tc::mbar_init(&kv_full[s], 32);
             tc::mbar_init(&kv_empty[s], 1);
         }
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&s_full[i], 1);
+        for (int i = 0; i < 4; ++i) {
+            tc::mbar_init(&s_full[i], 1);
+            tc::mbar_init(&p_full[i], 4);
+        }
         for (int q = 0; q < QT; ++q) {
-            tc::mbar_init(&p_full[q], TM);
             tc::mbar_init(&o_done[q], 1);
         }
         tc::fence_mbar_init();
@@ -139,7 +179,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tq = tbase + q * 256 + lane_off;
         unsigned char* sQq = sQ + q * TM * D * 2;
-        unsigned char* sPq = sP + q * TM * TN * 2;
         // Q rows of this tile (zero past the end)
         for (int gi = r; gi < TM * CH; gi += 128) {
             const int rr = (gi & 7) + 8 * (gi / (8 * CH));
@@ -158,69 +197,93 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         rc::cp_async_commit();
         rc::cp_async_wait<0>();
         tc::fence_proxy_async();
-        mbar_arrive(q_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
 
         const int r_tok = tok0 + row / G;
         const bool row_valid = r_tok < n_rows_tok;
         int lim;
         if constexpr (MODE == rc::MQMode::kExtend) lim = row_valid ? prefix + r_tok + 1 : 0;
         else lim = row_valid ? key_count : 0;
+        const float sc = p.scale_log2;
         float m_used = -INFINITY, l_run = 0.f;
         if (q < n_qt) {
             for (int t = 0; t < n_tiles && ok; ++t) {
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&s_full[q * 2 + (t & 1)], (t >> 1) & 1, kWaitIter));
                 tc::fence_after();
-                float s[TN];
                 const uint32_t tS = tq + (t & 1) * TN;
-                tc::tmem_ld32(tS, *reinterpret_cast<float(*)[32]>(&s[0]));
-                tc::tmem_ld32(tS + 32, *reinterpret_cast<float(*)[32]>(&s[32]));
-                const int kb = t * TN;
-                float mt = -INFINITY;
+                uint32_t sa[32], sb[32];
+                tc::tmem_ld32_issue(tS, sa);
+                tc::tmem_ld32_issue(tS + 32, sb);
+                tc::tmem_ld_wait(sa);
+                tc::tmem_ld_wait(sb);
+                float s[TN];
 #pragma unroll
-                for (int j = 0; j < TN; ++j) {
-                    s[j] = kb + j < lim ? s[j] * p.scale_log2 : -INFINITY;
-                    mt = fmaxf(mt, s[j]);
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = __uint_as_float(sa[j]);
+                    s[32 + j] = __uint_as_float(sb[j]);
                 }
-                // P.V of the previous tile must be done: O stable, P buffer free
-                if (t > 0) {
+                const int kb = t * TN;
+                if (kb + TN > lim) {  // the causal edge or the end of the keys
+#pragma unroll
+                    for (int j = 0; j < TN; ++j)
+                        if (kb + j >= lim) s[j] = -INFINITY;
+                }
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    m8[i] = max3(s[i], s[8 + i], s[16 + i]);
+                    m8[i] = max3(m8[i], s[24 + i], s[32 + i]);
+                    m8[i] = max3(m8[i], s[40 + i], s[48 + i]);
+                    m8[i] = fmaxf(m8[i], s[56 + i]);
+                }
+                const float mraw = max3(max3(m8[0], m8[1], m8[2]), max3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                const float mt = mraw * sc;  // sc > 0: the max of the scaled row
+                const bool grow = mt > m_used + 8.f;
+                const bool rescale_o = grow && m_used != -INFINITY;
+                if (__any_sync(0xffffffffu, rescale_o)) {
+                    // O must be stable: the previous tile's P.V has completed
                     ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (t - 1) & 1, kWaitIter)) && ok;
                     tc::fence_after();
-                }
-                if (mt > m_used + 8.f) {
-                    if (t > 0 && m_used != -INFINITY) {
-                        const float a = rc::fast_exp2(m_used - mt);
+                    const float a = rescale_o ? ex2(m_used - mt) : 1.f;
 #pragma unroll
-                        for (int c = 0; c < D / 32; ++c) {
-                            float v[32];
-                            tc::tmem_ld32(tq + 128 + c * 32, v);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tc::tmem_ld32_issue(tq + 128 + c * 32, v);
+                        tc::tmem_ld_wait(v);
 #pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] *= a;
-                            tc::tmem_st32(tq + 128 + c * 32, v);
-                        }
-                        l_run *= a;
+                        for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * a);
+                        tc::tmem_st32_issue(tq + 128 + c * 32, v);
                     }
+                    tc::tmem_st_wait();
+                }
+                if (grow) {
+                    l_run *= ex2(m_used - mt);  // 0 while nothing was seen
                     m_used = mt;
                 }
-                const float mu = m_used == -INFINITY ? 0.f : m_used;
+                const float nmu = m_used == -INFINITY ? 0.f : -m_used;
+                uint32_t pk[32];
+                float2 ls[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
-                for (int c = 0; c < TN / 8; ++c) {
-                    float e[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        e[j] = rc::fast_exp2(s[c * 8 + j] - mu);
-                        l_run += e[j];
-                    }
-                    uint4 w;
-                    w.x = rc::pack_bf16(e[0], e[1]);
-                    w.y = rc::pack_bf16(e[2], e[3]);
-                    w.z = rc::pack_bf16(e[4], e[5]);
-                    w.w = rc::pack_bf16(e[6], e[7]);
-                    *reinterpret_cast<uint4*>(sPq + tc::cm_offset(r, c, TN / 8)) = w;
+                for (int i = 0; i < 32; ++i) {
+                    const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc, nmu);
+                    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                    ls[i & 3] = fadd2(ls[i & 3], e);
+                    pk[i] = rc::pack_bf16(e.x, e.y);
                 }
-                tc::fence_proxy_async();
+                // P (bf16) over the first half of this S buffer: the A operand of P.V
+                tc::tmem_st32_issue(tS, pk);
+                const float2 l01 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
+                l_run += l01.x + l01.y;
+                tc::tmem_st_wait();
                 tc::fence_before();
-                mbar_arrive(&p_full[q]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[q * 2 + (t & 1)]);
             }
+            // the last two P.V products: S(n-1) only guarantees P(n-3).V, and a
+            // parity wait must not skip a phase
+            if (ok && n_tiles > 1)
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (n_tiles - 2) & 1, kWaitIter));
             if (ok && n_tiles > 0)
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (n_tiles - 1) & 1, kWaitIter));
             tc::fence_after();
@@ -233,8 +296,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         const int h = kvh * G + (row % G);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
+            uint32_t vb[32];
+            tc::tmem_ld32_issue(tq + 128 + c * 32, vb);
+            tc::tmem_ld_wait(vb);
             float v[32];
-            tc::tmem_ld32(tq + 128 + c * 32, v);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(vb[j]);
             if (!write) continue;
             if constexpr (MODE == rc::MQMode::kExtend) {
                 __nv_bfloat16* dst = p.out + ((int64_t)(qo0 + r_tok) * p.q_heads + h) * D + c * 32;
@@ -351,14 +418,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             }
             const uint32_t v0 = rc::smem_u32(sKV + s * 2 * KV_BYTES + KV_BYTES);
             for (int q = 0; q < n_qt && ok; ++q) {
-                ok = tc::mbar_wait(&p_full[q], t & 1, kWaitIter);
+                ok = tc::mbar_wait(&p_full[q * 2 + (t & 1)], (t >> 1) & 1, kWaitIter);
                 tc::fence_after();
                 if (!ok) break;
-                const uint32_t p0 = rc::smem_u32(sP + q * TM * TN * 2);
+                const uint32_t pt = tbase + q * 256 + (t & 1) * TN;  // P(t) in TMEM, 8 columns per 16 keys
 #pragma unroll
                 for (int j = 0; j < TN / 16; ++j)
-                    tc::mma_bf16(tbase + q * 256 + 128, tc::smem_desc(p0 + j * 256, 128, (TN / 8) * 128),
-                                 tc::smem_desc(v0 + j * 2 * SB, SB, 128), idPV, t > 0 || j > 0);
+                    tc::mma_bf16_ts(tbase + q * 256 + 128, pt + j * 8, tc::smem_desc(v0 + j * 2 * SB, SB, 128), idPV,
+                                    t > 0 || j > 0);
                 tc::commit(&o_done[q]);
             }
             tc::commit(&kv_empty[s]);  // stage s is free once everything issued so far is done
