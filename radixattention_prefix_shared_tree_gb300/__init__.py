@@ -217,10 +217,16 @@ def rc_dump(handle) -> str:
     return buf.value.decode()
 
 
+def _req_ptr(reqs):
+    """Address of an rc_request array: a ctypes array, or a numpy structured
+    array with the same record layout."""
+    return reqs.ctypes.data if isinstance(reqs, np.ndarray) else C.cast(reqs, VP)
+
+
 def rc_admit(handle, policy: int, reqs, n: int, max_batch: int, out_order):
-    """reqs: ctypes array of rc_request; out_order: int32 numpy array of n."""
+    """reqs: array of rc_request (see _req_ptr); out_order: int32 numpy array of n."""
     cnt = I32(0)
-    st = lib().rc_admit(handle, int(policy), C.cast(reqs, VP), int(n), int(max_batch), _np_ptr(out_order),
+    st = lib().rc_admit(handle, int(policy), _req_ptr(reqs), int(n), int(max_batch), _np_ptr(out_order),
                         C.byref(cnt))
     return st, cnt.value
 
@@ -257,7 +263,7 @@ def rc_cascade_plan(handle, nodes):
 
 def rc_commit(handle, reqs, idx, mode: int):
     idx = _i32(idx)
-    return lib().rc_commit(handle, C.cast(reqs, VP), _np_ptr(idx), len(idx), int(mode))
+    return lib().rc_commit(handle, _req_ptr(reqs), _np_ptr(idx), len(idx), int(mode))
 
 
 _STAT_RENAME = {"pool_slots": "pool", "free_slots": "free", "caller_slots": "caller"}

@@ -58,7 +58,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs.append(obj)
     for src in CPP_SOURCES:
         obj = os.path.join(BUILD, src.replace(".cpp", ".o"))
-        cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = ["g++", "-O3", "-std=c++17", "-fPIC", "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         jobs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
         objs.append(obj)
     failed = []

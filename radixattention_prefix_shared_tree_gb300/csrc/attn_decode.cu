@@ -451,15 +451,15 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     pl->chunk = (int)chunk;
     pl->n_chunks = max_len > 0 ? (int)((max_len + chunk - 1) / chunk) : 1;
     pl->fused = pl->n_chunks == 1;
-    // Cascade part: split each segment's keys so the grid covers the SMs a
-    // few times (the rows of one segment share every key tile).
+    // Cascade part: split each segment's keys so that the grid fills the SMs
+    // once (one CTA per SM: a second, partial wave would double the time).
     pl->seg_chunk = 0;
     pl->seg_chunks = 1;
     if (casc && casc->n_seg > 0 && casc->max_seg_len > 0) {
         const int G = d->q_heads / hkv;
         const int64_t row_blocks = (casc->max_seg_rows * (int64_t)G + rc_tc2::ROWS - 1) / rc_tc2::ROWS;
         const int64_t cbase = (int64_t)casc->n_seg * row_blocks * hkv;
-        int64_t sc = cbase > 0 ? (sms + cbase - 1) / cbase : 1;   // about one CTA per SM
+        int64_t sc = cbase > 0 ? sms / cbase : 1;
         const int64_t sc_max = (casc->max_seg_len + 255) / 256;
         if (sc > sc_max) sc = sc_max;
         if (sc < 1) sc = 1;

@@ -44,6 +44,18 @@ struct Rec {
     uint64_t lru_stamp = 0;  // stamp under which it sits in the LRU set
 };
 
+// Length of the common prefix of a[0..n) and b[0..n).  The whole range is
+// tried first with one memcmp (vectorised in the C library; a full match is
+// the common case), then 256-element blocks, then one element at a time.
+inline int64_t common_prefix(const int32_t* a, const int32_t* b, int64_t n) {
+    if (n <= 0) return 0;
+    if (std::memcmp(a, b, (size_t)n * sizeof(int32_t)) == 0) return n;
+    int64_t k = 0;
+    while (k + 256 <= n && std::memcmp(a + k, b + k, 256 * sizeof(int32_t)) == 0) k += 256;
+    while (a[k] == b[k]) ++k;  // a difference exists below n
+    return k;
+}
+
 inline uint64_t edge_key(int32_t parent, int32_t first_tok) {
     return ((uint64_t)(uint32_t)parent << 32) | (uint32_t)first_tok;
 }
@@ -174,8 +186,7 @@ struct rc_cache {
             const Rec& r = recs[(size_t)c];
             const int32_t* rt = toks(r);
             int64_t lim = std::min<int64_t>(r.len, n - i);
-            int64_t k = 1;
-            while (k < lim && rt[k] == tok[i + k]) ++k;
+            int64_t k = 1 + common_prefix(rt + 1, tok + i + 1, lim - 1);
             if (sl) sl->insert(sl->end(), slot_arena.begin() + r.off, slot_arena.begin() + r.off + k);
             i += k;
             if (k < r.len) {
@@ -283,16 +294,25 @@ rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, i
     return RC_OK;
 }
 
+// Every slot id in [0, pool); a branch-free scan.
+static bool slots_in_pool(const rc_cache* c, const int32_t* slots, int64_t n) {
+    const uint32_t pool = (uint32_t)c->pool;  // at most 2^31 - 1: a negative id reads as >= pool
+    uint32_t bad = 0;
+    for (int64_t i = 0; i < n; ++i) bad |= (uint32_t)slots[i] >= pool;
+    return bad == 0;
+}
+
 rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64_t n, int pin,
                     int64_t* already_present, rc_node* out_node, int32_t* out_slots) {
     if (!c || n < 0 || (n > 0 && (!tok || !slots)) || !already_present || !out_node) return RC_ERR_ARG;
-    for (int64_t i = 0; i < n; ++i)
-        if (slots[i] < 0 || slots[i] >= c->pool) return RC_ERR_ARG;
+    if (!slots_in_pool(c, slots, n)) return RC_ERR_ARG;
     std::vector<int32_t>& have = c->scratch_slots;
     have.clear();
     int64_t m = c->descend(tok, n, false, nullptr, &have);
     if (++c->epoch == 0) { std::fill(c->mark.begin(), c->mark.end(), 0); c->epoch = 1; }
-    for (int64_t i = 0; i < n; ++i) {
+    // positions whose slot is already the cached one need no check
+    const int64_t same = common_prefix(slots, have.data(), m);
+    for (int64_t i = same; i < n; ++i) {
         int32_t s = slots[i];
         if (i < m && s == have[(size_t)i]) continue;
         if (c->owner[(size_t)s] != HELD || c->mark[(size_t)s] == c->epoch) return RC_ERR_STATE;
@@ -316,7 +336,7 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
         c->path.push_back(leaf);
     }
     int64_t dup = 0;
-    for (int64_t i = 0; i < m; ++i) {
+    for (int64_t i = same; i < m; ++i) {
         int32_t s = slots[i];
         if (s == have[(size_t)i]) continue;
         c->owner[(size_t)s] = FREE;

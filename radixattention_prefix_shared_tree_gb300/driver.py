@@ -58,14 +58,22 @@ class SchedulerError(RuntimeError):
     pass
 
 
+class AdmitRound:
+    """One native admission round: the rc_request records (numpy, the
+    library's layout) and the flat array that holds every request's slot row
+    (row i at flat[off[i]:off[i+1]], written by rc_admit and rc_commit)."""
+
+    __slots__ = ("req", "flat", "off")
+
+    def __init__(self, req, flat, off):
+        self.req, self.flat, self.off = req, flat, off
+
+
+# record layout of rc_request (checked against the ctypes structure below)
 _REQ_DTYPE = np.dtype([("tokens", "u8"), ("prompt_len", "i8"), ("max_new", "i8"), ("slots", "u8"),
                        ("matched", "i8"), ("first", "i8"), ("node", "i8"), ("admitted", "i4"), ("_pad", "i4")])
-
-
-def _req_view(arr):
-    """Numpy view of a ctypes rc_request array (fields read without Python loops)."""
-    assert C.sizeof(rc_request) == _REQ_DTYPE.itemsize
-    return np.frombuffer(arr, dtype=_REQ_DTYPE)
+assert _REQ_DTYPE.itemsize == C.sizeof(rc_request)
+assert all(_REQ_DTYPE.fields[n][1] == getattr(rc_request, n).offset for n, _ in rc_request._fields_)
 
 
 def _ok(st, what):
@@ -129,42 +137,54 @@ class Scheduler:
 
     # ---- native batch path: the same rules, one C call per round
     def _admit_native(self, pending, policy, max_batch):
+        """One rc_admit over a record array filled column by column; the slot
+        rows of the round's requests are views into one flat array."""
         n = len(pending)
-        arr = (rc_request * n)()
-        for i, r in enumerate(pending):
+        for r in pending:
             if r.tokens.dtype != np.int32 or not r.tokens.flags.c_contiguous:
                 r.tokens = np.ascontiguousarray(r.tokens, np.int32)
-            r.slots = np.empty(r.prompt_len + r.max_new, np.int32)
-            c = arr[i]
-            c.tokens = r.tokens.ctypes.data
-            c.prompt_len, c.max_new = r.prompt_len, r.max_new
-            c.slots = r.slots.ctypes.data
+        req = np.zeros(n, _REQ_DTYPE)
+        req["tokens"] = np.fromiter((r.tokens.ctypes.data for r in pending), np.uint64, n)
+        plen = np.fromiter((r.prompt_len for r in pending), np.int64, n)
+        mnew = np.fromiter((r.max_new for r in pending), np.int64, n)
+        req["prompt_len"], req["max_new"] = plen, mnew
+        off = np.zeros(n + 1, np.int64)
+        np.cumsum(plen + mnew, out=off[1:])
+        flat = np.empty(int(off[-1]), np.int32)
+        req["slots"] = np.uint64(flat.ctypes.data) + 4 * off[:-1].astype(np.uint64)
         order = np.empty(n, np.int32)
-        st, cnt = self.cache.admit_batch(policy, arr, n, max_batch or 0, order)
+        st, cnt = self.cache.admit_batch(policy, req, n, max_batch or 0, order)
         _ok(st, "rc_admit")
-        view = _req_view(arr)
+        matched, first, node = req["matched"].tolist(), req["first"].tolist(), req["node"].tolist()
+        offs = off.tolist()
+        rnd = AdmitRound(req, flat, off)
         admitted = []
-        for k in range(cnt):
-            i = int(order[k])
+        for i in order[:cnt].tolist():
             r = pending[i]
-            r.matched, r.first, r.node = int(view["matched"][i]), int(view["first"][i]), int(view["node"][i])
-            r._batch = (arr, i)
+            r.matched, r.first, r.node = matched[i], first[i], node[i]
+            r.slots = flat[offs[i]:offs[i + 1]]
+            r._batch = (rnd, i)
             admitted.append(r)
-        took = set(int(i) for i in order[:cnt])
-        waiting = [r for i, r in enumerate(pending) if i not in took]
-        return admitted, waiting
+        if cnt == n:
+            return admitted, []
+        took = set(order[:cnt].tolist())
+        return admitted, [r for i, r in enumerate(pending) if i not in took]
 
     def _commit_native(self, batch, mode):
-        groups = {}
-        for r in batch:
-            arr, i = r._batch
-            groups.setdefault(id(arr), (arr, []))[1].append(i)
-        for arr, idx in groups.values():
-            _ok(self.cache.commit_batch(arr, idx, mode), "rc_commit")
-            view = _req_view(arr)
+        rnd0 = batch[0]._batch[0] if batch else None
+        if all(r._batch[0] is rnd0 for r in batch):     # one admission round: one call
+            groups = [(rnd0, batch)]
+        else:
+            by = {}
             for r in batch:
-                if r._batch[0] is arr:
-                    r.node = int(view["node"][r._batch[1]])
+                by.setdefault(id(r._batch[0]), (r._batch[0], []))[1].append(r)
+            groups = list(by.values())
+        for rnd, rs in groups:
+            idx = np.fromiter((r._batch[1] for r in rs), np.int32, len(rs))
+            _ok(self.cache.commit_batch(rnd.req, idx, mode), "rc_commit")
+            node = rnd.req["node"].tolist()
+            for r in rs:
+                r.node = node[r._batch[1]]
 
     def commit_prompts(self, batch: list):
         """After prefill: insert each prompt, keep it pinned, drop the admission pin."""
@@ -260,7 +280,7 @@ def plan_from_rows(rows: list) -> dict:
 class DeviceEngine:
     """KV pool + slot tables in HBM and the kernel launches of one batch."""
 
-    def __init__(self, shape, pool_slots: int, device="cuda", table_cap: int = 1 << 22):
+    def __init__(self, shape, pool_slots: int, device="cuda"):
         import torch
         self.torch = torch
         self.shape = shape
@@ -275,9 +295,12 @@ class DeviceEngine:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.pool = make_pool_desc(self.pool_k, self.pool_v, self.err, mla=shape.mla, head_dim_v=shape.head_dim_v)
         self.desc = make_attn_desc(self.pool, shape.q_heads, shape.scale)
-        self.table = torch.zeros(table_cap, dtype=torch.int32, device=dev)
+        self.sms = torch.cuda.get_device_properties(dev).multi_processor_count if dev.type == "cuda" else 1
         self._ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
-        self.timing = False          # record CUDA events around every device call
+        self._stage = [None, None]   # [pinned host int32, device int32, event] x 2, used in turn
+        self._stage_next = 0
+        self.timing = False          # record CUDA events around device calls
+        self.timing_every = 1        # decode steps: events on every n-th step only
         self.events = {}             # call name -> [(start, end, info)]
         self.launches = 0            # kernels launched by the library (counted per call)
         self._ev_pool = []
@@ -322,20 +345,40 @@ class DeviceEngine:
     def to_device(self, arr):
         return self.pinned(arr).to(self.device, non_blocking=True)
 
-    def upload_batch(self, batch: list, cascade: bool, planner=None):
-        """Slot rows of the batch -> device table; returns the batch's device layout."""
+    def stage(self, arrays: list) -> list:
+        """Host int32 arrays -> device, through one pinned staging buffer and
+        one host-to-device copy; returns device views in the same order and
+        shapes.  Two staging buffers are used in turn, and one is rewritten
+        only after the copy that last read it has run.  The device copy is
+        ordered on the current stream after every earlier kernel, so kernels
+        of the previous batch have finished reading a buffer it overwrites."""
         torch = self.torch
-        lens = np.asarray([len(r.slots) for r in batch], np.int64)
-        starts = np.zeros(len(batch), np.int64)
-        if len(batch) > 1:
-            starts[1:] = np.cumsum(lens[:-1])
-        total = int(lens.sum())
-        if total > self.table.numel():
-            self.table = torch.zeros(total, dtype=torch.int32, device=self.device)
-        flat = np.concatenate([r.slots for r in batch]).astype(np.int32) if batch else np.zeros(0, np.int32)
-        self.table[:total].copy_(self.pinned(flat), non_blocking=True)
-        lay = BatchLayout(self, batch, starts, cascade, planner)
-        return lay
+        offs, n = [], 0
+        for a in arrays:
+            offs.append(n)
+            n += (a.size + 63) // 64 * 64      # 256-byte aligned views
+        n = max(n, 64)
+        k = self._stage_next
+        self._stage_next ^= 1
+        slot = self._stage[k]
+        if slot is not None:
+            slot[2].synchronize()
+        if slot is None or slot[0].numel() < n:
+            cap = max(n + n // 4, 1 << 16)
+            slot = [torch.empty(cap, dtype=torch.int32).pin_memory(),
+                    torch.empty(cap, dtype=torch.int32, device=self.device), torch.cuda.Event()]
+            self._stage[k] = slot
+        host, dev, ev = slot
+        hv = host.numpy()
+        for a, o in zip(arrays, offs):
+            hv[o:o + a.size] = a.reshape(-1)
+        dev[:n].copy_(host[:n], non_blocking=True)
+        ev.record()
+        return [dev[o:o + a.size].view(a.shape) for a, o in zip(arrays, offs)]
+
+    def upload_batch(self, batch: list, cascade: bool, planner=None, parts=("extend", "decode")):
+        """Slot rows and index arrays of the batch -> device; returns its layout."""
+        return BatchLayout(self, batch, cascade, planner, parts)
 
     # -- kernels
     def store(self, slots_dev, k, v):
@@ -352,22 +395,25 @@ class DeviceEngine:
     def prepare_decode(self, lay):
         T, B = lay.max_new, lay.batch_size
         casc = lay.casc if lay.use_cascade else None
-        lay.kv_tables = [make_kv_table(self.table, lay.dec_start, lay.dec_len[t], int(lay.dec_max[t]))
-                         for t in range(T)]
-        sizes = {}
-        for kv in lay.kv_tables:
-            if kv.max_len not in sizes:
-                sizes[kv.max_len] = attn_decode_workspace(self.desc, B, kv.max_len, casc)
-        lay.ws_bytes = max(sizes.values()) if sizes else 256
+        lay.kv_tables = None
+        dec_max = lay.dec_max.tolist() if T else []
+        lay.ws_bytes = self._decode_ws(B, set(dec_max), casc)
         lay.ws = self.workspace(lay.ws_bytes)
         lay.casc_ref = C.byref(casc) if casc is not None else None
         lay.slot_ptrs = [lay.decode_slots[t].data_ptr() for t in range(T)]
+        # one table descriptor, its length row and bound set per step
+        lay.kv = make_kv_table(lay.table, lay.dec_start, lay.dec_len[0], dec_max[0]) if T else None
+        lay.kv_ref = C.byref(lay.kv) if T else None
+        lay.len_ptrs = [lay.dec_len[t].data_ptr() for t in range(T)]
+        lay.dec_max_list = dec_max
+        lay.pool_ref = C.byref(self.pool)
+        lay.desc_ref = C.byref(self.desc)
         # kernels per step: cascade (if any) + table pass + merge when a row is split
         # (the same thresholds as the library's plan)
-        sms = self.torch.cuda.get_device_properties(self.device).multi_processor_count
+        sms = self.sms
         if self.shape.mla:
             base = B * (self.shape.q_heads // 16)
-            max_len = max(kv.max_len for kv in lay.kv_tables) if lay.kv_tables else 0
+            max_len = max(dec_max) if dec_max else 0
             splits = min(max(-(-4 * sms // max(base, 1)), 1), max(-(-max_len // 1024), 1))
             split = splits > 1
         else:
@@ -375,20 +421,37 @@ class DeviceEngine:
         lay.decode_kernels = (1 if casc is not None else 0) + 1 + (1 if split else 0)
         lay.stream = C.c_void_p(self.torch.cuda.current_stream(self.device).cuda_stream)
 
+    def _decode_ws(self, B: int, max_lens, casc) -> int:
+        """Largest workspace attn_decode asks for over the steps' bounds."""
+        L = lib()
+        dref = C.byref(self.desc)
+        cref = C.byref(casc) if casc is not None else None
+        n = C.c_size_t(0)
+        best = 256
+        for m in max_lens:
+            st = L.attn_decode_workspace(dref, B, int(m), cref, C.byref(n))
+            if st != RC_OK:
+                raise RCError("attn_decode_workspace", st)
+            best = max(best, n.value)
+        return best
+
     def decode_step(self, lay, t: int, q, k, v, out, lse=None):
         L = lib()
         B = lay.batch_size
         ev = None
-        if self.timing:
+        if self.timing and t % self.timing_every == 0:
             ev = (self._event(), self._event(), self._event())
             ev[0].record()
-        st = L.kv_store(C.byref(self.pool), lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
+        st = L.kv_store(lay.pool_ref, lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
                         B, None, None, lay.stream)
         if st != RC_OK:
             raise RCError("kv_store", st)
         if ev:
             ev[1].record()
-        st = L.attn_decode(C.byref(self.desc), q.data_ptr(), C.byref(lay.kv_tables[t]), B, lay.casc_ref,
+        kv = lay.kv
+        kv.len = lay.len_ptrs[t]          # read by the call itself, not by its kernels
+        kv.max_len = lay.dec_max_list[t]
+        st = L.attn_decode(lay.desc_ref, q.data_ptr(), lay.kv_ref, B, lay.casc_ref,
                            out.data_ptr(), lse.data_ptr() if lse is not None else None, lay.ws.data_ptr(),
                            lay.ws_bytes, lay.stream)
         if st != RC_OK:
@@ -408,66 +471,97 @@ class DeviceEngine:
 
 
 class BatchLayout:
-    """Device-side index arrays of one admitted batch."""
+    """Device-side index arrays of one admitted batch (one staging copy).
 
-    def __init__(self, eng: DeviceEngine, batch: list, starts: np.ndarray, cascade: bool, planner=None):
-        torch = eng.torch
-        dev = eng.device
+    parts: "extend" (prefill: new-token slots, per-request extents) and/or
+    "decode" (per-step slots and lengths, cascade segments).  A batch taken
+    from one native admission round is laid out from the round's flat slot
+    array with vectorised indexing; otherwise from each request's slot row."""
+
+    def __init__(self, eng: DeviceEngine, batch: list, cascade: bool, planner=None,
+                 parts=("extend", "decode")):
         self.eng = eng
         self.batch = batch
-        self.batch_size = len(batch)
-        B = len(batch)
-        L = np.asarray([r.prompt_len for r in batch], np.int64)
-        first = np.asarray([r.first for r in batch], np.int64)
+        self.batch_size = B = len(batch)
+        rnd = batch[0]._batch[0] if B and hasattr(batch[0], "_batch") else None
+        if rnd is not None and all(getattr(r, "_batch", (None,))[0] is rnd for r in batch):
+            idx = np.fromiter((r._batch[1] for r in batch), np.int64, B)
+            flat = rnd.flat
+            starts = rnd.off[idx]
+            L = rnd.req["prompt_len"][idx]
+            first = rnd.req["first"][idx]
+            max_new = rnd.req["max_new"][idx]
+        else:
+            rows = np.fromiter((len(r.slots) for r in batch), np.int64, B)
+            starts = np.zeros(B, np.int64)
+            if B > 1:
+                np.cumsum(rows[:-1], out=starts[1:])
+            flat = np.concatenate([r.slots for r in batch]) if B else np.zeros(0, np.int32)
+            L = np.fromiter((r.prompt_len for r in batch), np.int64, B)
+            first = np.fromiter((r.first for r in batch), np.int64, B)
+            max_new = np.fromiter((r.max_new for r in batch), np.int64, B)
         n_new = L - first
         self.L, self.first, self.starts = L, first, starts
-        self.max_new = max([r.max_new for r in batch], default=0)
+        self.max_new = int(max_new.max()) if B else 0
         qo = np.zeros(B + 1, np.int64)
-        qo[1:] = np.cumsum(n_new)
+        np.cumsum(n_new, out=qo[1:])
         self.qo_host = qo
         self.max_q = int(n_new.max()) if B else 0
-        i32 = lambda a: eng.to_device(np.asarray(a, dtype=np.int32))
-        self.qo_indptr = i32(qo)
-        self.start_dev = i32(starts)
-        self.len_prompt = i32(L)
-        self.extend_table = make_kv_table(eng.table, self.start_dev, self.len_prompt, int(L.max()) if B else 0)
-        # slots of new tokens, in (request, position) order
-        ext = [r.slots[r.first:r.prompt_len] for r in batch]
-        self.extend_slots = i32(np.concatenate(ext) if ext else np.zeros(0, np.int32))
-        # decode: slots of step t for every row, and per-step lengths
-        T = self.max_new
-        if T:
-            dec = np.stack([r.slots[r.prompt_len:r.prompt_len + T] for r in batch], axis=1)  # [T, B]
-            self.decode_slots = i32(dec)
-            lens = (L[None, :] + np.arange(T)[:, None] + 1)
-        else:
-            self.decode_slots = None
-            lens = np.zeros((0, B), np.int64)
-        self.use_cascade = cascade and B > 1
+        host = [flat, starts, L]
+        names = ["table", "start_dev", "len_prompt"]
+        if "extend" in parts:
+            # slots of new tokens, in (request, position) order
+            pos = np.repeat(starts + first - qo[:-1], n_new) + np.arange(int(qo[-1]))
+            host += [qo, flat[pos]]
+            names += ["qo_indptr", "extend_slots"]
+        self.use_cascade = False
         self.private = np.zeros(B, np.int64)
         self.casc = None
-        if self.use_cascade:
-            plan = None
-            if planner is not None and all(r.node >= 0 for r in batch):
-                plan = planner(np.asarray([r.node for r in batch], np.int64))   # read off the tree
-            else:
-                plan = plan_from_rows([r.slots[:r.prompt_len] for r in batch])
-            if plan["n_seg"] > 0:
-                self.private = plan["private"].astype(np.int64)
-                ip = plan["seg_indptr"]
-                self.segments = [(plan["seg_slots"][ip[k]:ip[k + 1]],
-                                  plan["seg_rows"][plan["seg_row_indptr"][k]:plan["seg_row_indptr"][k + 1]])
-                                 for k in range(plan["n_seg"])]
-                self._casc_arrays = [i32(plan[k]) for k in ("seg_slots", "seg_indptr", "seg_row_indptr", "seg_rows",
-                                                            "req_seg_indptr", "req_seg_pos")]
-                self.casc = make_cascade(*self._casc_arrays, max_seg_rows=plan["max_seg_rows"],
-                                         max_seg_len=plan["max_seg_len"])
-            else:
-                self.use_cascade = False
-        self.dec_start = i32(starts + self.private)
-        self.dec_len = i32(lens - self.private[None, :]) if T else None
-        self.dec_max = (lens - self.private[None, :]).max(axis=1) if T else None
+        plan = None
+        T = self.max_new if "decode" in parts else 0
+        if T:
+            if (max_new != T).any():
+                raise ValueError("a decode batch needs one max_new for all its requests")
+            # slots of step t for every row [T, B], and per-step lengths
+            dec = flat[(starts + L)[None, :] + np.arange(T)[:, None]]
+            lens = L[None, :] + np.arange(T)[:, None] + 1
+            self.use_cascade = cascade and B > 1
+            if self.use_cascade:
+                if planner is not None and all(r.node >= 0 for r in batch):
+                    plan = planner(np.fromiter((r.node for r in batch), np.int64, B))   # read off the tree
+                else:
+                    plan = plan_from_rows([r.slots[:r.prompt_len] for r in batch])
+                if plan["n_seg"] > 0:
+                    self.private = plan["private"].astype(np.int64)
+                    ip = plan["seg_indptr"]
+                    self.segments = [(plan["seg_slots"][ip[k]:ip[k + 1]],
+                                      plan["seg_rows"][plan["seg_row_indptr"][k]:plan["seg_row_indptr"][k + 1]])
+                                     for k in range(plan["n_seg"])]
+                else:
+                    self.use_cascade = False
+                    plan = None
+            dec_len = lens - self.private[None, :]
+            self.dec_max = dec_len.max(axis=1)
+            host += [dec, starts + self.private, dec_len]
+            names += ["decode_slots", "dec_start", "dec_len"]
+        else:
+            self.dec_max = None
+        casc_keys = ("seg_slots", "seg_indptr", "seg_row_indptr", "seg_rows", "req_seg_indptr", "req_seg_pos")
+        if plan is not None:
+            host += [np.asarray(plan[k]) for k in casc_keys]
+        dv = eng.stage([np.asarray(a, np.int32) for a in host])
+        for nm, t in zip(names, dv):
+            setattr(self, nm, t)
+        if "extend" not in parts:
+            self.qo_indptr = self.extend_slots = None
+        if not T:
+            self.decode_slots = self.dec_start = self.dec_len = None
+        if plan is not None:
+            self._casc_arrays = dv[len(names):]
+            self.casc = make_cascade(*self._casc_arrays, max_seg_rows=plan["max_seg_rows"],
+                                     max_seg_len=plan["max_seg_len"])
+        self.extend_table = make_kv_table(self.table, self.start_dev, self.len_prompt, int(L.max()) if B else 0)
 
     def decode_table(self, t: int):
-        kv = make_kv_table(self.eng.table, self.dec_start, self.dec_len[t], int(self.dec_max[t]))
+        kv = make_kv_table(self.table, self.dec_start, self.dec_len[t], int(self.dec_max[t]))
         return kv, (self.casc if self.use_cascade else None)

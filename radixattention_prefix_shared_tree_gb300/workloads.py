@@ -59,7 +59,7 @@ class Runner:
 
     def _prefill(self, batch):
         eng, torch = self.engine, self.engine.torch
-        lay = eng.upload_batch(batch, cascade=False)
+        lay = eng.upload_batch(batch, cascade=False, parts=("extend",))
         total = int(lay.qo_host[-1])
         if total == 0:
             return
@@ -86,7 +86,7 @@ class Runner:
     def _decode(self, batch):
         eng, torch = self.engine, self.engine.torch
         planner = getattr(self.cache, "cascade_plan", None)
-        lay = eng.upload_batch(batch, cascade=self.cascade, planner=planner)
+        lay = eng.upload_batch(batch, cascade=self.cascade, planner=planner, parts=("decode",))
         self.last_layout = lay
         sh = eng.shape
         B = len(batch)
