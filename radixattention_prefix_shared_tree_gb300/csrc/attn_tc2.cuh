@@ -146,6 +146,36 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     // query tiles with at least one valid row
     const int n_qt = min(QT, ((min(n_rows_tok - tok0, TPC) * G) + TM - 1) / TM);
 
+    if (warp < 8) {
+        // Q rows of query tile warp/4, issued first so that their latency
+        // overlaps the set-up.  The row indices (cascade: a gather through
+        // seg_rows) are all loaded before the first copy is issued.
+        const int q = warp >> 2, r = tid & 127;
+        unsigned char* sQq = sQ + q * TM * D * 2;
+        int64_t qrow[CH];
+        bool qok[CH];
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+            const int gi = r + 128 * i;
+            const int rr = (gi & 7) + 8 * (gi / (8 * CH));
+            const int qr = q * TM + rr;
+            const int tk = tok0 + qr / G;
+            const int h = kvh * G + (qr % G);
+            qok[i] = tk < n_rows_tok;
+            if constexpr (MODE == rc::MQMode::kExtend) qrow[i] = (int64_t)(qo0 + tk) * p.q_heads + h;
+            else qrow[i] = qok[i] ? (int64_t)__ldg(p.seg_rows + qo0 + tk) * p.q_heads + h : 0;
+            if (!qok[i]) qrow[i] = 0;
+        }
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+            const int gi = r + 128 * i;
+            const int rr = (gi & 7) + 8 * (gi / (8 * CH));
+            const int c = (gi >> 3) % CH;
+            rc::cp_async16(rc::smem_u32(sQq + tc::cm_offset(rr, c, CH)), p.q + qrow[i] * D + c * 8,
+                           qok[i] ? 16u : 0u);
+        }
+        rc::cp_async_commit();
+    }
     if (tid == 0) {
         tc::mbar_init(q_full, 8);
         for (int s = 0; s < NS; ++s) {
@@ -178,24 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         const int row = q * TM + r;          // row within the CTA
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tq = tbase + q * 256 + lane_off;
-        unsigned char* sQq = sQ + q * TM * D * 2;
-        // Q rows of this tile (zero past the end)
-        for (int gi = r; gi < TM * CH; gi += 128) {
-            const int rr = (gi & 7) + 8 * (gi / (8 * CH));
-            const int c = (gi >> 3) % CH;
-            const int qr = q * TM + rr;
-            const int tk = tok0 + qr / G;
-            const int h = kvh * G + (qr % G);
-            int64_t qrow = 0;
-            if (tk < n_rows_tok) {
-                if constexpr (MODE == rc::MQMode::kExtend) qrow = (int64_t)(qo0 + tk) * p.q_heads + h;
-                else qrow = (int64_t)p.seg_rows[qo0 + tk] * p.q_heads + h;
-            }
-            rc::cp_async16(rc::smem_u32(sQq + tc::cm_offset(rr, c, CH)), p.q + qrow * D + c * 8,
-                           tk < n_rows_tok ? 16u : 0u);
-        }
-        rc::cp_async_commit();
-        rc::cp_async_wait<0>();
+        rc::cp_async_wait<0>();  // this thread's Q chunks (issued before the set-up)
         tc::fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(q_full);
@@ -289,45 +302,58 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             tc::fence_after();
         }
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
-        // ---- epilogue: normalised O row (and its log-sum-exp)
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const float lse2 = l_run > 0.f ? m_used + log2f(l_run) : -INFINITY;
-        const bool write = ok && row_valid && q < n_qt;
-        const int h = kvh * G + (row % G);
+        // ---- epilogue: normalised O rows and their log-sum-exp.  Rows go out
+        // through shared memory so that each store instruction writes whole
+        // row segments: per 32 columns, the warp's 32x32 fp32 block is staged
+        // (16-byte chunks XOR-swizzled by row: conflict-free both ways) in
+        // this warp's 4 KB of the Q region -- free once the tile's last P.V
+        // is done, since every S product was issued before it -- and read
+        // back 8 lanes per row, 4 rows per instruction.
+        if (q < n_qt) {
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            const float lse2 = l_run > 0.f ? m_used + log2f(l_run) : -INFINITY;
+            float* stg = reinterpret_cast<float*>(sQ + warp * 4096);
+            const int k8 = lane & 7;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t vb[32];
+                tc::tmem_ld32_issue(tq + 128 + c * 32, vb);
+                tc::tmem_ld_wait(vb);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            uint32_t vb[32];
-            tc::tmem_ld32_issue(tq + 128 + c * 32, vb);
-            tc::tmem_ld_wait(vb);
-            float v[32];
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4*>(stg + lane * 32 + ((k ^ (lane & 7)) * 4)) =
+                        make_float4(__uint_as_float(vb[4 * k]) * inv, __uint_as_float(vb[4 * k + 1]) * inv,
+                                    __uint_as_float(vb[4 * k + 2]) * inv, __uint_as_float(vb[4 * k + 3]) * inv);
+                __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(vb[j]);
-            if (!write) continue;
-            if constexpr (MODE == rc::MQMode::kExtend) {
-                __nv_bfloat16* dst = p.out + ((int64_t)(qo0 + r_tok) * p.q_heads + h) * D + c * 32;
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 w;
-                    w.x = rc::pack_bf16(v[j] * inv, v[j + 1] * inv);
-                    w.y = rc::pack_bf16(v[j + 2] * inv, v[j + 3] * inv);
-                    w.z = rc::pack_bf16(v[j + 4] * inv, v[j + 5] * inv);
-                    w.w = rc::pack_bf16(v[j + 6] * inv, v[j + 7] * inv);
-                    *reinterpret_cast<uint4*>(dst + j) = w;
+                for (int pass = 0; pass < 8; ++pass) {
+                    const int rr = pass * 4 + (lane >> 3);
+                    const float4 f = *reinterpret_cast<const float4*>(stg + rr * 32 + ((k8 ^ (rr & 7)) * 4));
+                    const int rc_ = q * TM + (warp & 3) * 32 + rr;  // row within the CTA
+                    const int tk = tok0 + rc_ / G;
+                    const int hh = kvh * G + (rc_ % G);
+                    if (!ok || tk >= n_rows_tok) continue;
+                    if constexpr (MODE == rc::MQMode::kExtend) {
+                        uint2 w;
+                        w.x = rc::pack_bf16(f.x, f.y);
+                        w.y = rc::pack_bf16(f.z, f.w);
+                        *reinterpret_cast<uint2*>(p.out + ((int64_t)(qo0 + tk) * p.q_heads + hh) * D + c * 32 + k8 * 4) =
+                            w;
+                    } else {
+                        *reinterpret_cast<float4*>(
+                            p.part_o + (((int64_t)(qo0 + tk) * p.q_heads + hh) * p.seg_chunks + chunk) * D + c * 32 +
+                            k8 * 4) = f;
+                    }
                 }
-            } else {
-                float* dst =
-                    p.part_o + (((int64_t)(qo0 + r_tok) * p.q_heads + h) * p.seg_chunks + chunk) * D + c * 32;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(dst + j) =
-                        make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv);
+                __syncwarp();
             }
-        }
-        if (write) {
-            if constexpr (MODE == rc::MQMode::kExtend) {
-                if (p.lse) p.lse[(int64_t)(qo0 + r_tok) * p.q_heads + h] = lse2 * rc::kLn2;
-            } else {
-                p.part_lse[((int64_t)(qo0 + r_tok) * p.q_heads + h) * p.seg_chunks + chunk] = lse2;
+            if (ok && row_valid) {
+                const int h = kvh * G + (row % G);
+                if constexpr (MODE == rc::MQMode::kExtend) {
+                    if (p.lse) p.lse[(int64_t)(qo0 + r_tok) * p.q_heads + h] = lse2 * rc::kLn2;
+                } else {
+                    p.part_lse[((int64_t)(qo0 + r_tok) * p.q_heads + h) * p.seg_chunks + chunk] = lse2;
+                }
             }
         }
     } else if (warp == 8 || warp == 9) {
