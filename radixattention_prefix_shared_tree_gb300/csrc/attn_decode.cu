@@ -56,6 +56,11 @@ struct DecParams {
 // streams its keys through a private ring of 16-key tiles (one m16 tile of
 // the swapped product) with cp.async, synchronising with __syncwarp only, so
 // the warps of an SM overlap each other's load latency and epilogues freely.
+// Wait until the grid this one depends on programmatically (the cascade
+// kernel) has finished and its writes are visible; returns at once when the
+// grid was launched without that dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 constexpr int kWarpKeys = 16;
 constexpr int kWarpStages = 3;
 constexpr int kWarpsPerCta = 4;
@@ -81,7 +86,10 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g_lane = lane >> 2, t_lane = lane & 3;
     const int it = blockIdx.x * kWarpsPerCta + warp;
-    if (it >= n_items) return;
+    if (it >= n_items) {
+        grid_dep_wait();
+        return;
+    }
     unsigned char* wbase = smem + warp * warp_smem_bytes<D>();
     unsigned char* sQ = wbase + kWarpStages * 2 * TILE_BYTES;
 
@@ -98,7 +106,10 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
     if (FUSED && lane == 0 && kvh == 0 && L > p.chunk) rc::flag_error(p.err, rc::kErrBadSlot);
     const int k0 = chunk * p.chunk;
     const int count = max(0, min(L - k0, p.chunk));
-    if (!FUSED && count == 0) return;
+    if (!FUSED && count == 0) {
+        grid_dep_wait();
+        return;
+    }
     const int32_t* keys = p.table + row0 + k0;
     const int n_tiles = (count + kWarpKeys - 1) / kWarpKeys;
 
@@ -263,6 +274,11 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
         sOwn[2 * t_lane + 1] = l_run[1] > 0.f ? m_run[1] + log2f(l_run[1]) : -INFINITY;
     }
     __syncwarp();
+    // The cascade kernel, when there is one, may still be running (this
+    // grid is its programmatic dependent): wait for it before reading its
+    // partials, and in any case before leaving, so that the end of this grid
+    // implies the end of both.
+    grid_dep_wait();
     if constexpr (!FUSED) {
         for (int h = 0; h < G; ++h) {
             const int64_t idx = ((int64_t)b * p.q_heads + kvh * G + h) * p.n_chunks + chunk;
@@ -479,15 +495,31 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     return RC_OK;
 }
 
+// after_cascade: launched as the programmatic dependent of the cascade kernel
+// just queued on the stream, so that its CTAs start on SMs the cascade leaves
+// free and as cascade CTAs finish, instead of after the whole cascade grid.
 template <int D, int G, bool FUSED>
-cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream_t st) {
+cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream_t st, bool after_cascade) {
     constexpr int smem = dec_smem_bytes<D>();
     cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G, FUSED>>(smem);
     if (e != cudaSuccess) return e;
     const int n_items = batch * kv_heads * p.n_chunks;
     const int grid = (n_items + kWarpsPerCta - 1) / kWarpsPerCta;
-    decode_split_kernel<D, G, FUSED><<<grid, 32 * kWarpsPerCta, smem, st>>>(p, n_items);
-    return cudaGetLastError();
+    if (!after_cascade) {
+        decode_split_kernel<D, G, FUSED><<<grid, 32 * kWarpsPerCta, smem, st>>>(p, n_items);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(32 * kWarpsPerCta);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, FUSED>, p, n_items);
 }
 
 template <int D, int G>
@@ -505,10 +537,11 @@ template <int D, int G>
 cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused, int batch,
                     int kv_heads, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
-    if (casc && casc->n_seg > 0 && casc->max_seg_rows > 0) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
+    const bool with_cascade = casc && casc->n_seg > 0 && casc->max_seg_rows > 0;
+    if (with_cascade) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
     if (e != cudaSuccess) return e;
-    return fused ? launch_split<D, G, true>(dp, batch, kv_heads, st)
-                 : launch_split<D, G, false>(dp, batch, kv_heads, st);
+    return fused ? launch_split<D, G, true>(dp, batch, kv_heads, st, with_cascade)
+                 : launch_split<D, G, false>(dp, batch, kv_heads, st, with_cascade);
 }
 
 template <int D>

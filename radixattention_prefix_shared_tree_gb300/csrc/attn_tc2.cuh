@@ -11,8 +11,9 @@
 //                      it, rescale the row's O in TMEM when its max grows by
 //                      more than 2^8;
 //   warps 8, 9         producers of the even and odd tiles: gather K/V rows
-//                      by slot id with cp.async into a 5-stage ring
-//                      (no-swizzle operand layout);
+//                      by slot id with 16-byte cp.async into a 5-stage ring
+//                      (no-swizzle operand layout), each lane's copies
+//                      arriving on the stage's mbarrier when they land;
 //   warp 10            issues every MMA (one thread) and owns TMEM.
 // Per 64-key tile and query tile q:  S_q = Q_q K^T (M=128, N=64, K=D) into
 // one of two S buffers, O_q += P_q V (M=128, N=D, K=64) with P read from
@@ -103,6 +104,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = blockIdx.y, z = blockIdx.z, blk = blockIdx.x;
+    // cascade: the table pass of attn_decode is this grid's programmatic
+    // dependent; it may start as soon as every CTA here has begun (it waits
+    // for this grid's end before reading the partials)
+    if constexpr (MODE == rc::MQMode::kCascade) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int tok0 = blk * TPC;
 
     // ---- this CTA's rows and keys (uniform)
@@ -358,9 +363,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         }
     } else if (warp == 8 || warp == 9) {
         // ============================================== producers (2 warps)
-        // warp 8 loads the even tiles, warp 9 the odd ones; each keeps one of
-        // its tiles in flight while it issues the next, and reads the slot ids
-        // of its next tile one tile ahead.
+        // warp 8 loads the even tiles, warp 9 the odd ones, each as far ahead
+        // as free stages allow (completion is signalled on the stage's
+        // barrier by the copies themselves), reading the slot ids of its next
+        // tile one tile ahead.
         // lane -> (key within an 8-key group, 16-byte column within a group of 4)
         const int klo = lane & 7, csub = lane >> 3;
         const int t0 = warp - 8;
@@ -373,7 +379,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         };
         int sl[2], sl_next[2];
         load_ids(t0, sl);
-        int prev = -1;
         for (int t = t0; t < n_tiles && ok; t += 2) {
             const int s = t % NS;
             load_ids(t + 2, sl_next);
@@ -400,20 +405,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                     rc::cp_async16(rc::smem_u32(sV + tc::cm_offset(key, c, CH)), p.pool_v + base + c * 8, bytes);
                 }
             }
-            rc::cp_async_commit();
-            // hand over this warp's previous tile once its rows have landed
-            if (prev >= 0) {
-                rc::cp_async_wait<1>();
-                tc::fence_proxy_async();
-                mbar_arrive(&kv_full[prev % NS]);
-            }
-            prev = t;
+            // each lane arrives on the stage's barrier when its copies have
+            // landed; the warp goes on to the next tile at once
+            tc::cp_async_mbar_arrive(&kv_full[s]);
             sl[0] = sl_next[0];
             sl[1] = sl_next[1];
         }
-        rc::cp_async_wait<0>();
-        tc::fence_proxy_async();
-        if (ok && prev >= 0) mbar_arrive(&kv_full[prev % NS]);
+        rc::cp_async_wait<0>();  // nothing in flight when the warp leaves
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     } else if (lane == 0) {
         // ==================================================== MMA (warp 10)
@@ -432,6 +430,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         if (ok && n_tiles > 0) {
             ok = tc::mbar_wait(&kv_full[0], 0, kWaitIter);
             tc::fence_after();
+            tc::fence_proxy_async();  // the rows arrived through the generic proxy; the tensor core reads them
             if (ok) issue_s(0);
         }
         for (int t = 0; t < n_tiles && ok; ++t) {
@@ -439,6 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             if (t + 1 < n_tiles) {  // next tile's S products first: they run during this softmax
                 ok = tc::mbar_wait(&kv_full[(t + 1) % NS], ((t + 1) / NS) & 1, kWaitIter);
                 tc::fence_after();
+                tc::fence_proxy_async();
                 if (!ok) break;
                 issue_s(t + 1);
             }

@@ -79,6 +79,13 @@ RC_DEV void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" :
 // make generic-proxy writes to shared memory visible to the tensor core
 RC_DEV void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// The mbarrier gets one of its expected arrivals (.noinc: counted in the
+// init count) once every cp.async this thread issued before has landed; the
+// thread itself does not wait.
+RC_DEV void cp_async_mbar_arrive(uint64_t* mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(rc::smem_u32(mbar)) : "memory");
+}
+
 RC_DEV void mbar_init(uint64_t* mbar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(rc::smem_u32(mbar)), "r"(count) : "memory");
 }
