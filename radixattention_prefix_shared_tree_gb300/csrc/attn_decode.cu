@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
                           ok ? 4u : 0u);
         }
     };
+    // a request's own keys are read once per step: they should not push the
+    // shared prefix (read by the cascade kernel every step) out of L2
+    const uint64_t pol = rc::l2_policy_evict_first();
     auto issue = [&](int t) {
         if (t < n_tiles) {
             unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
@@ -143,8 +146,8 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
                     bytes = 0;
                 }
                 const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
-                rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes);
-                rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes);
+                rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes, pol);
+                rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes, pol);
             }
         }
     };
@@ -193,16 +196,20 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
         rc::cp_async_commit();
         const unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
-        // S^T (16 keys x 8 heads) = K Q^T
+        // S^T (16 keys x 8 heads) = K Q^T, even and odd k-steps in two
+        // accumulators (two independent chains of MMAs)
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         {
+            float s2[4] = {0.f, 0.f, 0.f, 0.f};
             const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a0, a1, a2, a3;
                 rc::ldmatrix_x4(rc::smem_u32(sK + rc::swz<CH>(key, ks * 2 + (lane >> 4))), a0, a1, a2, a3);
-                rc::mma_bf16_16816(s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                rc::mma_bf16_16816(ks & 1 ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
             }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[i] += s2[i];
         }
         const int key_lo = t * kWarpKeys + g_lane;
         const bool v_lo = key_lo < count, v_hi = key_lo + 8 < count;
@@ -210,29 +217,41 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
         s[1] = v_lo ? s[1] * p.scale_log2 : -INFINITY;
         s[2] = v_hi ? s[2] * p.scale_log2 : -INFINITY;
         s[3] = v_hi ? s[3] * p.scale_log2 : -INFINITY;
+        // Online softmax with a lazy reference: exponentials are taken
+        // against m_run, which moves (rescaling O and l) only when a head's
+        // max grows past it by more than 2^8 -- the terms stay below 2^8, and
+        // most tiles skip the 32 multiplies of the rescale.
         float mx[2] = {fmaxf(s[0], s[2]), fmaxf(s[1], s[3])};
-        float alpha[2], mu[2];
+        float alpha[2] = {1.f, 1.f};
+        bool grow = false;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
             mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
-            const float m_new = fmaxf(m_run[j], mx[j]);
-            mu[j] = m_new == -INFINITY ? 0.f : m_new;
-            alpha[j] = rc::fast_exp2(m_run[j] - mu[j]);
-            m_run[j] = m_new;
+            if (mx[j] > m_run[j] + 8.f) {
+                alpha[j] = rc::fast_exp2(m_run[j] - mx[j]);  // 0 while nothing was seen
+                m_run[j] = mx[j];
+                grow = true;
+            }
         }
-        const float p0 = rc::fast_exp2(s[0] - mu[0]), p1 = rc::fast_exp2(s[1] - mu[1]);
-        const float p2 = rc::fast_exp2(s[2] - mu[0]), p3 = rc::fast_exp2(s[3] - mu[1]);
-        l_run[0] = l_run[0] * alpha[0] + p0 + p2;
-        l_run[1] = l_run[1] * alpha[1] + p1 + p3;
+        const float mu0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float mu1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
+        const float p0 = rc::fast_exp2(s[0] - mu0), p1 = rc::fast_exp2(s[1] - mu1);
+        const float p2 = rc::fast_exp2(s[2] - mu0), p3 = rc::fast_exp2(s[3] - mu1);
+        if (__any_sync(0xffffffffu, grow)) {
+            l_run[0] *= alpha[0];
+            l_run[1] *= alpha[1];
 #pragma unroll
-        for (int i = 0; i < KS; ++i) {
-            o[i][0] *= alpha[0];
-            o[i][1] *= alpha[1];
-            o[i][2] *= alpha[0];
-            o[i][3] *= alpha[1];
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= alpha[0];
+                o[i][1] *= alpha[1];
+                o[i][2] *= alpha[0];
+                o[i][3] *= alpha[1];
+            }
         }
+        l_run[0] += p0 + p2;
+        l_run[1] += p1 + p3;
         const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));
         const uint32_t pb1 = rc::movmatrix_trans(rc::pack_bf16(p2, p3));
         {

@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         // tile one tile ahead.
         // lane -> (key within an 8-key group, 16-byte column within a group of 4)
         const int klo = lane & 7, csub = lane >> 3;
+        // keys here are shared: by the CTAs of the other row blocks, and (a
+        // cached prefix) by later steps -- keep them in L2
+        const uint64_t pol = rc::l2_policy_evict_last();
         const int t0 = warp - 8;
         auto load_ids = [&](int t, int (&sl)[2]) {
 #pragma unroll
@@ -401,8 +404,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
 #pragma unroll
                 for (int cg = 0; cg < CH / 4; ++cg) {
                     const int c = cg * 4 + csub;
-                    rc::cp_async16(rc::smem_u32(sK + tc::cm_offset(key, c, CH)), p.pool_k + base + c * 8, bytes);
-                    rc::cp_async16(rc::smem_u32(sV + tc::cm_offset(key, c, CH)), p.pool_v + base + c * 8, bytes);
+                    rc::cp_async16(rc::smem_u32(sK + tc::cm_offset(key, c, CH)), p.pool_k + base + c * 8, bytes,
+                                   pol);
+                    rc::cp_async16(rc::smem_u32(sV + tc::cm_offset(key, c, CH)), p.pool_v + base + c * 8, bytes,
+                                   pol);
                 }
             }
             // each lane arrives on the stage's barrier when its copies have
