@@ -294,14 +294,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                 const float2 l01 = fadd2(fadd2(ls[0], ls[1]), fadd2(ls[2], ls[3]));
                 l_run += l01.x + l01.y;
                 tc::tmem_st_wait();
+                // Last tile: see P(n-2).V done before handing over P(n-1), while
+                // o_done can only be at phase n-2 or n-1 (a parity wait tells
+                // two phases apart, not three; S(n-1) guarantees P(n-3).V).
+                if (t == n_tiles - 1 && t > 0) {
+                    ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (t - 1) & 1, kWaitIter)) && ok;
+                    tc::fence_after();
+                }
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[q * 2 + (t & 1)]);
             }
-            // the last two P.V products: S(n-1) only guarantees P(n-3).V, and a
-            // parity wait must not skip a phase
-            if (ok && n_tiles > 1)
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (n_tiles - 2) & 1, kWaitIter));
+            // the last P.V: o_done is at phase n-1 or n here
             if (ok && n_tiles > 0)
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(&o_done[q], (n_tiles - 1) & 1, kWaitIter));
             tc::fence_after();

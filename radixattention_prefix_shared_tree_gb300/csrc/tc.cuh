@@ -94,6 +94,10 @@ RC_DEV void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluste
 // Wait for the phase of the given parity to complete: at most max_iter probes
 // and at most about a second; returns false if it gave up.
 constexpr uint64_t kWaitNs = 1000000000ull;
+// Each probe may suspend the thread until the phase completes (at most this
+// many ns), instead of returning at once: waiting warps then leave the
+// shared-memory pipe to the warps doing work.
+constexpr uint32_t kSuspendNs = 20000;
 RC_DEV bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t max_iter) {
     const uint32_t a = rc::smem_u32(mbar);
     uint64_t t0 = 0;
@@ -101,10 +105,10 @@ RC_DEV bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t max_iter) {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}\n"
             : "=r"(done)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (done) return true;
         if ((i & 255) == 255) {
