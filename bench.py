@@ -6,7 +6,8 @@ GQA 32 query / 8 KV heads, head_dim 128, bf16, KV pool of 2^21 slots.  One
 step is the whole hot path over that batch: sched_order (longest prefix
 first), rc_match_prefix + pin, rc_alloc, slot tables to the device, kv_store
 + attn_extend of the questions, rc_insert of the prompts, 128 decode steps
-(kv_store + cascade attn_decode), rc_insert of prompt + outputs and
+(attn_decode_append: the new token's K/V stored inside the cascade decode),
+rc_insert of prompt + outputs and
 rc_release.  Every step serves a new batch of questions (inputs already in
 HBM, ~0.55 GB per step, larger than L2).
 
@@ -199,15 +200,17 @@ def torch_empty_like(torch, t):
 
 
 # -------------------------------------------------------------- algorithmic
-def decode_bytes(lay, t, shape):
-    """Unique K/V rows touched (shared segments once) x row bytes + indices + Q + O."""
+def decode_bytes(lay, t, shape, stored=True):
+    """Unique K/V rows touched (shared segments once) x row bytes + indices + Q + O,
+    + the new token's K/V written to the pool when the call stores it."""
     R = 2 * shape.kv_heads * shape.head_dim_k * 2
     L = lay.L + t + 1
     tail = (L - lay.private).sum()
     seg = sum(len(s) for s, _ in lay.segments) if lay.use_cascade else 0
     B = lay.batch_size
     qo = B * shape.q_heads * (shape.head_dim_k + shape.head_dim_v) * 2
-    return int((seg + tail) * R + (seg + tail) * 4 + qo), int(L.sum() * R)
+    store = B * R if stored else 0
+    return int((seg + tail) * R + (seg + tail) * 4 + qo + store), int(L.sum() * R)
 
 
 def extend_flops(lay, shape):

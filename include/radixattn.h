@@ -303,6 +303,23 @@ rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table
                       int32_t batch, const rc_cascade* cascade, void* out, float* lse,
                       void* ws, size_t ws_bytes, rc_stream_t stream);
 
+/* attn_decode for a step whose new token's K/V is not stored yet: kv_store of
+ * those rows followed by attn_decode, in one launch less [N49 s.2: the new
+ * token's K/V joins its request's edge; LMI decode phase].  k_new, v_new:
+ * [batch][kv_heads][head_dim] bf16, 16-byte aligned, the K/V of each row's
+ * last key (position len[b]-1, slot slots[start[b]+len[b]-1]).  The kernel
+ * that reads row b's last key writes k_new[b]/v_new[b] to that slot of the
+ * pool and uses them directly for that key; the result (out, lse) is that of
+ * attn_decode on the updated pool, bit for bit.  The last key must be in the
+ * row's table part, not in a cascade segment (cascade segments hold cached
+ * keys only).  A bad slot id for it is skipped and flags RC_ERR_DEVICE.
+ * Same workspace (attn_decode_workspace) and errors as attn_decode; the latent
+ * layout returns RC_ERR_UNSUPPORTED (use kv_store + attn_decode). */
+rc_status attn_decode_append(const rc_attn_desc* desc, const void* q, const void* k_new,
+                             const void* v_new, const rc_kv_table* kv, int32_t batch,
+                             const rc_cascade* cascade, void* out, float* lse, void* ws,
+                             size_t ws_bytes, rc_stream_t stream);
+
 /* attn_decode without any device allocation, for callers that cannot call
  * cudaMalloc or hand over a workspace: for example a serving loop whose
  * device memory is all carved up at start-up (the KV pool takes what is left)

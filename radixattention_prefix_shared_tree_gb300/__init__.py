@@ -86,6 +86,8 @@ SIGNATURES = {
     "kv_store": (I32, [P(rc_pool_desc), VP, VP, VP, I32, VP, VP, VP]),
     "attn_decode_workspace": (I32, [P(rc_attn_desc), I32, I32, P(rc_cascade), P(C.c_size_t)]),
     "attn_decode": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP, C.c_size_t, VP]),
+    "attn_decode_append": (I32, [P(rc_attn_desc), VP, VP, VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP,
+                                 C.c_size_t, VP]),
     "attn_decode_static": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP]),
     "attn_extend_workspace": (I32, [P(rc_attn_desc), I32, I32, I32, P(C.c_size_t)]),
     "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
@@ -406,6 +408,16 @@ def attn_decode(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=Non
                            C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse), _tp(ws),
                            int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream))
     _check("attn_decode", st)
+
+
+def attn_decode_append(desc: rc_attn_desc, q, k_new, v_new, kv: rc_kv_table, batch: int, out, lse=None, ws=None,
+                       cascade: rc_cascade | None = None, stream=None):
+    """attn_decode that also stores each row's last key from k_new/v_new
+    ([batch][kv_heads][head_dim] bf16) into its pool slot (see the header)."""
+    st = lib().attn_decode_append(C.byref(desc), _tp(q), _tp(k_new), _tp(v_new), C.byref(kv), int(batch),
+                                  C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse), _tp(ws),
+                                  int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream))
+    _check("attn_decode_append", st)
 
 
 def attn_decode_static(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=None,

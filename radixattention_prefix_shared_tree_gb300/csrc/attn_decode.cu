@@ -50,6 +50,9 @@ struct DecParams {
     int32_t seg_chunks;
     __nv_bfloat16* out;
     float* lse;
+    // attn_decode_append: each row's last key comes from here and is stored
+    const __nv_bfloat16* k_new;  // [B][kv_heads][D] or NULL
+    const __nv_bfloat16* v_new;
 };
 
 // Decode with one warp per item (request b, KV head, key chunk).  Each warp
@@ -112,6 +115,26 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
     }
     const int32_t* keys = p.table + row0 + k0;
     const int n_tiles = (count + kWarpKeys - 1) / kWarpKeys;
+    // attn_decode_append: the row's last key (position L-1) is the step's new
+    // token.  The warp whose keys hold it gathers it from k_new/v_new and
+    // writes it to its pool slot (lanes 0..CH-1 the K row, CH..2CH-1 the V row).
+    const int new_at = (p.k_new && L > 0 && L - 1 >= k0 && L - 1 < k0 + count) ? L - 1 - k0 : -1;
+    if (new_at >= 0) {
+        const int slot = keys[new_at];
+        if (slot < 0 || (int64_t)slot >= p.n_slots) {
+            if (lane == 0) rc::flag_error(p.err, rc::kErrBadSlot);
+        } else if (lane < 2 * CH) {
+            const int c = lane % CH;
+            const int64_t off = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
+            const int64_t src = ((int64_t)b * p.kv_heads + kvh) * D + c * 8;
+            if (lane < CH)
+                *reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(p.pool_k) + off) =
+                    *reinterpret_cast<const uint4*>(p.k_new + src);
+            else
+                *reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(p.pool_v) + off) =
+                    *reinterpret_cast<const uint4*>(p.v_new + src);
+        }
+    }
 
     int32_t* sSlot = reinterpret_cast<int32_t*>(sQ + 8 * D * 2);  // [kSlotRing][kWarpKeys]
     // Slot ids travel through the cp.async pipeline too: the group committed at
@@ -139,15 +162,23 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
                 const int r = lin / CH, c = lin % CH;
                 int slot = ring[r];
                 uint32_t bytes = 16;
-                if (t * kWarpKeys + r >= count) { slot = 0; bytes = 0; }
-                else if (slot < 0 || (int64_t)slot >= p.n_slots) {
+                const __nv_bfloat16* bk = p.pool_k;
+                const __nv_bfloat16* bv = p.pool_v;
+                int64_t row = 0;
+                if (t * kWarpKeys + r >= count) bytes = 0;
+                else if (t * kWarpKeys + r == new_at) {  // the appended key, straight from its source
+                    bk = p.k_new;
+                    bv = p.v_new;
+                    row = b;
+                } else if (slot < 0 || (int64_t)slot >= p.n_slots) {
                     rc::flag_error(p.err, rc::kErrBadSlot);
-                    slot = 0;
                     bytes = 0;
+                } else {
+                    row = slot;
                 }
-                const int64_t roff = ((int64_t)slot * p.kv_heads + kvh) * D + c * 8;
-                rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), p.pool_k + roff, bytes, pol);
-                rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), p.pool_v + roff, bytes, pol);
+                const int64_t roff = (row * p.kv_heads + kvh) * D + c * 8;
+                rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), bk + roff, bytes, pol);
+                rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), bv + roff, bytes, pol);
             }
         }
     };
@@ -594,14 +625,17 @@ extern "C" rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t bat
     return RC_OK;
 }
 
-extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv, int32_t batch,
-                                 const rc_cascade* casc, void* out, float* lse, void* ws, size_t ws_bytes,
-                                 rc_stream_t stream) {
+namespace {
+
+rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new, const void* v_new,
+                      const rc_kv_table* kv, int32_t batch, const rc_cascade* casc, void* out, float* lse, void* ws,
+                      size_t ws_bytes, rc_stream_t stream) {
     if (!desc || !kv || batch < 0) return RC_ERR_ARG;
     if (batch == 0) return RC_OK;
     if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
     const bool use_casc = casc && casc->n_seg > 0;
     if (desc->pool.mla) {  // one latent KV head: its own kernel (attn_decode_mla.cu)
+        if (k_new) return RC_ERR_UNSUPPORTED;
         if (use_casc) return RC_ERR_UNSUPPORTED;
         if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return RC_ERR_ARG;
         return rc_host::mla_decode(desc, q, kv, batch, out, lse, ws, ws_bytes, (cudaStream_t)stream);
@@ -645,6 +679,8 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
     dp.seg_chunks = pl.seg_chunks;
     dp.out = static_cast<__nv_bfloat16*>(out);
     dp.lse = lse;
+    dp.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    dp.v_new = static_cast<const __nv_bfloat16*>(v_new);
     rc::MQParams mp{};
     mp.q = dp.q;
     mp.pool_k = dp.pool_k;
@@ -684,6 +720,23 @@ extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const 
         merge_kernel<64><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
                                              pl.seg_chunks, ri, rp, desc->q_heads, o, lse, P.err);
     return rc_host::launch_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" rc_status attn_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table* kv, int32_t batch,
+                                 const rc_cascade* casc, void* out, float* lse, void* ws, size_t ws_bytes,
+                                 rc_stream_t stream) {
+    return decode_impl(desc, q, nullptr, nullptr, kv, batch, casc, out, lse, ws, ws_bytes, stream);
+}
+
+extern "C" rc_status attn_decode_append(const rc_attn_desc* desc, const void* q, const void* k_new,
+                                        const void* v_new, const rc_kv_table* kv, int32_t batch,
+                                        const rc_cascade* casc, void* out, float* lse, void* ws, size_t ws_bytes,
+                                        rc_stream_t stream) {
+    if (!k_new || !v_new) return RC_ERR_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 15) return RC_ERR_ARG;
+    return decode_impl(desc, q, k_new, v_new, kv, batch, casc, out, lse, ws, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

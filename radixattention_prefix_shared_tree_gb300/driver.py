@@ -301,6 +301,7 @@ class DeviceEngine:
         self._stage_next = 0
         self.timing = False          # record CUDA events around device calls
         self.timing_every = 1        # decode steps: events on every n-th step only
+        self.fuse_store = True       # decode steps store the new token inside attn_decode_append
         self.events = {}             # call name -> [(start, end, info)]
         self.launches = 0            # kernels launched by the library (counted per call)
         self._ev_pool = []
@@ -436,31 +437,40 @@ class DeviceEngine:
         return best
 
     def decode_step(self, lay, t: int, q, k, v, out, lse=None):
+        """One decode step: the new token's K/V goes into its slot and the
+        step's attention runs -- fused into one call (attn_decode_append)
+        for GQA pools, kv_store + attn_decode for the latent layout."""
         L = lib()
         B = lay.batch_size
         ev = None
         if self.timing and t % self.timing_every == 0:
-            ev = (self._event(), self._event(), self._event())
+            ev = (self._event(), self._event())
             ev[0].record()
-        st = L.kv_store(lay.pool_ref, lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
-                        B, None, None, lay.stream)
-        if st != RC_OK:
-            raise RCError("kv_store", st)
-        if ev:
-            ev[1].record()
         kv = lay.kv
         kv.len = lay.len_ptrs[t]          # read by the call itself, not by its kernels
         kv.max_len = lay.dec_max_list[t]
-        st = L.attn_decode(lay.desc_ref, q.data_ptr(), lay.kv_ref, B, lay.casc_ref,
-                           out.data_ptr(), lse.data_ptr() if lse is not None else None, lay.ws.data_ptr(),
-                           lay.ws_bytes, lay.stream)
-        if st != RC_OK:
-            raise RCError("attn_decode", st)
+        if self.fuse_store and v is not None:
+            st = L.attn_decode_append(lay.desc_ref, q.data_ptr(), k.data_ptr(), v.data_ptr(), lay.kv_ref, B,
+                                      lay.casc_ref, out.data_ptr(), lse.data_ptr() if lse is not None else None,
+                                      lay.ws.data_ptr(), lay.ws_bytes, lay.stream)
+            if st != RC_OK:
+                raise RCError("attn_decode_append", st)
+            kernels = lay.decode_kernels
+        else:
+            st = L.kv_store(lay.pool_ref, lay.slot_ptrs[t], k.data_ptr(), v.data_ptr() if v is not None else None,
+                            B, None, None, lay.stream)
+            if st != RC_OK:
+                raise RCError("kv_store", st)
+            st = L.attn_decode(lay.desc_ref, q.data_ptr(), lay.kv_ref, B, lay.casc_ref,
+                               out.data_ptr(), lse.data_ptr() if lse is not None else None, lay.ws.data_ptr(),
+                               lay.ws_bytes, lay.stream)
+            if st != RC_OK:
+                raise RCError("attn_decode", st)
+            kernels = 1 + lay.decode_kernels
         if ev:
-            ev[2].record()
-            self.events.setdefault("kv_store", []).append((ev[0], ev[1], ("store", B)))
-            self.events.setdefault("attn_decode", []).append((ev[1], ev[2], ("decode", lay, t)))
-        self.launches += 1 + lay.decode_kernels
+            ev[1].record()
+            self.events.setdefault("attn_decode", []).append((ev[0], ev[1], ("decode", lay, t)))
+        self.launches += kernels
 
     def decode(self, lay, t: int, q, out, lse=None):
         kv, casc = lay.decode_table(t)

@@ -242,6 +242,101 @@ def test_cascade_equals_flat_and_oracle(cuda, Hq, Hkv, D):
     assert d.max() <= MAX_ABS and d.mean() <= MEAN_ABS
 
 
+def _append_vs_store_then_decode(cuda, Hq, Hkv, D, rows, casc_of=None):
+    """attn_decode_append on one copy of the pool == kv_store + attn_decode on
+    another: outputs and LSE bit for bit, and the pools equal afterwards; the
+    result also matches the oracle over the stored pool."""
+    n_slots = 20000
+    B = len(rows)
+    lens = [len(r) for r in rows]
+    pa = Pool(n_slots, Hkv, D, cuda, 7 + Hq)
+    pb = Pool(n_slots, Hkv, D, cuda, 7 + Hq)
+    _, table, start, length = _tables(lens, n_slots, 0, cuda)
+    table.copy_(torch.from_numpy(np.concatenate(rows)).to(cuda))
+    g = torch.Generator().manual_seed(21)
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    k_new = rand_bf16(g, (B, Hkv, D), cuda)
+    v_new = rand_bf16(g, (B, Hkv, D), cuda)
+    last = torch.from_numpy(np.asarray([r[-1] for r in rows], np.int32)).to(cuda)
+    scale = 1.0 / np.sqrt(D)
+    if casc_of is None:
+        kv, casc = ra.make_kv_table(table, start, length, max(lens)), None
+    else:
+        kv, casc = casc_of(table, start, lens)
+    outs = []
+    for pool, fused in ((pa, False), (pb, True)):
+        desc = ra.make_attn_desc(pool.desc, Hq, scale)
+        ws = torch.empty(ra.attn_decode_workspace(desc, B, kv.max_len, casc), dtype=torch.uint8, device=cuda)
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+        if fused:
+            ra.attn_decode_append(desc, q, k_new, v_new, kv, B, out, lse, ws, cascade=casc)
+        else:
+            ra.kv_store(pool.desc, last, k_new, v_new)
+            ra.attn_decode(desc, q, kv, B, out, lse, ws, cascade=casc)
+        assert ra.rc_sync(pool.err) == ra.RC_OK
+        outs.append((bits(out), lse.cpu().numpy()))
+    assert (outs[0][0] == outs[1][0]).all()
+    assert (outs[0][1].view(np.uint32) == outs[1][1].view(np.uint32)).all()
+    assert (bits(pa.k) == bits(pb.k)).all() and (bits(pa.v) == bits(pb.v)).all()
+    pa.kb, pa.vb = bits(pa.k), bits(pa.v)
+    ref, ref_lse = _oracle_rows(pa, rows, bits(q), lens, Hq, Hkv, D, scale)
+    check(outs[1][0], ref, outs[1][1], ref_lse)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,lens", [(32, 8, 128, [1, 17, 64, 200, 3000, 4097]),
+                                            (4, 4, 64, [1, 2, 63, 64, 65, 130])])
+def test_decode_append_split_rows(cuda, Hq, Hkv, D, lens):
+    """Few rows: the keys are split over chunks, the last key sits in the last."""
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(20000).astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    rows = [perm[offs[i]:offs[i + 1]] for i in range(len(lens))]
+    _append_vs_store_then_decode(cuda, Hq, Hkv, D, rows)
+
+
+def test_decode_append_fused_rows(cuda):
+    """Enough rows for one warp per row and KV head (fused epilogue)."""
+    rng = np.random.default_rng(6)
+    lens = rng.integers(1, 90, size=200)
+    perm = rng.permutation(20000).astype(np.int32)
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    rows = [perm[offs[i]:offs[i + 1]] for i in range(len(lens))]
+    _append_vs_store_then_decode(cuda, 32, 8, 128, rows)
+
+
+def test_decode_append_with_cascade(cuda):
+    """Shared root and mid segments in a cascade; the appended key is private."""
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(20000).astype(np.int32)
+    root, mids = perm[:700], [perm[700:900], perm[900:1157]]
+    off, rows = 1157, []
+    for b in range(12):
+        n = int(rng.integers(1, 150))
+        rows.append(np.concatenate([root, mids[b % 2] if b < 10 else np.zeros(0, np.int32),
+                                    perm[off:off + n]]).astype(np.int32))
+        off += n
+
+    def casc_of(table, start, lens):
+        segs, private = plan_cascade([r[:len(r) - 1] for r in rows])
+        B = len(rows)
+        seg_rows = np.concatenate([np.asarray(r, np.int32) for _, r in segs])
+        pos_of = [[p for p, b in enumerate(seg_rows) if b == bb] for bb in range(B)]
+        T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(cuda)
+        arrs = [T(np.concatenate([s for s, _ in segs])), T(np.concatenate([[0], np.cumsum([len(s) for s, _ in segs])])),
+                T(np.concatenate([[0], np.cumsum([len(r) for _, r in segs])])), T(seg_rows),
+                T(np.concatenate([[0], np.cumsum([len(x) for x in pos_of])])),
+                T(np.concatenate([np.asarray(x, np.int32) for x in pos_of]))]
+        casc = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs),
+                               max_seg_len=max(len(x) for x, _ in segs))
+        plen = np.asarray(lens) - private
+        kv = ra.make_kv_table(table, T(start.cpu().numpy() + private), T(plen), int(plen.max()))
+        kv._keep = kv._keep + (arrs,)
+        return kv, casc
+
+    _append_vs_store_then_decode(cuda, 32, 8, 128, rows, casc_of)
+
+
 def test_decode_reports_len_above_max_len(cuda):
     """A row longer than the promised max_len is reported, not read past."""
     pool = Pool(300, 8, 128, cuda, 1)
