@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--questions", type=int, default=N_QUESTIONS)
     ap.add_argument("--max-new", type=int, default=MAX_NEW)
     ap.add_argument("--pool-slots", type=int, default=0, help="KV pool size (default: the workload's 2^21)")
+    ap.add_argument("--no-paths", action="store_true",
+                    help="skip the per-path measurements (latent decode, host tree calls)")
     return ap.parse_args()
 
 
@@ -277,6 +279,54 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
 
 
 # -------------------------------------------------------------------- main
+def latent_path(dev, hbm, bf16, peak_src, steps: int = 8):
+    """Latent (MLA) decode at its full configuration: 128 requests, a
+    4,096-token shared prefix + U[0, 28,672] private tokens each, one
+    576-wide latent head, 128 query heads.  The contexts are stored
+    (kv_store, untimed), then `steps` decode steps run; attn_decode is timed
+    with CUDA events per call.  Both rooflines: bytes (unique latent rows,
+    the shared prefix once, and the rows this flat kernel actually reads)
+    and flops (2 * Hq * (576 + 512) per key)."""
+    import torch
+    import radixattention_prefix_shared_tree_gb300 as ra
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
+    from synth import traces
+    from synth.model import SynthModel
+
+    tr = traces.mla_long(steps=steps)
+    sh = tr.shape
+    model = SynthModel(sh, tr.seed, tr.vocab, device=dev)
+    eng = DeviceEngine(sh, tr.pool_slots, device=dev)
+    cache = ra.RadixCache(tr.pool_slots)
+    runner = wl.Runner(cache, model, eng, cascade=False, prefill_attention=False)
+    eng.start_timing(16 * steps + 64)
+    reqs = wl.run_mla(runner, tr)
+    torch.cuda.synchronize()
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+    evs = eng.events.get("attn_decode", [])
+    durs = [a.elapsed_time(b) * 1e-3 for a, b, _ in evs]
+    R = sh.head_dim_k * 2
+    shared = len(tr.shared)
+    ctx0 = np.asarray([r.prompt_len for r in reqs], np.int64)
+    uniq, logical, flops = [], [], []
+    for t in range(len(durs)):
+        ctx = ctx0 + t + 1
+        uniq.append((shared + (ctx - shared).sum()) * R)
+        logical.append(ctx.sum() * R)
+        flops.append(ctx.sum() * 2 * sh.q_heads * (sh.head_dim_k + sh.head_dim_v))
+    sec = sum(durs) / len(durs)
+    u, lg, f = np.mean(uniq), np.mean(logical), np.mean(flops)
+    return {"config": "128 requests, 4096 shared + U[0,28672] private tokens, latent 576 (512+64), "
+                      "128 query heads, bf16; %d decode steps" % len(durs),
+            "us_per_step": sec * 1e6, "tokens_per_s": len(reqs) / sec,
+            "unique_bytes": float(u), "logical_bytes": float(lg), "flops": float(f),
+            "hbm": {"achieved_unique_gbs": u / sec / 1e9, "achieved_read_gbs": lg / sec / 1e9, "peak": hbm,
+                    "frac_unique": u / sec / 1e9 / hbm, "frac_read": lg / sec / 1e9 / hbm},
+            "tensor": {"achieved_tflops": f / sec / 1e12, "peak": bf16, "frac": f / sec / 1e12 / bf16},
+            "peak_source": f"{peak_src} HBM copy and bf16 dense burst"}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -360,6 +410,19 @@ def main():
     torch.cuda.synchronize()
     assert ra.rc_sync(eng.err) == ra.RC_OK
 
+    # host time of the tree calls (one admission round, prompt commit and
+    # finish per step, each over the whole batch), per request
+    host_t = {"admit": 0.0, "commit_prompts": 0.0, "finish": 0.0}
+
+    def timed(name, fn):
+        def g(*a, **k):
+            t = time.perf_counter()
+            try:
+                return fn(*a, **k)
+            finally:
+                host_t[name] += time.perf_counter() - t
+        return g
+
     # ---------------------------------------------------------- timed region
     # per-kernel durations: CUDA events around every call of the prefill and
     # around every 4th decode step (recording them costs host time per call)
@@ -374,6 +437,9 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sched_calls = {n: getattr(runner.sched, n) for n in host_t}
+    for n, fn in sched_calls.items():
+        setattr(runner.sched, n, timed(n, fn))
     w0 = time.perf_counter()
     ev0.record()
     for s in range(args.warmup, n_main):
@@ -484,13 +550,21 @@ def main():
         cpu = oracle_baseline(trace_fn, shape, tr0.seed, tr0.vocab, args.cpu_seconds)
         cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
 
+    for n, fn in sched_calls.items():
+        setattr(runner.sched, n, fn)
+    paths = None
+    if rank == 0 and not args.no_paths:
+        n_req = args.steps * args.questions
+        paths = {"host_tree_us_per_request": {n: 1e6 * v / n_req for n, v in host_t.items()},
+                 "latent_decode": latent_path(dev, hbm, bf16, peak_src)}
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
                 "clocks": clk, "hit_rate": {"tokens": hit_tok, "requests": hit_req},
-                "kernels": summary, "wall_s_timed": wall,
+                "kernels": summary, "paths": paths, "wall_s_timed": wall,
                 "parallelism": "replicas" if world > 1 else "single"}
         print(json.dumps(line), flush=True)
     if world > 1:

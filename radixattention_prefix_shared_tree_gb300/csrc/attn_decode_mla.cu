@@ -15,6 +15,7 @@
 // 128w..128w+127 (P.V over the tile's 32 keys).  Output: the final bf16 row
 // when one chunk covers the request, else normalised partials for the merge.
 
+#include "attn_decode_mla_tc.cuh"
 #include "common.cuh"
 
 namespace rc_mla {
@@ -285,9 +286,24 @@ __global__ void __launch_bounds__(32) mla_merge_kernel(const Params p) {
 
 namespace rc_host {
 
+// 128 query heads: the tcgen05 kernel (attn_decode_mla_tc.cuh), all heads in
+// one CTA per (key chunk, value half, request).
+bool mla_use_tc(int32_t q_heads) { return q_heads == rc_mla_tc::M; }
+
 // Plan of the latent decode: keys per CTA and chunks per request.
 void mla_plan(int32_t batch, int32_t q_heads, int32_t max_len, int* chunk, int* n_chunks) {
     const int64_t sms = sm_count();
+    if (mla_use_tc(q_heads)) {
+        // about four CTAs per SM over the batch (rows are about half the
+        // longest on average, two value halves per chunk), 256..4096 keys
+        int64_t c = max_len > 0 ? (int64_t)batch * max_len / (4 * sms) : rc_mla_tc::TN;
+        c = (c + rc_mla_tc::TN - 1) / rc_mla_tc::TN * rc_mla_tc::TN;
+        if (c < 256) c = 256;
+        if (c > 4096) c = 4096;
+        *chunk = (int)c;
+        *n_chunks = max_len > 0 ? (int)((max_len + c - 1) / c) : 1;
+        return;
+    }
     const int64_t base = (int64_t)batch * (q_heads / rc_mla::HB);
     int64_t splits = base > 0 ? (4 * sms + base - 1) / base : 1;
     const int64_t max_splits = max_len > 0 ? (max_len + 1023) / 1024 : 1;
@@ -332,9 +348,41 @@ rc_status mla_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table*
                                           ((rows * rc_mla::DV * sizeof(float) + 255) & ~size_t(255)));
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
+    cudaError_t e;
+    if (mla_use_tc(desc->q_heads)) {
+        rc_mla_tc::Params t{};
+        t.q = p.q;
+        t.pool = p.pool;
+        t.n_slots = p.n_slots;
+        t.scale_log2 = p.scale_log2;
+        t.err = p.err;
+        t.table = p.table;
+        t.start = p.start;
+        t.len = p.len;
+        t.table_len = p.table_len;
+        t.chunk = p.chunk;
+        t.n_chunks = p.n_chunks;
+        t.part_o = p.part_o;
+        t.part_lse = p.part_lse;
+        t.out = p.out;
+        t.lse = p.lse;
+        constexpr int smem_tc = rc_mla_tc::smem_bytes();
+        dim3 grid_tc(2 * p.n_chunks, batch);
+        if (p.n_chunks == 1) {
+            e = ensure_smem<rc_mla_tc::mla_tc_kernel<true>>(smem_tc);
+            if (e != cudaSuccess) return RC_ERR_CUDA;
+            rc_mla_tc::mla_tc_kernel<true><<<grid_tc, rc_mla_tc::THREADS, smem_tc, st>>>(t);
+            return launch_status(cudaGetLastError());
+        }
+        e = ensure_smem<rc_mla_tc::mla_tc_kernel<false>>(smem_tc);
+        if (e != cudaSuccess) return RC_ERR_CUDA;
+        rc_mla_tc::mla_tc_kernel<false><<<grid_tc, rc_mla_tc::THREADS, smem_tc, st>>>(t);
+        if (cudaGetLastError() != cudaSuccess) return RC_ERR_CUDA;
+        rc_mla::mla_merge_kernel<<<(unsigned)(batch * desc->q_heads), 32, 0, st>>>(p);
+        return launch_status(cudaGetLastError());
+    }
     constexpr int smem = rc_mla::smem_bytes();
     dim3 grid(p.n_chunks, desc->q_heads / rc_mla::HB, batch);
-    cudaError_t e;
     if (p.n_chunks == 1) {
         e = ensure_smem<rc_mla::mla_decode_kernel<true>>(smem);
         if (e != cudaSuccess) return RC_ERR_CUDA;

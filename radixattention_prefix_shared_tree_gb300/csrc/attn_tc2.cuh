@@ -46,41 +46,11 @@ __host__ __device__ constexpr int smem_bytes() {
     return QT * TM * D * 2 + NS * 2 * TN * D * 2 + kBars * 8 + 16;
 }
 
-RC_DEV void mbar_arrive(uint64_t* mbar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}\n" ::"r"(rc::smem_u32(mbar))
-                 : "memory");
-}
-
-RC_DEV float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-RC_DEV float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-// (a.x*b + c, a.y*b + c) in one packed instruction
-RC_DEV float2 ffma2(float2 a, float b, float c) {
-    uint64_t r, x, y, z;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(b));
-    asm("mov.b64 %0, {%1, %1};" : "=l"(z) : "f"(c));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
-RC_DEV float2 fadd2(float2 a, float2 b) {
-    uint64_t r, x, y;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
-    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
-    float2 o;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(o.x), "=f"(o.y) : "l"(r));
-    return o;
-}
+using tc::ex2;
+using tc::fadd2;
+using tc::ffma2;
+using tc::max3;
+using tc::mbar_arrive;
 
 template <int D, int G, rc::MQMode MODE>
 __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams p) {
@@ -151,6 +121,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     // query tiles with at least one valid row
     const int n_qt = min(QT, ((min(n_rows_tok - tok0, TPC) * G) + TM - 1) / TM);
 
+    // producers: slot ids of their first tile, loaded before the set-up too
+    int sl_first[2] = {-1, -1};
+    if (warp == 8 || warp == 9) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int key = (warp - 8) * TN + lane + 32 * h2;
+            if (warp - 8 < n_tiles && key < key_count) sl_first[h2] = __ldg(keys + key);
+        }
+    }
     if (warp < 8) {
         // Q rows of query tile warp/4, issued first so that their latency
         // overlaps the set-up.  The row indices (cascade: a gather through
@@ -384,8 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                 sl[h2] = (t < n_tiles && key < key_count) ? __ldg(keys + key) : -1;
             }
         };
-        int sl[2], sl_next[2];
-        load_ids(t0, sl);
+        int sl[2] = {sl_first[0], sl_first[1]}, sl_next[2];
         for (int t = t0; t < n_tiles && ok; t += 2) {
             const int s = t % NS;
             load_ids(t + 2, sl_next);

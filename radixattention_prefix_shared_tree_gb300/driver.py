@@ -413,10 +413,14 @@ class DeviceEngine:
         # (the same thresholds as the library's plan)
         sms = self.sms
         if self.shape.mla:
-            base = B * (self.shape.q_heads // 16)
             max_len = max(dec_max) if dec_max else 0
-            splits = min(max(-(-4 * sms // max(base, 1)), 1), max(-(-max_len // 1024), 1))
-            split = splits > 1
+            if self.shape.q_heads == 128:   # tcgen05 latent kernel: chunks of 256..4096 keys
+                c = max(256, min(4096, -(-(B * max_len // (4 * sms)) // 32) * 32)) if max_len else 32
+                split = max_len > c
+            else:
+                base = B * (self.shape.q_heads // 16)
+                splits = min(max(-(-4 * sms // max(base, 1)), 1), max(-(-max_len // 1024), 1))
+                split = splits > 1
         else:
             split = B * self.shape.kv_heads < 8 * sms
         lay.decode_kernels = (1 if casc is not None else 0) + 1 + (1 if split else 0)
