@@ -65,14 +65,14 @@ struct DecParams {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 constexpr int kWarpKeys = 16;
-constexpr int kWarpStages = 3;
-constexpr int kWarpsPerCta = 4;
-
-constexpr int kSlotRing = 4;     // tiles of slot ids: written 4 ahead into the entry of the tile issued 2 iterations ago
+constexpr int kWarpStages = 2;   // one tile in flight while the warp reduces the other
+constexpr int kWarpsPerCta = 2;
+constexpr int kCtasPerSm = 7;    // 14 warps per SM: 2128 resident, the 2048 (row, KV head) items of a
+                                 // 256-row GQA-8 batch in one wave
 
 template <int D>
-__host__ __device__ constexpr int warp_smem_bytes() {  // per warp: K/V ring + Q + slot ring
-    return kWarpStages * 2 * kWarpKeys * D * 2 + 8 * D * 2 + kSlotRing * kWarpKeys * 4;
+__host__ __device__ constexpr int warp_smem_bytes() {  // per warp: the K/V ring only (Q and slot ids in registers)
+    return kWarpStages * 2 * kWarpKeys * D * 2;
 }
 template <int D>
 __host__ __device__ constexpr int dec_smem_bytes() {
@@ -80,11 +80,12 @@ __host__ __device__ constexpr int dec_smem_bytes() {
 }
 
 template <int D, int G, bool FUSED>
-__global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p, int n_items) {
+__global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_kernel(const DecParams p, int n_items) {
     constexpr int CH = D / 8;                       // 16-byte chunks per row
     constexpr int KS = D / 16;
     constexpr int PER = kWarpKeys * CH / 32;        // chunks per lane per matrix
     constexpr int TILE_BYTES = kWarpKeys * D * 2;
+    static_assert(kWarpKeys == 16, "slot ids: one lane per key");
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g_lane = lane >> 2, t_lane = lane & 3;
@@ -94,7 +95,6 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
         return;
     }
     unsigned char* wbase = smem + warp * warp_smem_bytes<D>();
-    unsigned char* sQ = wbase + kWarpStages * 2 * TILE_BYTES;
 
     const int kvh = it % p.kv_heads;
     const int rest = it / p.kv_heads;
@@ -136,31 +136,24 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
         }
     }
 
-    int32_t* sSlot = reinterpret_cast<int32_t*>(sQ + 8 * D * 2);  // [kSlotRing][kWarpKeys]
-    // Slot ids travel through the cp.async pipeline too: the group committed at
-    // iteration t holds K/V of tile t+2 and the slot ids of tile t+4, so the
-    // gather of a tile reads ids that landed two iterations earlier.
-    auto copy_slots = [&](int t) {
-        if (lane < kWarpKeys) {
-            const int key = t * kWarpKeys + lane;
-            const bool ok = t < n_tiles && key < count;
-            rc::cp_async4(rc::smem_u32(sSlot + (t % kSlotRing) * kWarpKeys + lane), ok ? keys + key : keys,
-                          ok ? 4u : 0u);
-        }
+    // Slot ids are prefetched into registers one tile ahead: lane l (and
+    // l + 16) holds the slot of key l of a tile.
+    auto slot_of = [&](int t) -> int {
+        const int key = t * kWarpKeys + (lane & 15);
+        return (t < n_tiles && key < count) ? __ldg(keys + key) : 0;
     };
     // a request's own keys are read once per step: they should not push the
     // shared prefix (read by the cascade kernel every step) out of L2
     const uint64_t pol = rc::l2_policy_evict_first();
-    auto issue = [&](int t) {
+    auto issue = [&](int t, int tslots) {
         if (t < n_tiles) {
-            unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
+            unsigned char* sK = wbase + (t & 1) * 2 * TILE_BYTES;
             unsigned char* sV = sK + TILE_BYTES;
-            const int32_t* ring = sSlot + (t % kSlotRing) * kWarpKeys;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int lin = i * 32 + lane;
                 const int r = lin / CH, c = lin % CH;
-                int slot = ring[r];
+                const int slot = __shfl_sync(0xffffffffu, tslots, r);
                 uint32_t bytes = 16;
                 const __nv_bfloat16* bk = p.pool_k;
                 const __nv_bfloat16* bv = p.pool_v;
@@ -182,34 +175,22 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
             }
         }
     };
-    // prologue: slot ids of tiles 0..3, then Q + K/V of tiles 0 and 1
-#pragma unroll
-    for (int t = 0; t < 4; ++t) copy_slots(t);
+    // prologue: slot ids of tiles 0 and 1, K/V of tile 0, and the Q operand
+    // fragments straight from global memory (head g_lane of this KV head's
+    // group, zero for g_lane >= G; two bf16 per register, as ldmatrix would
+    // give them)
+    int cur = slot_of(0), nxt = slot_of(1);
+    issue(0, cur);
     rc::cp_async_commit();
-    rc::cp_async_wait<0>();
-    __syncwarp();
-    for (int i = lane; i < 8 * CH; i += 32) {
-        const int r = i / CH, c = i % CH;
-        const __nv_bfloat16* src = p.q + ((int64_t)b * p.q_heads + kvh * G + (r < G ? r : 0)) * D + c * 8;
-        rc::cp_async16(rc::smem_u32(sQ + rc::swz<CH>(r, c)), src, r < G ? 16u : 0u);
-    }
-    issue(0);
-    rc::cp_async_commit();
-    issue(1);
-    rc::cp_async_commit();
-    rc::cp_async_wait<1>();
-    __syncwarp();
-
     uint32_t qb[KS][2];
+    {
+        const bool hv = g_lane < G;
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+            p.q + ((int64_t)b * p.q_heads + kvh * G + (hv ? g_lane : 0)) * D);
 #pragma unroll
-    for (int ks = 0; ks < KS; ks += 2) {
-        uint32_t r0, r1, r2, r3;
-        rc::ldmatrix_x4(rc::smem_u32(sQ + rc::swz<CH>(lane & 7, ks * 2 + (lane >> 3))), r0, r1, r2, r3);
-        qb[ks][0] = r0;
-        qb[ks][1] = r1;
-        if (ks + 1 < KS) {
-            qb[ks + 1][0] = r2;
-            qb[ks + 1][1] = r3;
+        for (int ks = 0; ks < KS; ++ks) {
+            qb[ks][0] = hv ? __ldg(qrow + ks * 8 + t_lane) : 0u;
+            qb[ks][1] = hv ? __ldg(qrow + ks * 8 + 4 + t_lane) : 0u;
         }
     }
     float o[KS][4];
@@ -218,14 +199,13 @@ __global__ void __launch_bounds__(128, 2) decode_split_kernel(const DecParams p,
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     for (int t = 0; t < n_tiles; ++t) {
-        if (t > 0) {
-            rc::cp_async_wait<1>();
-            __syncwarp();
-        }
-        issue(t + 2);
-        copy_slots(t + 4);
+        rc::cp_async_wait<0>();  // tile t landed; the other stage (tile t-1) is free
+        __syncwarp();
+        cur = nxt;
+        nxt = slot_of(t + 2);
+        issue(t + 1, cur);
         rc::cp_async_commit();
-        const unsigned char* sK = wbase + (t % kWarpStages) * 2 * TILE_BYTES;
+        const unsigned char* sK = wbase + (t & 1) * 2 * TILE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
         // S^T (16 keys x 8 heads) = K Q^T, even and odd k-steps in two
         // accumulators (two independent chains of MMAs)
