@@ -89,6 +89,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g_lane = lane >> 2, t_lane = lane & 3;
+    // the next step's cascade kernel (launched as this grid's dependent) may
+    // take SMs as they free up: it waits for this grid's end itself
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int it = blockIdx.x * kWarpsPerCta + warp;
     if (it >= n_items) {
         grid_dep_wait();
@@ -558,9 +561,19 @@ cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_he
     cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade>>(smem);
     if (e != cudaSuccess) return e;
     constexpr int TPC = rc_tc2::ROWS / G;
-    dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
-    rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade><<<grid, rc_tc2::THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+    // programmatic dependent of the previous kernel on the stream (the kernel
+    // waits for it before reading anything)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
+    cfg.blockDim = dim3(rc_tc2::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade>, p);
 }
 
 template <int D, int G>

@@ -74,10 +74,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int kvh = blockIdx.y, z = blockIdx.z, blk = blockIdx.x;
-    // cascade: the table pass of attn_decode is this grid's programmatic
-    // dependent; it may start as soon as every CTA here has begun (it waits
-    // for this grid's end before reading the partials)
-    if constexpr (MODE == rc::MQMode::kCascade) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // cascade: launched as the programmatic dependent of whatever precedes it
+    // on the stream (the previous step's table pass), so its CTAs take SMs as
+    // that grid drains; nothing is read before that grid has finished.  The
+    // table pass of this call is in turn this grid's dependent: it may start
+    // once every CTA here has begun (it waits for this grid's end before
+    // reading the partials).
+    if constexpr (MODE == rc::MQMode::kCascade) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
     const int tok0 = blk * TPC;
 
     // ---- this CTA's rows and keys (uniform)
