@@ -66,9 +66,9 @@ __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.w
 
 constexpr int kWarpKeys = 16;
 constexpr int kWarpStages = 2;   // one tile in flight while the warp reduces the other
-constexpr int kWarpsPerCta = 2;
-constexpr int kCtasPerSm = 7;    // 14 warps per SM: 2128 resident, the 2048 (row, KV head) items of a
-                                 // 256-row GQA-8 batch in one wave
+constexpr int kWarpsPerCta = 14;  // one CTA per SM (14 x 16 KB + the CTA's 1 KB reserve fit; seven CTAs of
+constexpr int kCtasPerSm = 1;     // two warps would not): 2128 resident warps, the 2048 (row, KV head) items
+                                  // of a 256-row GQA-8 batch in one wave
 
 template <int D>
 __host__ __device__ constexpr int warp_smem_bytes() {  // per warp: the K/V ring only (Q and slot ids in registers)
