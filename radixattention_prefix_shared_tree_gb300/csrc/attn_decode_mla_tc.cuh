@@ -7,15 +7,15 @@
 // CTA = (key chunk, value half, request).  Both value halves compute
 // S = Q K^T over the full 576-wide key; each accumulates O for its 256 of the
 // 512 value columns, which is what TMEM holds next to two S buffers.
-// Six warps with fixed roles:
+// Seven warps with fixed roles:
 //   warps 0-3  softmax: one thread per head (TMEM lane); read S, write P (bf16)
 //              back over it, rescale the head's O in TMEM when its max grows by
 //              more than 2^8;
-//   warp 4     producer: gathers 32 latent rows per tile by slot id with
-//              16-byte cp.async into a 2-stage ring (no-swizzle core-matrix
-//              layout), each lane arriving on the stage's barrier when its
-//              copies land;
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+//   warps 4, 5 producers of the even and odd tiles (stage 0 and 1): gather 32
+//              latent rows per tile by slot id with 16-byte cp.async (no-swizzle
+//              core-matrix layout), each lane arriving on the stage's barrier
+//              when its copies land;
+//   warp 6     MMA issuer (one thread) and TMEM owner.
 // Per 32-key tile: S = Q K^T (M 128, N 32, K 576 in 36 steps) into one of two
 // S buffers; O += P V (M 128, N 256, K 32) with P read from TMEM and V the
 // value half of the same shared-memory tile read as an MN-major operand.  The
@@ -34,7 +34,7 @@ constexpr int M = 128;        // query heads per CTA (all)
 constexpr int TN = 32;        // keys per tile
 constexpr int NS = 2;         // K/V stages
 constexpr int CK = DK / 8;    // 72 chunks of 16 bytes per latent row
-constexpr int THREADS = 192;
+constexpr int THREADS = 224;
 constexpr int Q_BYTES = M * DK * 2;
 constexpr int TILE_BYTES = TN * DK * 2;
 constexpr uint32_t SB = CK * 128;  // bytes between 8-row groups of Q and of a tile
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
 
     // producer: slot ids of the first tile, before the set-up
     int sl = -1;
-    if (warp == 4 && lane < count) sl = __ldg(keys + lane);
+    if ((warp == 4 || warp == 5) && (warp - 4) * TN + lane < count) sl = __ldg(keys + (warp - 4) * TN + lane);
     if (warp < 4) {
         // Q (all 128 heads): 8 consecutive lanes write 8 rows of one 16-byte
         // column, 128 contiguous bytes of the core-matrix layout
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
         tc::mbar_init(o_done, 1);
         tc::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 6) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
@@ -271,17 +271,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
                 p.part_lse[bh * p.n_chunks + chunk] = lse2;
             }
         }
-    } else if (warp == 4) {
-        // ================================================ producer
+    } else if (warp == 4 || warp == 5) {
+        // ================================================ producers (even / odd tiles)
         // lane -> (key within an 8-key group, 16-byte column within a group
         // of 4): 8 lanes write 128 contiguous bytes of the core-matrix layout
         const int klo = lane & 7, csub = lane >> 3;
-        for (int t = 0; t < n_tiles && ok; ++t) {
+        for (int t = warp - 4; t < n_tiles && ok; t += 2) {
             const int s = t % NS;
             int sl_next = -1;
             {
-                const int key = (t + 1) * TN + lane;
-                if (t + 1 < n_tiles && key < count) sl_next = __ldg(keys + key);
+                const int key = (t + 2) * TN + lane;
+                if (t + 2 < n_tiles && key < count) sl_next = __ldg(keys + key);
             }
             if (t >= NS) ok = __all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[s], ((t / NS) + 1) & 1, kWaitIter));
             if (!ok) break;
@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
         rc::cp_async_wait<0>();
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     } else if (lane == 0) {
-        // ================================================ MMA (warp 5)
+        // ================================================ MMA (warp 6)
         const uint32_t q0 = rc::smem_u32(sQ);
         auto issue_s = [&](int t) {
             const uint32_t k0s = rc::smem_u32(sKV + (t % NS) * TILE_BYTES);
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 6) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }
