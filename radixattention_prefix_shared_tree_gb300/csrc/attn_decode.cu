@@ -65,7 +65,7 @@ struct DecParams {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 constexpr int kWarpKeys = 16;
-constexpr int kWarpStages = 2;   // one tile in flight while the warp reduces the other
+constexpr int kWarpStages = 2;   // two tiles in flight while the warp waits
 constexpr int kWarpsPerCta = 14;  // one CTA per SM (14 x 16 KB + the CTA's 1 KB reserve fit; seven CTAs of
 constexpr int kCtasPerSm = 1;     // two warps would not): 2128 resident warps, the 2048 (row, KV head) items
                                   // of a 256-row GQA-8 batch in one wave
@@ -182,8 +182,12 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     // fragments straight from global memory (head g_lane of this KV head's
     // group, zero for g_lane >= G; two bf16 per register, as ldmatrix would
     // give them)
-    int cur = slot_of(0), nxt = slot_of(1);
-    issue(0, cur);
+    // Tiles t and t+1 are in flight while the warp waits for tile t; tile
+    // t+2 goes into tile t's stage as soon as tile t has been reduced.
+    int cur = slot_of(2), nxt;
+    issue(0, slot_of(0));
+    rc::cp_async_commit();
+    issue(1, slot_of(1));
     rc::cp_async_commit();
     uint32_t qb[KS][2];
     {
@@ -202,12 +206,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     for (int t = 0; t < n_tiles; ++t) {
-        rc::cp_async_wait<0>();  // tile t landed; the other stage (tile t-1) is free
+        rc::cp_async_wait<1>();  // tile t landed (tile t+1 may still be in flight)
         __syncwarp();
-        cur = nxt;
-        nxt = slot_of(t + 2);
-        issue(t + 1, cur);
-        rc::cp_async_commit();
+        nxt = slot_of(t + 3);
         const unsigned char* sK = wbase + (t & 1) * 2 * TILE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
         // S^T (16 keys x 8 heads) = K Q^T, even and odd k-steps in two
@@ -278,6 +279,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
                 rc::mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
+        __syncwarp();  // every lane has read tile t: its stage takes tile t+2
+        issue(t + 2, cur);
+        rc::cp_async_commit();
+        cur = nxt;
     }
     rc::cp_async_wait<0>();
     __syncwarp();
