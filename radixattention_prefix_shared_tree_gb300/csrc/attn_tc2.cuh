@@ -10,11 +10,12 @@
 //                      TMEM lane; read S from TMEM, write P (bf16) back over
 //                      it, rescale the row's O in TMEM when its max grows by
 //                      more than 2^8;
-//   warps 8, 9         producers of the even and odd tiles: gather K/V rows
-//                      by slot id with 16-byte cp.async into a 5-stage ring
-//                      (no-swizzle operand layout), each lane's copies
-//                      arriving on the stage's mbarrier when they land;
-//   warp 10            issues every MMA (one thread) and owns TMEM.
+//   warps 8..8+NP-1    producers, warp 8+i of the tiles t = i mod NP: gather
+//                      K/V rows by slot id with 16-byte cp.async into a
+//                      5-stage ring (no-swizzle operand layout), each lane's
+//                      copies arriving on the stage's mbarrier when they
+//                      land;
+//   warp 8+NP          issues every MMA (one thread) and owns TMEM.
 // Per 64-key tile and query tile q:  S_q = Q_q K^T (M=128, N=64, K=D) into
 // one of two S buffers, O_q += P_q V (M=128, N=D, K=64) with P read from
 // tensor memory.  The next tile's S products are issued before this tile's
@@ -37,7 +38,9 @@ constexpr int TM = 128;        // rows per query tile
 constexpr int ROWS = QT * TM;  // query rows per CTA
 constexpr int TN = 64;         // keys per tile
 constexpr int NS = 5;          // K/V stages
-constexpr int THREADS = 352;
+constexpr int NP = 2;          // producer warps (a third one measured no faster)
+constexpr int MMA_WARP = 8 + NP;
+constexpr int THREADS = 32 * (MMA_WARP + 1);
 constexpr uint32_t kWaitIter = 1u << 24;
 constexpr int kBars = 1 + 2 * NS + 4 + 4 + 2;
 
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
 
     // producers: slot ids of their first tile, loaded before the set-up too
     int sl_first[2] = {-1, -1};
-    if (warp == 8 || warp == 9) {
+    if (warp >= 8 && warp < MMA_WARP) {
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
             const int key = (warp - 8) * TN + lane + 32 * h2;
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         }
         tc::fence_mbar_init();
     }
-    if (warp == 10) {
+    if (warp == MMA_WARP) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
@@ -350,12 +353,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                 }
             }
         }
-    } else if (warp == 8 || warp == 9) {
-        // ============================================== producers (2 warps)
-        // warp 8 loads the even tiles, warp 9 the odd ones, each as far ahead
-        // as free stages allow (completion is signalled on the stage's
-        // barrier by the copies themselves), reading the slot ids of its next
-        // tile one tile ahead.
+    } else if (warp < MMA_WARP) {
+        // ============================================== producers (NP warps)
+        // warp 8+i loads the tiles t = i mod NP, each as far ahead as free
+        // stages allow (completion is signalled on the stage's barrier by the
+        // copies themselves), reading the slot ids of its next tile one tile
+        // ahead.
         // lane -> (key within an 8-key group, 16-byte column within a group of 4)
         const int klo = lane & 7, csub = lane >> 3;
         // keys here are shared: by the CTAs of the other row blocks, and (a
@@ -370,9 +373,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             }
         };
         int sl[2] = {sl_first[0], sl_first[1]}, sl_next[2];
-        for (int t = t0; t < n_tiles && ok; t += 2) {
+        for (int t = t0; t < n_tiles && ok; t += NP) {
             const int s = t % NS;
-            load_ids(t + 2, sl_next);
+            load_ids(t + NP, sl_next);
             if (t >= NS) ok = __all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[s], ((t / NS) + 1) & 1, kWaitIter));
             if (!ok) break;
             unsigned char* sK = sKV + s * 2 * KV_BYTES;
@@ -407,7 +410,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         rc::cp_async_wait<0>();  // nothing in flight when the warp leaves
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     } else if (lane == 0) {
-        // ==================================================== MMA (warp 10)
+        // ================================================= MMA (warp 8+NP)
         auto issue_s = [&](int t) {
             const uint32_t k0 = rc::smem_u32(sKV + (t % NS) * 2 * KV_BYTES);
             for (int q = 0; q < n_qt; ++q) {
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 10) {
+    if (warp == MMA_WARP) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }
