@@ -214,6 +214,66 @@ rc_status rc_stats(rc_cache* cache, rc_stats_t* out);
  * Writes at most cap-1 bytes plus a NUL; *needed = full length (no NUL). */
 rc_status rc_dump(rc_cache* cache, char* buf, int64_t cap, int64_t* needed);
 
+/* Keys of an image for the tree [SG, multimodal results: the input image's
+ * hash is the key in the radix tree, so its tokens' KV is reused]: a run of
+ * n_tokens keys, all in [-2^30, -1] (never a text token id, which is >= 0),
+ * a function of the image's bytes alone.  Definition: h = FNV-1a 64 of
+ * data[0..bytes); out[i] = -1 - (splitmix64 finaliser of
+ * h + (i+1)*0x9E3779B97F4A7C15) >> 34.  Put the run where the image sits in the
+ * prompt; equal images give equal runs, so a later prompt with the same image
+ * matches through it.  data may be NULL when bytes == 0.
+ * Errors: RC_ERR_ARG (negative sizes, null pointers with non-zero sizes). */
+rc_status rc_image_key(const void* data, int64_t bytes, int32_t n_tokens, int32_t* out);
+
+/* ---------------------------------------------------------- block comparator
+ * A prefix cache over fixed-size token blocks, the scheme [N49 s.3] sets
+ * against the radix tree (vLLM: a hash chain of 16-token blocks, whole-block
+ * matches, reference counts, least recently used first).  Same pool rules,
+ * call shapes, clock and pins as the rc_* calls, so both run one trace and
+ * differ only in match granularity.  Readings: only a full block is cached,
+ * keyed exactly by (the block before it, its tokens); a lookup walks whole
+ * blocks from the start; insert caches the full blocks not cached yet and
+ * leaves the partial last block with the caller, who frees it (bc_free) when
+ * the request is done; every match and insert advance the clock by one and
+ * stamp the touched chain (root included); a pin counts on every block of
+ * the chain; eviction takes unpinned blocks (never the root) by last access,
+ * ties to the block farther from the chain's start, whole blocks, until the
+ * freed count reaches the request.  Node handles (rc_node) are block ids:
+ * 0 is the root (the empty chain), ids count block creations. */
+typedef struct bc_cache bc_cache;
+
+/* block_tokens in [1, 4096] (16 for the comparison of [N49 s.3]).
+ * Errors: RC_ERR_ARG, RC_ERR_NOMEM. */
+rc_status bc_create(int64_t pool_slots, int32_t block_tokens, bc_cache** out);
+void bc_destroy(bc_cache* cache);
+/* As rc_match_prefix; *matched is a multiple of block_tokens, *out_node the
+ * last matched block (0 when none). */
+rc_status bc_match_prefix(bc_cache* cache, const int32_t* tok, int64_t n, int pin,
+                          int64_t* matched, int32_t* out_slots, rc_node* out_node);
+/* As rc_insert for the floor(n / block_tokens) full blocks of tok[0..n); the
+ * slots of the partial last block stay held by the caller.  *already_present:
+ * tokens in blocks that were cached before the call.  out_slots: room for n
+ * (cached slots, then the caller's for new blocks and the partial tail).
+ * Errors: RC_ERR_ARG, RC_ERR_STATE (nothing changed), RC_ERR_NOMEM. */
+rc_status bc_insert(bc_cache* cache, const int32_t* tok, const int32_t* slots, int64_t n,
+                    int pin, int64_t* already_present, rc_node* out_node, int32_t* out_slots);
+/* Drop one pin from every block of the chain ending at node.
+ * Errors: RC_ERR_STATE (unknown or evicted block, or not pinned). */
+rc_status bc_release(bc_cache* cache, rc_node node);
+/* Evict unpinned blocks until at least n_tokens slots are freed or none is
+ * left; log: NULL or room for log_cap block ids in eviction order;
+ * *n_evicted counts blocks (even beyond log_cap).  Errors: RC_ERR_ARG. */
+rc_status bc_evict(bc_cache* cache, int64_t n_tokens, int64_t* freed,
+                   int64_t* log, int64_t log_cap, int64_t* n_evicted);
+/* As rc_alloc / rc_free. */
+rc_status bc_alloc(bc_cache* cache, int64_t n, int32_t* out);
+rc_status bc_free(bc_cache* cache, const int32_t* slots, int64_t n);
+/* As sched_order, with the block-granular look-ahead match. */
+rc_status bc_sched_order(bc_cache* cache, int policy, const int32_t* const* prompts,
+                         const int64_t* lens, int32_t n, int32_t* out_order);
+/* As rc_stats: nodes counts live blocks (root included), evicted_nodes blocks. */
+rc_status bc_stats(bc_cache* cache, rc_stats_t* out);
+
 /* ---------------------------------------------------------------- device */
 
 /* KV pool in HBM (caller-owned).  GQA: k and v are [n_slots][kv_heads][head_dim]

@@ -93,6 +93,17 @@ SIGNATURES = {
     "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
     "rc_sync": (I32, [VP, VP]),
     "rc_strerror": (C.c_char_p, [I32]),
+    "rc_image_key": (I32, [VP, I64, I32, VP]),
+    "bc_create": (I32, [I64, I32, P(VP)]),
+    "bc_destroy": (None, [VP]),
+    "bc_match_prefix": (I32, [VP, VP, I64, C.c_int, P(I64), VP, P(I64)]),
+    "bc_insert": (I32, [VP, VP, VP, I64, C.c_int, P(I64), P(I64), VP]),
+    "bc_release": (I32, [VP, I64]),
+    "bc_evict": (I32, [VP, I64, P(I64), VP, I64, P(I64)]),
+    "bc_alloc": (I32, [VP, I64, VP]),
+    "bc_free": (I32, [VP, VP, I64]),
+    "bc_sched_order": (I32, [VP, C.c_int, VP, VP, I32, VP]),
+    "bc_stats": (I32, [VP, P(rc_stats_t)]),
 }
 
 _lib = None
@@ -154,61 +165,70 @@ def rc_destroy(handle):
     lib().rc_destroy(handle)
 
 
-def rc_match_prefix(handle, tokens, pin: bool):
+def rc_match_prefix(handle, tokens, pin: bool, _fn: str = "rc_match_prefix"):
     t = _i32(tokens)
     out = np.empty(max(len(t), 1), np.int32)
     m, node = I64(0), I64(-1)
-    st = lib().rc_match_prefix(handle, _np_ptr(t), len(t), int(pin), C.byref(m), out.ctypes.data_as(VP),
-                               C.byref(node))
+    st = getattr(lib(), _fn)(handle, _np_ptr(t), len(t), int(pin), C.byref(m), out.ctypes.data_as(VP),
+                             C.byref(node))
     return st, m.value, out[:m.value].copy(), node.value
 
 
-def rc_insert(handle, tokens, slots, pin: bool):
+def rc_insert(handle, tokens, slots, pin: bool, _fn: str = "rc_insert"):
     t, s = _i32(tokens), _i32(slots)
     if len(t) != len(s):
         raise ValueError("tokens and slots differ in length")
     out = np.empty(max(len(t), 1), np.int32)
     present, node = I64(0), I64(-1)
-    st = lib().rc_insert(handle, _np_ptr(t), _np_ptr(s), len(t), int(pin), C.byref(present), C.byref(node),
-                         out.ctypes.data_as(VP))
+    st = getattr(lib(), _fn)(handle, _np_ptr(t), _np_ptr(s), len(t), int(pin), C.byref(present), C.byref(node),
+                             out.ctypes.data_as(VP))
     return st, present.value, node.value, out[:len(t)].copy()
 
 
-def rc_release(handle, node: int):
-    return lib().rc_release(handle, int(node))
+def rc_release(handle, node: int, _fn: str = "rc_release"):
+    return getattr(lib(), _fn)(handle, int(node))
 
 
-def rc_evict(handle, n_tokens: int, log_cap: int = 4096):
+def rc_evict(handle, n_tokens: int, log_cap: int = 4096, _fn: str = "rc_evict"):
     log = np.empty(max(log_cap, 1), np.int64)
     freed, cnt = I64(0), I64(0)
-    st = lib().rc_evict(handle, int(n_tokens), C.byref(freed), log.ctypes.data_as(VP), log_cap, C.byref(cnt))
+    st = getattr(lib(), _fn)(handle, int(n_tokens), C.byref(freed), log.ctypes.data_as(VP), log_cap, C.byref(cnt))
     return st, freed.value, log[:min(cnt.value, log_cap)].copy()
 
 
-def rc_alloc(handle, n: int):
+def rc_alloc(handle, n: int, _fn: str = "rc_alloc"):
     out = np.empty(max(n, 1), np.int32)
-    st = lib().rc_alloc(handle, int(n), out.ctypes.data_as(VP))
+    st = getattr(lib(), _fn)(handle, int(n), out.ctypes.data_as(VP))
     return st, (out[:n].copy() if st == RC_OK else np.empty(0, np.int32))
 
 
-def rc_free(handle, slots):
+def rc_free(handle, slots, _fn: str = "rc_free"):
     s = _i32(slots)
-    return lib().rc_free(handle, _np_ptr(s), len(s))
+    return getattr(lib(), _fn)(handle, _np_ptr(s), len(s))
 
 
-def sched_order(handle, policy: int, prompts):
+def sched_order(handle, policy: int, prompts, _fn: str = "sched_order"):
     arrs = [_i32(p) for p in prompts]
     ptrs = (VP * max(len(arrs), 1))(*[a.ctypes.data if a.size else None for a in arrs])
     lens = np.asarray([len(a) for a in arrs], np.int64)
     out = np.empty(max(len(arrs), 1), np.int32)
-    st = lib().sched_order(handle, int(policy), ptrs, _np_ptr(lens), len(arrs), out.ctypes.data_as(VP))
+    st = getattr(lib(), _fn)(handle, int(policy), ptrs, _np_ptr(lens), len(arrs), out.ctypes.data_as(VP))
     return st, out[:len(arrs)].copy()
 
 
-def rc_stats(handle) -> dict:
+def rc_stats(handle, _fn: str = "rc_stats") -> dict:
     s = rc_stats_t()
-    _check("rc_stats", lib().rc_stats(handle, C.byref(s)))
+    _check(_fn, getattr(lib(), _fn)(handle, C.byref(s)))
     return {n: int(getattr(s, n)) for n, _ in rc_stats_t._fields_}
+
+
+def rc_image_key(data, n_tokens: int):
+    """Key run of an image (bytes-like or numpy array) for the tree."""
+    buf = np.frombuffer(bytes(data), np.uint8) if not isinstance(data, np.ndarray) else \
+        np.ascontiguousarray(data).view(np.uint8).reshape(-1)
+    out = np.empty(max(int(n_tokens), 1), np.int32)
+    _check("rc_image_key", lib().rc_image_key(_np_ptr(buf), buf.size, int(n_tokens), out.ctypes.data_as(VP)))
+    return out[:int(n_tokens)].copy()
 
 
 def rc_dump(handle) -> str:
@@ -322,6 +342,54 @@ class RadixCache:
 
     def stats(self) -> dict:
         return {_STAT_RENAME.get(k, k): v for k, v in rc_stats(self._h).items()}
+
+
+class BlockCache:
+    """The block-granular comparator (bc_* calls) with RadixCache's method
+    shapes; ``uncached_tail(n)`` is how many of n inserted tokens stay with the
+    caller (the partial last block)."""
+
+    def __init__(self, pool_slots: int, block_tokens: int = 16):
+        h = VP()
+        _check("bc_create", lib().bc_create(int(pool_slots), int(block_tokens), C.byref(h)))
+        self._h = h
+        self.block_tokens = int(block_tokens)
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h and _lib is not None:
+            _lib.bc_destroy(h)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def match(self, tokens, pin: bool):
+        return rc_match_prefix(self._h, tokens, pin, _fn="bc_match_prefix")
+
+    def insert(self, tokens, slots, pin: bool):
+        return rc_insert(self._h, tokens, slots, pin, _fn="bc_insert")
+
+    def release(self, node: int):
+        return rc_release(self._h, node, _fn="bc_release")
+
+    def evict(self, n_tokens: int, log_cap: int = 4096):
+        return rc_evict(self._h, n_tokens, log_cap, _fn="bc_evict")
+
+    def alloc(self, n: int):
+        return rc_alloc(self._h, n, _fn="bc_alloc")
+
+    def free(self, slots):
+        return rc_free(self._h, slots, _fn="bc_free")
+
+    def sched_order(self, policy: int, prompts):
+        return sched_order(self._h, policy, prompts, _fn="bc_sched_order")
+
+    def uncached_tail(self, n: int) -> int:
+        return int(n) % self.block_tokens
+
+    def stats(self) -> dict:
+        return {_STAT_RENAME.get(k, k): v for k, v in rc_stats(self._h, _fn="bc_stats").items()}
 
 
 # ---------------------------------------------------------------- device calls

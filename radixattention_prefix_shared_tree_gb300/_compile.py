@@ -18,7 +18,7 @@ LIB = os.path.join(BUILD, "libradixattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 CU_SOURCES = ["kv_store.cu", "attn_decode.cu", "attn_decode_mla.cu", "attn_extend.cu", "runtime.cu"]
-CPP_SOURCES = ["radix_cache.cpp"]
+CPP_SOURCES = ["radix_cache.cpp", "block_cache.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -12,10 +12,11 @@
 //  * one hash map keyed by (parent index, first token) holds every edge;
 //  * evictable leaves (no children, no pins, not the root) sit in an ordered
 //    set keyed by (last access, id), so the next victim is its first element;
-//  * free slots are a two-level bitmap, so "the n smallest free ids" is a
-//    scan of set bits from the lowest non-empty word.
+//  * free slots are a two-level bitmap (slot_pool.h), so "the n smallest free
+//    ids" is a scan of set bits from the lowest non-empty word.
 
 #include "../../include/radixattn.h"
+#include "slot_pool.h"
 
 #include <algorithm>
 #include <cstdio>
@@ -29,7 +30,9 @@
 
 namespace {
 
-enum : uint8_t { FREE = 0, HELD = 1, CACHED = 2 };
+using rc_pool::CACHED;
+using rc_pool::FREE;
+using rc_pool::HELD;
 
 struct Rec {
     int64_t id = -1;
@@ -62,13 +65,7 @@ inline uint64_t edge_key(int32_t parent, int32_t first_tok) {
 
 }  // namespace
 
-struct rc_cache {
-    int64_t pool = 0;
-    std::vector<uint8_t> owner;      // per slot: FREE, HELD (by a caller), CACHED (in the tree)
-    std::vector<uint64_t> bits;      // 1 = free
-    std::vector<uint64_t> summary;   // 1 = bits[w] != 0
-    int64_t n_free = 0, n_held = 0, n_cached = 0;
-
+struct rc_cache : rc_pool::SlotPool {
     std::vector<Rec> recs;
     std::vector<int32_t> spare;      // recycled node indices
     std::vector<int32_t> tok_arena, slot_arena;
@@ -80,50 +77,12 @@ struct rc_cache {
     int64_t next_id = 0;
     int64_t n_nodes = 0;
 
-    std::vector<uint32_t> mark;      // per slot epoch marks for duplicate checks
-    uint32_t epoch = 0;
     std::vector<int32_t> path;       // scratch
     std::vector<int32_t> scratch_slots;
 
     int64_t match_calls = 0, match_tokens = 0, match_hits = 0, match_hit_tokens = 0;
     int64_t insert_calls = 0, insert_new_tokens = 0, insert_dup_freed = 0;
     int64_t evicted_nodes = 0, evicted_tokens = 0;
-
-    // ------------------------------------------------------------- slots
-    void slot_set_free(int32_t s) {
-        size_t w = (size_t)s >> 6;
-        bits[w] |= 1ull << (s & 63);
-        summary[w >> 6] |= 1ull << (w & 63);
-    }
-    int64_t next_word(int64_t w) const {  // first word index >= w with free bits, or -1
-        int64_t nw = (int64_t)bits.size();
-        if (w >= nw) return -1;
-        size_t sw = (size_t)w >> 6;
-        uint64_t m = summary[sw] & (~0ull << (w & 63));
-        while (!m) {
-            if (++sw >= summary.size()) return -1;
-            m = summary[sw];
-        }
-        return (int64_t)(sw << 6) + __builtin_ctzll(m);
-    }
-    void take_lowest(int64_t n, int32_t* out) {
-        int64_t got = 0, w = next_word(0);
-        while (got < n) {
-            uint64_t b = bits[(size_t)w];
-            while (b && got < n) {
-                int t = __builtin_ctzll(b);
-                b &= b - 1;
-                int32_t s = (int32_t)(w * 64 + t);
-                out[got++] = s;
-                owner[(size_t)s] = HELD;
-            }
-            bits[(size_t)w] = b;
-            if (!b) summary[(size_t)w >> 6] &= ~(1ull << (w & 63));
-            if (got < n) w = next_word(w + 1);
-        }
-        n_free -= n;
-        n_held += n;
-    }
 
     // ------------------------------------------------------------- nodes
     int32_t new_rec(int32_t parent, int64_t off, int32_t len) {
@@ -255,16 +214,7 @@ rc_status rc_create(int64_t pool_slots, rc_cache** out) {
     rc_cache* c = new (std::nothrow) rc_cache();
     if (!c) return RC_ERR_NOMEM;
     try {
-        c->pool = pool_slots;
-        c->owner.assign((size_t)pool_slots, FREE);
-        c->mark.assign((size_t)pool_slots, 0);
-        size_t nw = (size_t)((pool_slots + 63) / 64);
-        c->bits.assign(nw, ~0ull);
-        if (pool_slots & 63) c->bits[nw - 1] = (1ull << (pool_slots & 63)) - 1;
-        c->summary.assign((nw + 63) / 64 + 1, 0);
-        for (size_t w = 0; w < nw; ++w)
-            if (c->bits[w]) c->summary[w >> 6] |= 1ull << (w & 63);
-        c->n_free = pool_slots;
+        c->init_slots(pool_slots);
         c->new_rec(-1, 0, 0);  // root: index 0, id 0
     } catch (...) {
         delete c;
@@ -309,7 +259,7 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     std::vector<int32_t>& have = c->scratch_slots;
     have.clear();
     int64_t m = c->descend(tok, n, false, nullptr, &have);
-    if (++c->epoch == 0) { std::fill(c->mark.begin(), c->mark.end(), 0); c->epoch = 1; }
+    c->new_epoch();
     // positions whose slot is already the cached one need no check
     const int64_t same = common_prefix(slots, have.data(), m);
     for (int64_t i = same; i < n; ++i) {
@@ -419,21 +369,8 @@ rc_status rc_alloc(rc_cache* c, int64_t n, int32_t* out) {
 
 rc_status rc_free(rc_cache* c, const int32_t* slots, int64_t n) {
     if (!c || n < 0 || (n > 0 && !slots)) return RC_ERR_ARG;
-    for (int64_t i = 0; i < n; ++i)
-        if (slots[i] < 0 || slots[i] >= c->pool) return RC_ERR_ARG;
-    if (++c->epoch == 0) { std::fill(c->mark.begin(), c->mark.end(), 0); c->epoch = 1; }
-    for (int64_t i = 0; i < n; ++i) {
-        int32_t s = slots[i];
-        if (c->owner[(size_t)s] != HELD || c->mark[(size_t)s] == c->epoch) return RC_ERR_STATE;
-        c->mark[(size_t)s] = c->epoch;
-    }
-    for (int64_t i = 0; i < n; ++i) {
-        c->owner[(size_t)slots[i]] = FREE;
-        c->slot_set_free(slots[i]);
-    }
-    c->n_free += n;
-    c->n_held -= n;
-    return RC_OK;
+    const int r = c->free_held(slots, n);
+    return r == -1 ? RC_ERR_ARG : r == -2 ? RC_ERR_STATE : RC_OK;
 }
 
 rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, const int64_t* lens,
@@ -646,3 +583,33 @@ rc_status rc_dump(rc_cache* c, char* buf, int64_t cap, int64_t* needed) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ image keys
+// The unite.ai article on SGLang, multimodal results: for RadixAttention the
+// hash of an input image is computed and used as the key in the tree, so the
+// KV of the image's tokens is reused whenever the same image comes again.
+// Here an image becomes a run of n_tokens keys (the model's image-token
+// count), all derived from a hash of its bytes and all negative, so they
+// never equal a text token id (>= 0).  Byte hash: FNV-1a 64 (Fowler, Noll,
+// Vo); key i: the top 30 bits of the splitmix64 finaliser (Steele, Lea,
+// Flood 2014) of hash + (i+1) * 0x9E3779B97F4A7C15, as -1 - bits.
+namespace {
+inline uint64_t image_mix(uint64_t z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+}  // namespace
+
+extern "C" rc_status rc_image_key(const void* data, int64_t bytes, int32_t n_tokens, int32_t* out) {
+    if (bytes < 0 || n_tokens < 0 || (bytes > 0 && !data) || (n_tokens > 0 && !out)) return RC_ERR_ARG;
+    const unsigned char* p = static_cast<const unsigned char*>(data);
+    uint64_t h = 0xCBF29CE484222325ull;
+    for (int64_t i = 0; i < bytes; ++i) {
+        h ^= p[i];
+        h *= 0x100000001B3ull;
+    }
+    for (int32_t i = 0; i < n_tokens; ++i)
+        out[i] = -1 - (int32_t)(image_mix(h + (uint64_t)(i + 1) * 0x9E3779B97F4A7C15ull) >> 34);
+    return RC_OK;
+}

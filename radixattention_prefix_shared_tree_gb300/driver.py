@@ -198,6 +198,17 @@ class Scheduler:
             r.slots[:L] = canon
             _ok(self.cache.release(r.node), "release")
             r.node = node if r.max_new > 0 else -1
+            if r.max_new == 0:
+                self._free_tail(r, L)
+
+    def _free_tail(self, r, n: int):
+        """A done request's tokens that the cache did not take (the partial
+        last block of a block-granular cache) go back to the pool."""
+        tail = getattr(self.cache, "uncached_tail", None)
+        k = tail(n) if tail is not None else 0
+        if k:
+            _ok(self.cache.free(r.slots[n - k:n]), "free")
+            self._rec("free_tail", r.rid, k)
 
     def finish(self, batch: list):
         """After decode: insert prompt + generated tokens, unpin."""
@@ -213,6 +224,7 @@ class Scheduler:
             r.slots[:n] = canon
             _ok(self.cache.release(r.node), "release")
             r.node = -1
+            self._free_tail(r, n)
 
 
 # ------------------------------------------------------------------ cascade

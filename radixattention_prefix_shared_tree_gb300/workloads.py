@@ -200,3 +200,18 @@ def run_mla(runner: Runner, trace, n_requests: int | None = None):
     admitted, waiting = runner.serve(reqs)
     assert not waiting
     return admitted
+
+
+def run_multimodal(runner: Runner, trace, key_fn, batch: int = 64):
+    """Questions about images in arrival order, served in rounds of up to
+    `batch` (the scheduler orders each round); an image's key run comes from
+    key_fn(bytes, n_tokens)."""
+    reqs = [runner.request(trace.prompt(i, key_fn), trace.max_new) for i in range(len(trace.questions))]
+    served = []
+    pending = reqs
+    while pending:
+        admitted, pending = runner.serve(pending, batch)
+        if not admitted:
+            raise RuntimeError("no progress: pool too small for any waiting request")
+        served.extend(admitted)
+    return served

@@ -218,3 +218,45 @@ def mla_long(batch: int = 128, shared_len: int = 4096, private_max: int = 28672,
         tr.private.append(_tokens(rng, n, tr.vocab, first=firsts[i] if n else None))
     tr.pool_slots = shared_len + sum(len(p) for p in tr.private) + batch * steps
     return tr
+
+
+# ------------------------------------------------------- multimodal (images)
+@dataclass
+class MultimodalTrace:
+    """Questions about images, several per image, arriving interleaved.
+    Images are raw bytes; a prompt is system + the image's key run + question,
+    where the caller turns an image into keys with its own function (the
+    product's rc_image_key, or the oracle's), so neither side's inputs come
+    from the other."""
+    shape: Shape = GQA_32_8
+    vocab: int = 32000
+    seed: int = SEED0 + 5
+    max_new: int = 32
+    image_tokens: int = 576
+    pool_slots: int = 0
+    system: np.ndarray = field(default_factory=lambda: np.zeros(0, np.int32))
+    images: list = field(default_factory=list)      # bytes
+    questions: list = field(default_factory=list)   # (image index, tokens), arrival order
+
+    def prompt(self, i: int, key_fn) -> np.ndarray:
+        img, q = self.questions[i]
+        keys = np.asarray(key_fn(self.images[img], self.image_tokens), np.int32)
+        return np.concatenate([self.system, keys, q]).astype(np.int32)
+
+
+def multimodal(n_images: int = 24, per_image: int = 8, system_len: int = 50, qmin: int = 16, qmax: int = 48,
+               image_bytes: int = 4096, image_tokens: int = 576, max_new: int = 32) -> MultimodalTrace:
+    rng = _rng(5)
+    tr = MultimodalTrace(max_new=max_new, image_tokens=image_tokens)
+    tr.system = _tokens(rng, system_len, tr.vocab)
+    tr.images = [rng.integers(0, 256, image_bytes, dtype=np.int64).astype(np.uint8).tobytes()
+                 for _ in range(n_images)]
+    qs = []
+    for img in range(n_images):
+        for _ in range(per_image):
+            qs.append((img, _tokens(rng, int(rng.integers(qmin, qmax + 1)), tr.vocab)))
+    order = rng.permutation(len(qs))
+    tr.questions = [qs[int(i)] for i in order]
+    per_req = system_len + image_tokens + qmax + max_new
+    tr.pool_slots = int(per_req * len(qs))
+    return tr

@@ -69,9 +69,11 @@ def lpm_dynamic_order(cache, prompts):
     return total
 
 
-def random_trace(cache, rng, n_ops, vocab=4, max_len=12, log=None):
+def random_trace(cache, rng, n_ops, vocab=4, max_len=12, log=None, bases=None):
     """Random mix of every host call over a tiny vocabulary (forces splits,
-    duplicates, evictions, pinning errors).  Logs every result."""
+    duplicates, evictions, pinning errors).  Logs every result.  With `bases`
+    (token arrays), most requests are a prefix of one of them, possibly with
+    one token changed, so that long shared prefixes occur."""
     pinned = []      # node handles we hold pins on
     held = []        # slots we own
     for _ in range(n_ops):
@@ -79,6 +81,12 @@ def random_trace(cache, rng, n_ops, vocab=4, max_len=12, log=None):
         if op in (0, 1):  # request: match+pin, alloc, insert (pin or not), maybe release
             n = int(rng.integers(1, max_len + 1))
             tok = rng.integers(0, vocab, n).astype(np.int32)
+            if bases is not None and rng.random() < 0.8:
+                base = bases[int(rng.integers(0, len(bases)))]
+                n = min(n, len(base))
+                tok = base[:n].copy()
+                if rng.random() < 0.3:
+                    tok[int(rng.integers(0, n))] = int(rng.integers(0, vocab))
             st, m, ms, node = cache.match(tok, True)
             log.append(("match", st, m, tuple(int(x) for x in ms), node))
             st, new = cache.alloc(n - m)
@@ -100,6 +108,9 @@ def random_trace(cache, rng, n_ops, vocab=4, max_len=12, log=None):
             log.append(("insert", st, present, node2, tuple(int(x) for x in canon)))
             if st != OK:
                 held.extend(mine)
+            elif hasattr(cache, "uncached_tail"):  # a block cache leaves the partial block with us
+                k = cache.uncached_tail(n)
+                held.extend(int(x) for x in canon[n - k:])
             log.append(("rel", cache.release(node)))
             if pin and st == OK:
                 pinned.append(node2)

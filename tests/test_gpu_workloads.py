@@ -175,3 +175,25 @@ def test_mla_reduced_vs_oracle(cuda):
     check_requests(runner, model, [r.rid for r in reqs[::3]], tr.shape, stats)
     assert stats["sum"] / stats["n"] <= MEAN_ABS
     assert cache.stats()["match_hit_tokens"] >= 12 * 512
+
+
+@pytest.mark.parametrize("cache_kind", ["radix", "block16"])
+def test_multimodal_image_keys_vs_oracle(cuda, cache_kind):
+    """Questions about images whose key runs share the tree (or 16-token
+    blocks): prefill and decode of sampled requests against the oracle, and the
+    host results identical to the oracle cache running the same trace."""
+    from oracle import block_oracle as bo
+    tr = traces.multimodal(n_images=5, per_image=4, image_tokens=96, max_new=4)
+    make = ra.RadixCache if cache_kind == "radix" else (lambda n: ra.BlockCache(n, 16))
+    runner, model, cache, log, reqs = run(tr, lambda r, t: wl.run_multimodal(r, t, ra.rc_image_key, batch=4),
+                                          tr.pool_slots, cuda, cache_cls=make)
+    stats = {}
+    check_requests(runner, model, [r.rid for r in reqs[::3]], tr.shape, stats)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS
+    # later questions about an image reuse its run
+    assert cache.stats()["match_hit_tokens"] > len(reqs) * len(tr.system)
+    omake = oracle.OracleTree if cache_kind == "radix" else (lambda n: bo.OracleBlockCache(n, 16))
+    olog = []
+    orunner = wl.Runner(omake(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=olog)
+    wl.run_multimodal(orunner, tr, bo.image_key, batch=4)
+    assert olog == log
