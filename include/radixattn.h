@@ -279,7 +279,13 @@ rc_status bc_stats(bc_cache* cache, rc_stats_t* out);
 /* KV pool in HBM (caller-owned).  GQA: k and v are [n_slots][kv_heads][head_dim]
  * bf16, row-major, 16-byte aligned.  Latent (mla != 0): kv_heads == 1, k is
  * [n_slots][head_dim_k] and its first head_dim_v columns are V; v is NULL.
- * err: device int32 that kernels OR RC error bits into (may be NULL). */
+ * err: device int32 that kernels OR RC error bits into (may be NULL).
+ * FP8 pool (kv_fp8 != 0; GQA, head_dim 128) [DS s.1: KV cache FP8 quantisation;
+ * block-wise FP8: E4M3 with one dynamic scale per token per 128-channel
+ * group]: k and v hold E4M3 codes, one byte per element in the same
+ * [n_slots][kv_heads][head_dim] layout, and k_scale / v_scale are fp32
+ * [n_slots][kv_heads]; an element's value is its code times the scale of its
+ * (slot, head) row.  kv_store quantises (see there); attn_decode reads it. */
 typedef struct rc_pool_desc {
     void* k;
     void* v;
@@ -289,6 +295,9 @@ typedef struct rc_pool_desc {
     int32_t head_dim_v;
     int32_t mla;
     int32_t* err;
+    int32_t kv_fp8;
+    float* k_scale;
+    float* v_scale;
 } rc_pool_desc;
 
 typedef struct rc_attn_desc {
@@ -316,8 +325,13 @@ typedef struct rc_kv_table {
  * slots[i].  If table and table_pos are both non-NULL, also
  * table[table_pos[i]] = slots[i] (appends to the slot tables).
  * A slot outside [0, n_slots) is skipped and flags RC_ERR_DEVICE in pool->err.
- * Errors (host): RC_ERR_ARG, RC_ERR_UNSUPPORTED (row bytes not a multiple of 16),
- * RC_ERR_CUDA (launch). */
+ * FP8 pool: each (token, head) row x of head_dim bf16 values is stored as
+ * scale = amax|x| / 448 (fp32, rounded to nearest) and codes
+ * e4m3(x_i / scale) (fp32 quotient rounded to nearest, then to the nearest
+ * E4M3 value, ties to even, saturating at +-448); an all-zero row stores scale
+ * 0 and zero codes.
+ * Errors (host): RC_ERR_ARG, RC_ERR_UNSUPPORTED (row bytes not a multiple of 16;
+ * an FP8 pool that is latent or whose head_dim is not 128), RC_ERR_CUDA (launch). */
 rc_status kv_store(const rc_pool_desc* pool, const int32_t* slots, const void* k_new,
                    const void* v_new, int32_t n, int32_t* table, const int32_t* table_pos,
                    rc_stream_t stream);

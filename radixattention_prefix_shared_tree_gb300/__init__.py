@@ -34,7 +34,8 @@ P = C.POINTER
 
 class rc_pool_desc(C.Structure):
     _fields_ = [("k", VP), ("v", VP), ("n_slots", I64), ("kv_heads", I32), ("head_dim_k", I32),
-                ("head_dim_v", I32), ("mla", I32), ("err", VP)]
+                ("head_dim_v", I32), ("mla", I32), ("err", VP), ("kv_fp8", I32), ("k_scale", VP),
+                ("v_scale", VP)]
 
 
 class rc_attn_desc(C.Structure):
@@ -404,8 +405,10 @@ def _stream(stream):
     return C.c_void_p(s.cuda_stream)
 
 
-def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = None) -> rc_pool_desc:
-    """Descriptor of a pool held in torch tensors: k [n_slots, Hkv, dk] (or [n_slots, dk] latent)."""
+def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = None, k_scale=None,
+                   v_scale=None) -> rc_pool_desc:
+    """Descriptor of a pool held in torch tensors: k [n_slots, Hkv, dk] (or [n_slots, dk] latent).
+    With k_scale / v_scale (fp32 [n_slots, Hkv]) the pool is FP8: k, v hold E4M3 codes (uint8)."""
     d = rc_pool_desc()
     d.k = k.data_ptr()
     d.v = v.data_ptr() if v is not None else None
@@ -418,7 +421,10 @@ def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = N
         d.head_dim_v = v.shape[2]
     d.mla = int(mla)
     d.err = err.data_ptr() if err is not None else None
-    d._keep = (k, v, err)   # the descriptor holds raw pointers: keep the tensors alive with it
+    if k_scale is not None:
+        d.kv_fp8 = 1
+        d.k_scale, d.v_scale = k_scale.data_ptr(), v_scale.data_ptr()
+    d._keep = (k, v, err, k_scale, v_scale)   # raw pointers inside: keep the tensors alive with it
     return d
 
 

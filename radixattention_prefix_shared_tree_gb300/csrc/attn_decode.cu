@@ -53,6 +53,9 @@ struct DecParams {
     // attn_decode_append: each row's last key comes from here and is stored
     const __nv_bfloat16* k_new;  // [B][kv_heads][D] or NULL
     const __nv_bfloat16* v_new;
+    // FP8 pool: pool_k / pool_v hold E4M3 codes, these the per-row scales
+    const float* k_scale;  // [n_slots][kv_heads]
+    const float* v_scale;
 };
 
 // Decode with one warp per item (request b, KV head, key chunk).  Each warp
@@ -65,27 +68,41 @@ struct DecParams {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 
 constexpr int kWarpKeys = 16;
-constexpr int kWarpStages = 2;   // two tiles in flight while the warp waits
 constexpr int kWarpsPerCta = 14;  // one CTA per SM (14 x 16 KB + the CTA's 1 KB reserve fit; seven CTAs of
 constexpr int kCtasPerSm = 1;     // two warps would not): 2128 resident warps, the 2048 (row, KV head) items
                                   // of a 256-row GQA-8 batch in one wave
 
-template <int D>
-__host__ __device__ constexpr int warp_smem_bytes() {  // per warp: the K/V ring only (Q and slot ids in registers)
-    return kWarpStages * 2 * kWarpKeys * D * 2;
+// Per-warp ring: S stages of one 16-key tile each (K then V, then for an FP8
+// pool the tile's 16 K scales and 16 V scales); a stage is refilled as soon
+// as its tile is reduced, so S tiles are in flight while the warp waits.
+template <bool FP8>
+__host__ __device__ constexpr int warp_stages() { return FP8 ? 3 : 2; }
+template <int D, bool FP8>
+__host__ __device__ constexpr int tile_bytes() { return kWarpKeys * D * (FP8 ? 1 : 2); }
+template <int D, bool FP8>
+__host__ __device__ constexpr int stage_bytes() { return 2 * tile_bytes<D, FP8>() + (FP8 ? 2 * kWarpKeys * 4 : 0); }
+template <int D, bool FP8>
+__host__ __device__ constexpr int warp_smem_bytes() {  // the K/V ring only (Q and slot ids in registers)
+    return warp_stages<FP8>() * stage_bytes<D, FP8>();
 }
-template <int D>
+template <int D, bool FP8>
 __host__ __device__ constexpr int dec_smem_bytes() {
-    return kWarpsPerCta * warp_smem_bytes<D>();
+    return kWarpsPerCta * warp_smem_bytes<D, FP8>();
 }
 
-template <int D, int G, bool FUSED>
+template <int D, int G, bool FUSED, bool FP8>
 __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_kernel(const DecParams p, int n_items) {
-    constexpr int CH = D / 8;                       // 16-byte chunks per row
+    constexpr int ESZ = FP8 ? 1 : 2;                // bytes per K/V element
+    constexpr int CH = D * ESZ / 16;                // 16-byte chunks per row
     constexpr int KS = D / 16;
     constexpr int PER = kWarpKeys * CH / 32;        // chunks per lane per matrix
-    constexpr int TILE_BYTES = kWarpKeys * D * 2;
+    constexpr int S = warp_stages<FP8>();
+    constexpr int TILE_BYTES = tile_bytes<D, FP8>();
+    constexpr int STAGE_BYTES = stage_bytes<D, FP8>();
     static_assert(kWarpKeys == 16, "slot ids: one lane per key");
+    static_assert(!FP8 || D == 128, "FP8 pools: head_dim 128");
+    // the epilogue reuses the ring: [8][D] fp32 outputs plus the merge scratch
+    static_assert(warp_smem_bytes<D, FP8>() >= 8 * D * 4 + 32 + 32 * 8 + G * 32 * 4 + G * 8, "epilogue scratch");
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g_lane = lane >> 2, t_lane = lane & 3;
@@ -97,7 +114,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
         grid_dep_wait();
         return;
     }
-    unsigned char* wbase = smem + warp * warp_smem_bytes<D>();
+    unsigned char* wbase = smem + warp * warp_smem_bytes<D, FP8>();
 
     const int kvh = it % p.kv_heads;
     const int rest = it / p.kv_heads;
@@ -121,7 +138,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     // attn_decode_append: the row's last key (position L-1) is the step's new
     // token.  The warp whose keys hold it gathers it from k_new/v_new and
     // writes it to its pool slot (lanes 0..CH-1 the K row, CH..2CH-1 the V row).
-    const int new_at = (p.k_new && L > 0 && L - 1 >= k0 && L - 1 < k0 + count) ? L - 1 - k0 : -1;
+    const int new_at = (!FP8 && p.k_new && L > 0 && L - 1 >= k0 && L - 1 < k0 + count) ? L - 1 - k0 : -1;
     if (new_at >= 0) {
         const int slot = keys[new_at];
         if (slot < 0 || (int64_t)slot >= p.n_slots) {
@@ -150,7 +167,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     const uint64_t pol = rc::l2_policy_evict_first();
     auto issue = [&](int t, int tslots) {
         if (t < n_tiles) {
-            unsigned char* sK = wbase + (t & 1) * 2 * TILE_BYTES;
+            unsigned char* sK = wbase + (t % S) * STAGE_BYTES;
             unsigned char* sV = sK + TILE_BYTES;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
@@ -158,13 +175,13 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
                 const int r = lin / CH, c = lin % CH;
                 const int slot = __shfl_sync(0xffffffffu, tslots, r);
                 uint32_t bytes = 16;
-                const __nv_bfloat16* bk = p.pool_k;
-                const __nv_bfloat16* bv = p.pool_v;
+                const unsigned char* bk = reinterpret_cast<const unsigned char*>(p.pool_k);
+                const unsigned char* bv = reinterpret_cast<const unsigned char*>(p.pool_v);
                 int64_t row = 0;
                 if (t * kWarpKeys + r >= count) bytes = 0;
                 else if (t * kWarpKeys + r == new_at) {  // the appended key, straight from its source
-                    bk = p.k_new;
-                    bv = p.v_new;
+                    bk = reinterpret_cast<const unsigned char*>(p.k_new);
+                    bv = reinterpret_cast<const unsigned char*>(p.v_new);
                     row = b;
                 } else if (slot < 0 || (int64_t)slot >= p.n_slots) {
                     rc::flag_error(p.err, rc::kErrBadSlot);
@@ -172,9 +189,15 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
                 } else {
                     row = slot;
                 }
-                const int64_t roff = (row * p.kv_heads + kvh) * D + c * 8;
+                const int64_t roff = (row * p.kv_heads + kvh) * (D * ESZ) + c * 16;
                 rc::cp_async16(rc::smem_u32(sK + rc::swz<CH>(r, c)), bk + roff, bytes, pol);
                 rc::cp_async16(rc::smem_u32(sV + rc::swz<CH>(r, c)), bv + roff, bytes, pol);
+            }
+            if constexpr (FP8) {  // lanes 0-15: K scale of key lane, 16-31: V scale of key lane-16
+                const int r = lane & 15;
+                const bool ok = t * kWarpKeys + r < count && tslots >= 0 && (int64_t)tslots < p.n_slots;
+                const float* src = (lane < 16 ? p.k_scale : p.v_scale) + (ok ? (int64_t)tslots * p.kv_heads + kvh : 0);
+                rc::cp_async4(rc::smem_u32(sV + TILE_BYTES + lane * 4), src, ok ? 4u : 0u);
             }
         }
     };
@@ -182,13 +205,14 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     // fragments straight from global memory (head g_lane of this KV head's
     // group, zero for g_lane >= G; two bf16 per register, as ldmatrix would
     // give them)
-    // Tiles t and t+1 are in flight while the warp waits for tile t; tile
-    // t+2 goes into tile t's stage as soon as tile t has been reduced.
-    int cur = slot_of(2), nxt;
-    issue(0, slot_of(0));
-    rc::cp_async_commit();
-    issue(1, slot_of(1));
-    rc::cp_async_commit();
+    // Tiles t..t+S-1 are in flight while the warp waits for tile t; tile
+    // t+S goes into tile t's stage as soon as tile t has been reduced.
+    int cur = slot_of(S), nxt;
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+        issue(i, slot_of(i));
+        rc::cp_async_commit();
+    }
     uint32_t qb[KS][2];
     {
         const bool hv = g_lane < G;
@@ -196,8 +220,15 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
             p.q + ((int64_t)b * p.q_heads + kvh * G + (hv ? g_lane : 0)) * D);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            qb[ks][0] = hv ? __ldg(qrow + ks * 8 + t_lane) : 0u;
-            qb[ks][1] = hv ? __ldg(qrow + ks * 8 + 4 + t_lane) : 0u;
+            if constexpr (FP8) {
+                // f16 operands, and k-step ks takes dims 16ks+4t..16ks+4t+3 of
+                // this lane's K words (see below): the same dims of Q
+                qb[ks][0] = hv ? rc::bf16x2_to_f16x2(__ldg(qrow + ks * 8 + 2 * t_lane)) : 0u;
+                qb[ks][1] = hv ? rc::bf16x2_to_f16x2(__ldg(qrow + ks * 8 + 2 * t_lane + 1)) : 0u;
+            } else {
+                qb[ks][0] = hv ? __ldg(qrow + ks * 8 + t_lane) : 0u;
+                qb[ks][1] = hv ? __ldg(qrow + ks * 8 + 4 + t_lane) : 0u;
+            }
         }
     }
     float o[KS][4];
@@ -206,25 +237,48 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
     for (int t = 0; t < n_tiles; ++t) {
-        rc::cp_async_wait<1>();  // tile t landed (tile t+1 may still be in flight)
+        rc::cp_async_wait<S - 1>();  // tile t landed (later tiles may still be in flight)
         __syncwarp();
-        nxt = slot_of(t + 3);
-        const unsigned char* sK = wbase + (t & 1) * 2 * TILE_BYTES;
+        nxt = slot_of(t + S + 1);
+        const unsigned char* sK = wbase + (t % S) * STAGE_BYTES;
         const unsigned char* sV = sK + TILE_BYTES;
+        const float* sSc = reinterpret_cast<const float*>(sV + TILE_BYTES);  // FP8: K scales, then V scales
         // S^T (16 keys x 8 heads) = K Q^T, even and odd k-steps in two
         // accumulators (two independent chains of MMAs)
         float s[4] = {0.f, 0.f, 0.f, 0.f};
         {
             float s2[4] = {0.f, 0.f, 0.f, 0.f};
-            const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+            if constexpr (FP8) {
+                // A fragment from E4M3 words: row g (and g+8), 16-byte chunk ks,
+                // word t_lane = dims 16ks+4t..+3; the k-step's columns 2t, 2t+1
+                // take the word's first two dims, 2t+8, 2t+9 the last two
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                uint32_t a0, a1, a2, a3;
-                rc::ldmatrix_x4(rc::smem_u32(sK + rc::swz<CH>(key, ks * 2 + (lane >> 4))), a0, a1, a2, a3);
-                rc::mma_bf16_16816(ks & 1 ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                for (int ks = 0; ks < KS; ++ks) {
+                    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sK + rc::swz<CH>(g_lane, ks) + 4 * t_lane);
+                    const uint32_t w1 =
+                        *reinterpret_cast<const uint32_t*>(sK + rc::swz<CH>(g_lane + 8, ks) + 4 * t_lane);
+                    rc::mma_f16_16816(ks & 1 ? s2 : s, rc::e4m3x2_to_f16x2(w0), rc::e4m3x2_to_f16x2(w1),
+                                      rc::e4m3x2_to_f16x2(w0 >> 16), rc::e4m3x2_to_f16x2(w1 >> 16), qb[ks][0],
+                                      qb[ks][1]);
+                }
+            } else {
+                const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t a0, a1, a2, a3;
+                    rc::ldmatrix_x4(rc::smem_u32(sK + rc::swz<CH>(key, ks * 2 + (lane >> 4))), a0, a1, a2, a3);
+                    rc::mma_bf16_16816(ks & 1 ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+                }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[i] += s2[i];
+            if constexpr (FP8) {  // code products times the keys' scales
+                const float k_lo = sSc[g_lane], k_hi = sSc[g_lane + 8];
+                s[0] *= k_lo;
+                s[1] *= k_lo;
+                s[2] *= k_hi;
+                s[3] *= k_hi;
+            }
         }
         const int key_lo = t * kWarpKeys + g_lane;
         const bool v_lo = key_lo < count, v_hi = key_lo + 8 < count;
@@ -267,9 +321,32 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
         }
         l_run[0] += p0 + p2;
         l_run[1] += p1 + p3;
-        const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));
-        const uint32_t pb1 = rc::movmatrix_trans(rc::pack_bf16(p2, p3));
-        {
+        if constexpr (FP8) {
+            // P times the values' scales (f16), then O^T += V^T P^T with V^T
+            // built from E4M3 bytes: this lane reads 16-byte chunk g of keys
+            // 2t, 2t+1, 2t+8, 2t+9 (dims 16g..16g+15); product mt uses dims
+            // 16g+2mt (row g) and 16g+2mt+1 (row g+8), paired across keys
+            // with a byte permute
+            const float v_lo = sSc[kWarpKeys + g_lane], v_hi = sSc[kWarpKeys + g_lane + 8];
+            const uint32_t pb0 = rc::movmatrix_trans(rc::pack_f16(p0 * v_lo, p1 * v_lo));
+            const uint32_t pb1 = rc::movmatrix_trans(rc::pack_f16(p2 * v_hi, p3 * v_hi));
+            const uint4 w0 = *reinterpret_cast<const uint4*>(sV + rc::swz<CH>(2 * t_lane, g_lane));
+            const uint4 w1 = *reinterpret_cast<const uint4*>(sV + rc::swz<CH>(2 * t_lane + 1, g_lane));
+            const uint4 w8 = *reinterpret_cast<const uint4*>(sV + rc::swz<CH>(2 * t_lane + 8, g_lane));
+            const uint4 w9 = *reinterpret_cast<const uint4*>(sV + rc::swz<CH>(2 * t_lane + 9, g_lane));
+            const uint32_t x0[4] = {w0.x, w0.y, w0.z, w0.w}, x1[4] = {w1.x, w1.y, w1.z, w1.w};
+            const uint32_t x8[4] = {w8.x, w8.y, w8.z, w8.w}, x9[4] = {w9.x, w9.y, w9.z, w9.w};
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t lo = rc::prmt(x0[mt >> 1], x1[mt >> 1], sel);
+                const uint32_t hi = rc::prmt(x8[mt >> 1], x9[mt >> 1], sel);
+                rc::mma_f16_16816(o[mt], rc::e4m3x2_to_f16x2(lo), rc::e4m3x2_to_f16x2(lo >> 16),
+                                  rc::e4m3x2_to_f16x2(hi), rc::e4m3x2_to_f16x2(hi >> 16), pb0, pb1);
+            }
+        } else {
+            const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));
+            const uint32_t pb1 = rc::movmatrix_trans(rc::pack_bf16(p2, p3));
             const int key = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
@@ -279,8 +356,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
                 rc::mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
             }
         }
-        __syncwarp();  // every lane has read tile t: its stage takes tile t+2
-        issue(t + 2, cur);
+        __syncwarp();  // every lane has read tile t: its stage takes tile t+S
+        issue(t + S, cur);
         rc::cp_async_commit();
         cur = nxt;
     }
@@ -301,11 +378,13 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     const float inv1 = l_run[1] > 0.f ? 1.f / l_run[1] : 0.f;
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
-        const int d0 = mt * 16 + g_lane;
+        // accumulator rows g and g+8 of product mt: dims d0 and d1
+        const int d0 = FP8 ? 16 * g_lane + 2 * mt : mt * 16 + g_lane;
+        const int d1 = FP8 ? d0 + 1 : d0 + 8;
         sE[(2 * t_lane) * D + d0] = o[mt][0] * inv0;
         sE[(2 * t_lane + 1) * D + d0] = o[mt][1] * inv1;
-        sE[(2 * t_lane) * D + d0 + 8] = o[mt][2] * inv0;
-        sE[(2 * t_lane + 1) * D + d0 + 8] = o[mt][3] * inv1;
+        sE[(2 * t_lane) * D + d1] = o[mt][2] * inv0;
+        sE[(2 * t_lane + 1) * D + d1] = o[mt][3] * inv1;
     }
     if (g_lane == 0) {
         sOwn[2 * t_lane] = l_run[0] > 0.f ? m_run[0] + log2f(l_run[0]) : -INFINITY;
@@ -536,15 +615,15 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
 // after_cascade: launched as the programmatic dependent of the cascade kernel
 // just queued on the stream, so that its CTAs start on SMs the cascade leaves
 // free and as cascade CTAs finish, instead of after the whole cascade grid.
-template <int D, int G, bool FUSED>
+template <int D, int G, bool FUSED, bool FP8>
 cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream_t st, bool after_cascade) {
-    constexpr int smem = dec_smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G, FUSED>>(smem);
+    constexpr int smem = dec_smem_bytes<D, FP8>();
+    cudaError_t e = rc_host::ensure_smem<decode_split_kernel<D, G, FUSED, FP8>>(smem);
     if (e != cudaSuccess) return e;
     const int n_items = batch * kv_heads * p.n_chunks;
     const int grid = (n_items + kWarpsPerCta - 1) / kWarpsPerCta;
     if (!after_cascade) {
-        decode_split_kernel<D, G, FUSED><<<grid, 32 * kWarpsPerCta, smem, st>>>(p, n_items);
+        decode_split_kernel<D, G, FUSED, FP8><<<grid, 32 * kWarpsPerCta, smem, st>>>(p, n_items);
         return cudaGetLastError();
     }
     cudaLaunchConfig_t cfg = {};
@@ -557,7 +636,7 @@ cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, FUSED>, p, n_items);
+    return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, FUSED, FP8>, p, n_items);
 }
 
 template <int D, int G>
@@ -582,25 +661,30 @@ cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_he
 }
 
 template <int D, int G>
-cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused, int batch,
-                    int kv_heads, cudaStream_t st) {
+cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused, bool fp8,
+                    int batch, int kv_heads, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     const bool with_cascade = casc && casc->n_seg > 0 && casc->max_seg_rows > 0;
     if (with_cascade) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
     if (e != cudaSuccess) return e;
-    return fused ? launch_split<D, G, true>(dp, batch, kv_heads, st, with_cascade)
-                 : launch_split<D, G, false>(dp, batch, kv_heads, st, with_cascade);
+    if constexpr (D == 128) {
+        if (fp8)
+            return fused ? launch_split<D, G, true, true>(dp, batch, kv_heads, st, with_cascade)
+                         : launch_split<D, G, false, true>(dp, batch, kv_heads, st, with_cascade);
+    }
+    return fused ? launch_split<D, G, true, false>(dp, batch, kv_heads, st, with_cascade)
+                 : launch_split<D, G, false, false>(dp, batch, kv_heads, st, with_cascade);
 }
 
 template <int D>
 cudaError_t dispatch_group(int G, const DecParams& dp, const rc::MQParams& mp, const rc_cascade* casc, bool fused,
-                           int batch, int kv_heads, cudaStream_t st, bool* ok) {
+                           bool fp8, int batch, int kv_heads, cudaStream_t st, bool* ok) {
     *ok = true;
     switch (G) {
-        case 1: return run_gqa<D, 1>(dp, mp, casc, fused, batch, kv_heads, st);
-        case 2: return run_gqa<D, 2>(dp, mp, casc, fused, batch, kv_heads, st);
-        case 4: return run_gqa<D, 4>(dp, mp, casc, fused, batch, kv_heads, st);
-        case 8: return run_gqa<D, 8>(dp, mp, casc, fused, batch, kv_heads, st);
+        case 1: return run_gqa<D, 1>(dp, mp, casc, fused, fp8, batch, kv_heads, st);
+        case 2: return run_gqa<D, 2>(dp, mp, casc, fused, fp8, batch, kv_heads, st);
+        case 4: return run_gqa<D, 4>(dp, mp, casc, fused, fp8, batch, kv_heads, st);
+        case 8: return run_gqa<D, 8>(dp, mp, casc, fused, fp8, batch, kv_heads, st);
         default: *ok = false; return cudaSuccess;
     }
 }
@@ -633,7 +717,7 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
     const bool use_casc = casc && casc->n_seg > 0;
     if (desc->pool.mla) {  // one latent KV head: its own kernel (attn_decode_mla.cu)
-        if (k_new) return RC_ERR_UNSUPPORTED;
+        if (k_new || desc->pool.kv_fp8) return RC_ERR_UNSUPPORTED;
         if (use_casc) return RC_ERR_UNSUPPORTED;
         if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return RC_ERR_ARG;
         return rc_host::mla_decode(desc, q, kv, batch, out, lse, ws, ws_bytes, (cudaStream_t)stream);
@@ -649,6 +733,12 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     const rc_pool_desc& P = desc->pool;
     const int D = P.head_dim_k;
     if (P.mla || P.head_dim_v != D || !P.v) return RC_ERR_UNSUPPORTED;
+    const bool fp8 = P.kv_fp8 != 0;
+    if (fp8) {  // E4M3 pool: the table pass and the cascade read codes and scales
+        if (D != 128 || k_new) return RC_ERR_UNSUPPORTED;
+        if (!P.k_scale || !P.v_scale) return RC_ERR_ARG;
+        if (use_casc && !rc_tc2::fp8_cascade_supported()) return RC_ERR_UNSUPPORTED;
+    }
     const int G = desc->q_heads / P.kv_heads;
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* seg_o = reinterpret_cast<float*>(w + pl.tail_o + pl.tail_lse);
@@ -679,6 +769,8 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     dp.lse = lse;
     dp.k_new = static_cast<const __nv_bfloat16*>(k_new);
     dp.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    dp.k_scale = fp8 ? P.k_scale : nullptr;
+    dp.v_scale = fp8 ? P.v_scale : nullptr;
     rc::MQParams mp{};
     mp.q = dp.q;
     mp.pool_k = dp.pool_k;
@@ -702,8 +794,8 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     bool ok = false;
     cudaError_t e = cudaSuccess;
     const rc_cascade* cc = use_casc ? casc : nullptr;
-    if (D == 128) e = dispatch_group<128>(G, dp, mp, cc, pl.fused, batch, P.kv_heads, st, &ok);
-    else if (D == 64) e = dispatch_group<64>(G, dp, mp, cc, pl.fused, batch, P.kv_heads, st, &ok);
+    if (D == 128) e = dispatch_group<128>(G, dp, mp, cc, pl.fused, fp8, batch, P.kv_heads, st, &ok);
+    else if (D == 64) e = dispatch_group<64>(G, dp, mp, cc, pl.fused, false, batch, P.kv_heads, st, &ok);
     if (!ok) return RC_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return RC_ERR_CUDA;
     if (pl.fused) return RC_OK;

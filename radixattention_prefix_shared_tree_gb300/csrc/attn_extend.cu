@@ -60,7 +60,7 @@ extern "C" rc_status attn_extend(const rc_attn_desc* desc, const void* q, const 
     if (!q || !qo_indptr || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
     const rc_pool_desc& P = desc->pool;
     if (P.kv_heads <= 0 || desc->q_heads <= 0 || desc->q_heads % P.kv_heads) return RC_ERR_ARG;
-    if (P.mla || !P.v || P.head_dim_v != P.head_dim_k) return RC_ERR_UNSUPPORTED;
+    if (P.mla || !P.v || P.head_dim_v != P.head_dim_k || P.kv_fp8) return RC_ERR_UNSUPPORTED;
     rc::MQParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.pool_k = static_cast<const __nv_bfloat16*>(P.k);

@@ -49,6 +49,10 @@ __host__ __device__ constexpr int smem_bytes() {
     return QT * TM * D * 2 + NS * 2 * TN * D * 2 + kBars * 8 + 16;
 }
 
+// Whether the cascade path reads FP8 pools (not yet: the caller is told
+// RC_ERR_UNSUPPORTED instead).
+inline constexpr bool fp8_cascade_supported() { return false; }
+
 using tc::ex2;
 using tc::fadd2;
 using tc::ffma2;

@@ -421,3 +421,111 @@ def test_decode_latent_vs_oracle(cuda, lens):
     offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
     ref, ref_lse = oracle.attention(bits(q), ks, None, offs, np.asarray(lens), Hq, 1, 576, 512, scale, latent=True)
     check(bits(out), ref, lse.cpu().numpy(), ref_lse)
+
+
+# ------------------------------------------------------------------ FP8 pool
+class Fp8Pool:
+    """An E4M3 pool filled through kv_store (which quantises) from random bf16 rows."""
+
+    def __init__(self, n_slots, Hkv, dev, seed, magnitudes=True):
+        g = torch.Generator().manual_seed(seed)
+        D = 128
+        k = rand_bf16(g, (n_slots, Hkv, D), dev)
+        v = rand_bf16(g, (n_slots, Hkv, D), dev)
+        if magnitudes:  # rows of very different size, a few all-zero and tiny ones
+            k = (k.float() * torch.exp(2 * torch.randn(n_slots, Hkv, 1, generator=g)).to(dev)).to(torch.bfloat16)
+            # (values near unit size keep the outputs O(1), where the mean bound means something)
+            v = (v.float() * torch.exp(0.5 * torch.randn(n_slots, Hkv, 1, generator=g)).to(dev)).to(torch.bfloat16)
+            k[::97] = 0
+            v[5::89] = 0
+            k[3::101] *= 1e-30
+        self.kb, self.vb = bits(k), bits(v)
+        self.k8 = torch.zeros(n_slots, Hkv, D, dtype=torch.uint8, device=dev)
+        self.v8 = torch.zeros(n_slots, Hkv, D, dtype=torch.uint8, device=dev)
+        self.ks = torch.full((n_slots, Hkv), -1.0, dtype=torch.float32, device=dev)
+        self.vs = torch.full((n_slots, Hkv), -1.0, dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.desc = ra.make_pool_desc(self.k8, self.v8, self.err, k_scale=self.ks, v_scale=self.vs)
+        slots = torch.randperm(n_slots, generator=g).to(torch.int32).to(dev)
+        ra.kv_store(self.desc, slots, k[slots.long()].contiguous(), v[slots.long()].contiguous())
+        assert ra.rc_sync(self.err) == ra.RC_OK
+
+
+def test_kv_store_fp8_quantisation_bit_exact(cuda):
+    from oracle import fp8_oracle as f8
+    pool = Fp8Pool(3000, 8, cuda, 11)
+    for codes, scales, src in ((pool.k8, pool.ks, pool.kb), (pool.v8, pool.vs, pool.vb)):
+        c_ref, s_ref = f8.quantize_rows(src)
+        got_c = codes.cpu().numpy()
+        got_s = scales.cpu().numpy()
+        assert np.array_equal(got_s.view(np.uint32), s_ref.view(np.uint32))
+        # codes equal; the sign of a zero is not compared
+        strip = lambda c: np.where((c & 0x7F) == 0, 0, c)
+        assert np.array_equal(strip(got_c), strip(c_ref))
+    assert (pool.ks.cpu().numpy() == 0).sum() >= 3000 * 8 // 97 - 8
+
+
+FP8_DECODE_CASES = [
+    # Hq, Hkv, lens, rows of very different magnitude
+    (32, 8, [1, 17, 64, 200, 1000, 2500, 4097], False),
+    (64, 8, [5, 129, 3000], False),
+    (8, 8, [1, 1024, 33], False),
+    (32, 8, [48 + (i * 37) % 150 for i in range(160)], False),   # one wave, fused epilogue
+    (32, 8, [1, 17, 64, 200, 1000, 2500, 4097], True),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens,magnitudes", FP8_DECODE_CASES)
+def test_decode_fp8_flat_vs_oracle(cuda, Hq, Hkv, lens, magnitudes):
+    """Against the oracle on the dequantised pool.  Unit-scale rows take the
+    usual bar; rows spread over e^(+-8) in size (peaked softmax, outputs up to
+    several units) take the same elementwise bound and a mean bound scaled by
+    the outputs' size (the bf16 rounding of an output grows with it)."""
+    from oracle import fp8_oracle as f8
+    n_slots = 24000
+    pool = Fp8Pool(n_slots, Hkv, cuda, Hq + len(lens), magnitudes=magnitudes)
+    rows, table, start, length = _tables(lens, n_slots, 3, cuda)
+    g = torch.Generator().manual_seed(2)
+    B = len(lens)
+    D = 128
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    ws = torch.empty(ra.attn_decode_workspace(desc, B, max(lens)), dtype=torch.uint8, device=cuda)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_decode(desc, q, kv, B, out, lse, ws)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    kd = f8.dequantize(pool.k8.cpu().numpy(), pool.ks.cpu().numpy())
+    vd = f8.dequantize(pool.v8.cpu().numpy(), pool.vs.cpu().numpy())
+    sel = np.concatenate(rows)
+    offs = np.zeros(B, np.int64)
+    offs[1:] = np.cumsum(lens)[:-1]
+    ref, ref_lse = f8.attention(bits(q), kd[sel], vd[sel], offs, np.asarray(lens), Hq, Hkv, scale)
+    if not magnitudes:
+        check(bits(out), ref, lse.cpu().numpy(), ref_lse)
+        return
+    got = hg.bf16_bits_to_f32(bits(out)).astype(np.float64)
+    err = np.abs(got - ref)
+    assert (err <= np.maximum(MAX_ABS, bf16_ulp(ref))).all()
+    assert err.mean() <= MEAN_ABS * np.maximum(1.0, np.abs(ref)).mean()
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= LSE_ABS * max(1.0, np.abs(ref_lse).max() / 100)
+
+
+def test_fp8_pool_rejected_where_unsupported(cuda):
+    pool = Fp8Pool(512, 8, cuda, 1, magnitudes=False)
+    desc = ra.make_attn_desc(pool.desc, 32, 0.1)
+    lens = [10, 20]
+    rows, table, start, length = _tables(lens, 512, 3, cuda)
+    kv = ra.make_kv_table(table, start, length, 20)
+    q = torch.zeros(2, 32, 128, dtype=torch.bfloat16, device=cuda)
+    out = torch.empty_like(q)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=cuda)
+    qo = torch.tensor([0, 1, 2], dtype=torch.int32, device=cuda)
+    with pytest.raises(ra.RCError) as e:
+        ra.attn_extend(desc, q, qo, kv, 2, 1, out, None)
+    assert e.value.status == ra.RC_ERR_UNSUPPORTED
+    with pytest.raises(ra.RCError) as e:
+        ra.attn_decode_append(desc, q, q[:, :8], q[:, :8], kv, 2, out, None, ws)
+    assert e.value.status == ra.RC_ERR_UNSUPPORTED
