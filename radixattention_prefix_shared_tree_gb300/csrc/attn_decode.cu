@@ -639,10 +639,10 @@ cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream
     return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, FUSED, FP8>, p, n_items);
 }
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_heads, cudaStream_t st) {
-    constexpr int smem = rc_tc2::smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade>>(smem);
+    constexpr int smem = rc_tc2::smem_bytes<D, FP8>();
+    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade, FP8>>(smem);
     if (e != cudaSuccess) return e;
     constexpr int TPC = rc_tc2::ROWS / G;
     // programmatic dependent of the previous kernel on the stream (the kernel
@@ -657,7 +657,7 @@ cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_he
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade>, p);
+    return cudaLaunchKernelEx(&cfg, rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade, FP8>, p);
 }
 
 template <int D, int G>
@@ -665,13 +665,16 @@ cudaError_t run_gqa(const DecParams& dp, const rc::MQParams& mp, const rc_cascad
                     int batch, int kv_heads, cudaStream_t st) {
     cudaError_t e = cudaSuccess;
     const bool with_cascade = casc && casc->n_seg > 0 && casc->max_seg_rows > 0;
-    if (with_cascade) e = launch_cascade<D, G>(mp, casc, kv_heads, st);
-    if (e != cudaSuccess) return e;
     if constexpr (D == 128) {
-        if (fp8)
+        if (fp8) {
+            if (with_cascade) e = launch_cascade<D, G, true>(mp, casc, kv_heads, st);
+            if (e != cudaSuccess) return e;
             return fused ? launch_split<D, G, true, true>(dp, batch, kv_heads, st, with_cascade)
                          : launch_split<D, G, false, true>(dp, batch, kv_heads, st, with_cascade);
+        }
     }
+    if (with_cascade) e = launch_cascade<D, G, false>(mp, casc, kv_heads, st);
+    if (e != cudaSuccess) return e;
     return fused ? launch_split<D, G, true, false>(dp, batch, kv_heads, st, with_cascade)
                  : launch_split<D, G, false, false>(dp, batch, kv_heads, st, with_cascade);
 }
@@ -780,6 +783,8 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     mp.q_heads = dp.q_heads;
     mp.scale_log2 = dp.scale_log2;
     mp.err = dp.err;
+    mp.k_scale = dp.k_scale;
+    mp.v_scale = dp.v_scale;
     if (use_casc) {
         mp.seg_slots = casc->seg_slots;
         mp.seg_indptr = casc->seg_indptr;

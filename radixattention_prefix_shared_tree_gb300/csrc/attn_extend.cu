@@ -17,26 +17,34 @@
 
 namespace {
 
-template <int D, int G>
+template <int D, int G, bool FP8>
 cudaError_t launch_extend(const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st) {
-    constexpr int smem = rc_tc2::smem_bytes<D>();
-    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend>>(smem);
+    constexpr int smem = rc_tc2::smem_bytes<D, FP8>();
+    cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend, FP8>>(smem);
     if (e != cudaSuccess) return e;
     constexpr int TPC = rc_tc2::ROWS / G;
     dim3 grid((max_q + TPC - 1) / TPC, kv_heads, batch);
-    rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend><<<grid, rc_tc2::THREADS, smem, st>>>(p);
+    rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kExtend, FP8><<<grid, rc_tc2::THREADS, smem, st>>>(p);
     return cudaGetLastError();
 }
 
+template <int D, int G>
+cudaError_t launch_extend_any(const rc::MQParams& p, bool fp8, int batch, int max_q, int kv_heads, cudaStream_t st) {
+    if constexpr (D == 128) {
+        if (fp8) return launch_extend<D, G, true>(p, batch, max_q, kv_heads, st);
+    }
+    return launch_extend<D, G, false>(p, batch, max_q, kv_heads, st);
+}
+
 template <int D>
-cudaError_t dispatch(int G, const rc::MQParams& p, int batch, int max_q, int kv_heads, cudaStream_t st,
+cudaError_t dispatch(int G, const rc::MQParams& p, bool fp8, int batch, int max_q, int kv_heads, cudaStream_t st,
                      bool* ok) {
     *ok = true;
     switch (G) {
-        case 1: return launch_extend<D, 1>(p, batch, max_q, kv_heads, st);
-        case 2: return launch_extend<D, 2>(p, batch, max_q, kv_heads, st);
-        case 4: return launch_extend<D, 4>(p, batch, max_q, kv_heads, st);
-        case 8: return launch_extend<D, 8>(p, batch, max_q, kv_heads, st);
+        case 1: return launch_extend_any<D, 1>(p, fp8, batch, max_q, kv_heads, st);
+        case 2: return launch_extend_any<D, 2>(p, fp8, batch, max_q, kv_heads, st);
+        case 4: return launch_extend_any<D, 4>(p, fp8, batch, max_q, kv_heads, st);
+        case 8: return launch_extend_any<D, 8>(p, fp8, batch, max_q, kv_heads, st);
         default: *ok = false; return cudaSuccess;
     }
 }
@@ -60,7 +68,10 @@ extern "C" rc_status attn_extend(const rc_attn_desc* desc, const void* q, const 
     if (!q || !qo_indptr || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
     const rc_pool_desc& P = desc->pool;
     if (P.kv_heads <= 0 || desc->q_heads <= 0 || desc->q_heads % P.kv_heads) return RC_ERR_ARG;
-    if (P.mla || !P.v || P.head_dim_v != P.head_dim_k || P.kv_fp8) return RC_ERR_UNSUPPORTED;
+    if (P.mla || !P.v || P.head_dim_v != P.head_dim_k) return RC_ERR_UNSUPPORTED;
+    const bool fp8 = P.kv_fp8 != 0;
+    if (fp8 && P.head_dim_k != 128) return RC_ERR_UNSUPPORTED;
+    if (fp8 && (!P.k_scale || !P.v_scale)) return RC_ERR_ARG;
     rc::MQParams p{};
     p.q = static_cast<const __nv_bfloat16*>(q);
     p.pool_k = static_cast<const __nv_bfloat16*>(P.k);
@@ -77,12 +88,14 @@ extern "C" rc_status attn_extend(const rc_attn_desc* desc, const void* q, const 
     p.table_len = kv->table_len;
     p.out = static_cast<__nv_bfloat16*>(out);
     p.lse = lse;
+    p.k_scale = fp8 ? P.k_scale : nullptr;
+    p.v_scale = fp8 ? P.v_scale : nullptr;
     const int G = desc->q_heads / P.kv_heads;
     bool ok = false;
     cudaError_t e = cudaSuccess;
     cudaStream_t st = (cudaStream_t)stream;
-    if (P.head_dim_k == 128) e = dispatch<128>(G, p, batch, max_q, P.kv_heads, st, &ok);
-    else if (P.head_dim_k == 64) e = dispatch<64>(G, p, batch, max_q, P.kv_heads, st, &ok);
+    if (P.head_dim_k == 128) e = dispatch<128>(G, p, fp8, batch, max_q, P.kv_heads, st, &ok);
+    else if (P.head_dim_k == 64) e = dispatch<64>(G, p, false, batch, max_q, P.kv_heads, st, &ok);
     if (!ok) return RC_ERR_UNSUPPORTED;
     return rc_host::launch_status(e);
 }

@@ -26,6 +26,15 @@
 // thread's MMAs in issue order, so S(t+2) overwrites P(t) only after P(t).V
 // has read it.  All hand-offs are mbarriers; every wait is bounded and a wait
 // that gives up flags RC_ERR_TIMEOUT.
+//
+// FP8 pool (E4M3 codes, one fp32 scale per (slot, KV head) row): the products
+// run in f16 (every E4M3 value is an f16 value; the bf16 queries convert
+// exactly within f16's range).  The producers load codes with plain 16-byte
+// loads, widen them to f16 in registers and store the operand tiles
+// themselves (then fence to the async proxy and arrive), along with the
+// tile's 64 K and 64 V scales; the softmax scales S by the K scales and folds
+// the V scales into P.  The ring has 4 stages (the scales take the room of
+// the fifth).
 #pragma once
 
 #include "mq_attn.cuh"
@@ -37,21 +46,25 @@ constexpr int QT = 2;          // query tiles per CTA
 constexpr int TM = 128;        // rows per query tile
 constexpr int ROWS = QT * TM;  // query rows per CTA
 constexpr int TN = 64;         // keys per tile
-constexpr int NS = 5;          // K/V stages
+constexpr int NS_BF16 = 5;     // K/V stages
+constexpr int NS_FP8 = 4;
 constexpr int NP = 2;          // producer warps (a third one measured no faster)
 constexpr int MMA_WARP = 8 + NP;
 constexpr int THREADS = 32 * (MMA_WARP + 1);
 constexpr uint32_t kWaitIter = 1u << 24;
-constexpr int kBars = 1 + 2 * NS + 4 + 4 + 2;
+template <bool FP8>
+__host__ __device__ constexpr int stages() { return FP8 ? NS_FP8 : NS_BF16; }
+template <bool FP8>
+__host__ __device__ constexpr int n_bars() { return 1 + 2 * stages<FP8>() + 4 + 4 + 2; }
 
-template <int D>
+template <int D, bool FP8 = false>
 __host__ __device__ constexpr int smem_bytes() {
-    return QT * TM * D * 2 + NS * 2 * TN * D * 2 + kBars * 8 + 16;
+    return QT * TM * D * 2 + stages<FP8>() * 2 * TN * D * 2 + (FP8 ? stages<FP8>() * 2 * TN * 4 : 0) +
+           n_bars<FP8>() * 8 + 16;
 }
 
-// Whether the cascade path reads FP8 pools (not yet: the caller is told
-// RC_ERR_UNSUPPORTED instead).
-inline constexpr bool fp8_cascade_supported() { return false; }
+// The cascade path reads FP8 pools too.
+inline constexpr bool fp8_cascade_supported() { return true; }
 
 using tc::ex2;
 using tc::fadd2;
@@ -59,18 +72,22 @@ using tc::ffma2;
 using tc::max3;
 using tc::mbar_arrive;
 
-template <int D, int G, rc::MQMode MODE>
+template <int D, int G, rc::MQMode MODE, bool FP8 = false>
 __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams p) {
+    static_assert(!FP8 || D == 128, "FP8 pools: head_dim 128");
+    constexpr int NS = stages<FP8>();
+    constexpr int kBars = n_bars<FP8>();
     constexpr int CH = D / 8;
     constexpr int TPC = ROWS / G;               // tokens (or requests) per CTA
     constexpr int KV_BYTES = TN * D * 2;
     constexpr uint32_t SB = CH * 128;            // bytes between 8-row groups of Q/K/V tiles
-    constexpr uint32_t idS = tc::idesc_bf16(TM, TN, false);
-    constexpr uint32_t idPV = tc::idesc_bf16(TM, D, true);
+    constexpr uint32_t idS = FP8 ? tc::idesc_f16(TM, TN, false) : tc::idesc_bf16(TM, TN, false);
+    constexpr uint32_t idPV = FP8 ? tc::idesc_f16(TM, D, true) : tc::idesc_bf16(TM, D, true);
     extern __shared__ __align__(1024) unsigned char smem[];
     unsigned char* sQ = smem;                                  // [QT][128 rows][D]
     unsigned char* sKV = sQ + QT * TM * D * 2;                 // [NS][K, V]
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + NS * 2 * KV_BYTES);
+    float* sScale = reinterpret_cast<float*>(sKV + NS * 2 * KV_BYTES);  // FP8: [NS][K scales, V scales]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + NS * 2 * KV_BYTES + (FP8 ? NS * 2 * TN * 4 : 0));
     uint64_t* q_full = bar + 0;              // count 8 (softmax warps)
     uint64_t* kv_full = bar + 1;             // [NS], count 32 (the lanes of the tile's producer warp)
     uint64_t* kv_empty = bar + 1 + NS;       // [NS], count 1 (MMA commit)
@@ -163,15 +180,33 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             else qrow[i] = qok[i] ? (int64_t)__ldg(p.seg_rows + qo0 + tk) * p.q_heads + h : 0;
             if (!qok[i]) qrow[i] = 0;
         }
+        if constexpr (FP8) {  // f16 operand: load, convert, store
+            uint4 qv[CH];
 #pragma unroll
-        for (int i = 0; i < CH; ++i) {
-            const int gi = r + 128 * i;
-            const int rr = (gi & 7) + 8 * (gi / (8 * CH));
-            const int c = (gi >> 3) % CH;
-            rc::cp_async16(rc::smem_u32(sQq + tc::cm_offset(rr, c, CH)), p.q + qrow[i] * D + c * 8,
-                           qok[i] ? 16u : 0u);
+            for (int i = 0; i < CH; ++i) {
+                const int c = ((r + 128 * i) >> 3) % CH;
+                qv[i] = qok[i] ? __ldg(reinterpret_cast<const uint4*>(p.q + qrow[i] * D + c * 8)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int gi = r + 128 * i;
+                const int rr = (gi & 7) + 8 * (gi / (8 * CH));
+                const int c = (gi >> 3) % CH;
+                *reinterpret_cast<uint4*>(sQq + tc::cm_offset(rr, c, CH)) =
+                    make_uint4(rc::bf16x2_to_f16x2(qv[i].x), rc::bf16x2_to_f16x2(qv[i].y),
+                               rc::bf16x2_to_f16x2(qv[i].z), rc::bf16x2_to_f16x2(qv[i].w));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int gi = r + 128 * i;
+                const int rr = (gi & 7) + 8 * (gi / (8 * CH));
+                const int c = (gi >> 3) % CH;
+                rc::cp_async16(rc::smem_u32(sQq + tc::cm_offset(rr, c, CH)), p.q + qrow[i] * D + c * 8,
+                               qok[i] ? 16u : 0u);
+            }
+            rc::cp_async_commit();
         }
-        rc::cp_async_commit();
     }
     if (tid == 0) {
         tc::mbar_init(q_full, 8);
@@ -233,6 +268,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                     s[j] = __uint_as_float(sa[j]);
                     s[32 + j] = __uint_as_float(sb[j]);
                 }
+                const float* tsc = sScale + (t % NS) * 2 * TN;  // FP8: this tile's K then V scales
+                if constexpr (FP8) {
+                    // the producer's scale stores are visible once its arrival
+                    // on the stage is (that phase completed before S(t) ran)
+                    ok = __all_sync(0xffffffffu, tc::mbar_wait(&kv_full[t % NS], (t / NS) & 1, kWaitIter)) && ok;
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) s[j] *= tsc[j];
+                }
                 const int kb = t * TN;
                 if (kb + TN > lim) {  // the causal edge or the end of the keys
 #pragma unroll
@@ -279,7 +322,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                     const float2 x = ffma2(make_float2(s[2 * i], s[2 * i + 1]), sc, nmu);
                     const float2 e = make_float2(ex2(x.x), ex2(x.y));
                     ls[i & 3] = fadd2(ls[i & 3], e);
-                    pk[i] = rc::pack_bf16(e.x, e.y);
+                    if constexpr (FP8) pk[i] = rc::pack_f16(e.x * tsc[TN + 2 * i], e.y * tsc[TN + 2 * i + 1]);
+                    else pk[i] = rc::pack_bf16(e.x, e.y);
                 }
                 // P (bf16) over the first half of this S buffer: the A operand of P.V
                 tc::tmem_st32_issue(tS, pk);
@@ -384,6 +428,61 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             if (!ok) break;
             unsigned char* sK = sKV + s * 2 * KV_BYTES;
             unsigned char* sV = sK + KV_BYTES;
+            if constexpr (FP8) {
+                // 16 E4M3 codes per load (8 keys x 64 bytes per instruction,
+                // so the 16-byte f16 stores of 8 keys are 128 contiguous bytes)
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const unsigned char* src = reinterpret_cast<const unsigned char*>(m ? p.pool_v : p.pool_k);
+                    unsigned char* dst = m ? sV : sK;
+                    uint4 w[TN / 8][2];
+#pragma unroll
+                    for (int kg = 0; kg < TN / 8; ++kg) {
+                        const int key = kg * 8 + klo;
+                        int slot = __shfl_sync(0xffffffffu, sl[kg >> 2], (kg & 3) * 8 + klo);
+                        bool live = t * TN + key < key_count;
+                        if (live && (slot < 0 || (int64_t)slot >= p.n_slots)) {
+                            if (m == 0) rc::flag_error(p.err, rc::kErrBadSlot);
+                            live = false;
+                        }
+                        const int64_t base = ((int64_t)(live ? slot : 0) * p.kv_heads + kvh) * D;
+#pragma unroll
+                        for (int cg = 0; cg < 2; ++cg)
+                            w[kg][cg] = live ? __ldg(reinterpret_cast<const uint4*>(src + base + (cg * 4 + csub) * 16))
+                                             : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int kg = 0; kg < TN / 8; ++kg) {
+                        const int key = kg * 8 + klo;
+#pragma unroll
+                        for (int cg = 0; cg < 2; ++cg) {
+                            const int c8 = cg * 4 + csub;  // 16-code chunk: f16 chunks 2*c8, 2*c8+1
+                            const uint4 x = w[kg][cg];
+                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8, CH)) =
+                                make_uint4(rc::e4m3x2_to_f16x2(x.x), rc::e4m3x2_to_f16x2(x.x >> 16),
+                                           rc::e4m3x2_to_f16x2(x.y), rc::e4m3x2_to_f16x2(x.y >> 16));
+                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8 + 1, CH)) =
+                                make_uint4(rc::e4m3x2_to_f16x2(x.z), rc::e4m3x2_to_f16x2(x.z >> 16),
+                                           rc::e4m3x2_to_f16x2(x.w), rc::e4m3x2_to_f16x2(x.w >> 16));
+                        }
+                    }
+                }
+                float* tsc = sScale + s * 2 * TN;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int key = lane + 32 * h2;
+                    const int slot = sl[h2];
+                    const bool live = t * TN + key < key_count && slot >= 0 && (int64_t)slot < p.n_slots;
+                    const int64_t row = (int64_t)(live ? slot : 0) * p.kv_heads + kvh;
+                    tsc[key] = live ? __ldg(p.k_scale + row) : 0.f;
+                    tsc[TN + key] = live ? __ldg(p.v_scale + row) : 0.f;
+                }
+                tc::fence_proxy_async();  // this lane's stores, before the tensor core reads them
+                mbar_arrive(&kv_full[s]);
+                sl[0] = sl_next[0];
+                sl[1] = sl_next[1];
+                continue;
+            }
 #pragma unroll
             for (int kg = 0; kg < TN / 8; ++kg) {
                 const int key = kg * 8 + klo;

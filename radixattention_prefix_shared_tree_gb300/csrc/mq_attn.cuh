@@ -35,6 +35,9 @@ struct MQParams {
     float* part_lse;  // [total_seg_rows][q_heads][seg_chunks], log2 units (-inf: empty chunk)
     int32_t seg_chunk;   // keys per cascade CTA
     int32_t seg_chunks;  // chunks per segment (grid z = segment * seg_chunks + chunk)
+    // FP8 pool: pool_k / pool_v hold E4M3 codes and these the per-row scales
+    const float* k_scale;  // [n_slots][kv_heads]
+    const float* v_scale;
 };
 
 }  // namespace rc

@@ -44,6 +44,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with f16 A and B (format code 0).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+    return idesc_bf16(M, N, b_mn_major) & ~((1u << 7) | (1u << 10));
+}
+
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
 RC_DEV void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool accumulate) {
     asm volatile(

@@ -292,20 +292,30 @@ def plan_from_rows(rows: list) -> dict:
 class DeviceEngine:
     """KV pool + slot tables in HBM and the kernel launches of one batch."""
 
-    def __init__(self, shape, pool_slots: int, device="cuda"):
+    def __init__(self, shape, pool_slots: int, device="cuda", kv_fp8: bool = False):
         import torch
         self.torch = torch
         self.shape = shape
         self.device = torch.device(device)
+        self.kv_fp8 = bool(kv_fp8)
         dev = self.device
+        self.k_scale = self.v_scale = None
         if shape.mla:
+            if kv_fp8:
+                raise ValueError("FP8 pools are GQA only")
             self.pool_k = torch.zeros(pool_slots, shape.head_dim_k, dtype=torch.bfloat16, device=dev)
             self.pool_v = None
+        elif kv_fp8:  # E4M3 codes and one fp32 scale per (slot, KV head) row
+            self.pool_k = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_k, dtype=torch.uint8, device=dev)
+            self.pool_v = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_v, dtype=torch.uint8, device=dev)
+            self.k_scale = torch.zeros(pool_slots, shape.kv_heads, dtype=torch.float32, device=dev)
+            self.v_scale = torch.zeros(pool_slots, shape.kv_heads, dtype=torch.float32, device=dev)
         else:
             self.pool_k = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_k, dtype=torch.bfloat16, device=dev)
             self.pool_v = torch.zeros(pool_slots, shape.kv_heads, shape.head_dim_v, dtype=torch.bfloat16, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.pool = make_pool_desc(self.pool_k, self.pool_v, self.err, mla=shape.mla, head_dim_v=shape.head_dim_v)
+        self.pool = make_pool_desc(self.pool_k, self.pool_v, self.err, mla=shape.mla, head_dim_v=shape.head_dim_v,
+                                   k_scale=self.k_scale, v_scale=self.v_scale)
         self.desc = make_attn_desc(self.pool, shape.q_heads, shape.scale)
         self.sms = torch.cuda.get_device_properties(dev).multi_processor_count if dev.type == "cuda" else 1
         self._ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
@@ -313,7 +323,7 @@ class DeviceEngine:
         self._stage_next = 0
         self.timing = False          # record CUDA events around device calls
         self.timing_every = 1        # decode steps: events on every n-th step only
-        self.fuse_store = True       # decode steps store the new token inside attn_decode_append
+        self.fuse_store = not kv_fp8  # decode steps store the new token inside attn_decode_append (bf16 pools)
         self.events = {}             # call name -> [(start, end, info)]
         self.launches = 0            # kernels launched by the library (counted per call)
         self._ev_pool = []

@@ -522,10 +522,106 @@ def test_fp8_pool_rejected_where_unsupported(cuda):
     q = torch.zeros(2, 32, 128, dtype=torch.bfloat16, device=cuda)
     out = torch.empty_like(q)
     ws = torch.empty(1 << 20, dtype=torch.uint8, device=cuda)
-    qo = torch.tensor([0, 1, 2], dtype=torch.int32, device=cuda)
-    with pytest.raises(ra.RCError) as e:
-        ra.attn_extend(desc, q, qo, kv, 2, 1, out, None)
-    assert e.value.status == ra.RC_ERR_UNSUPPORTED
     with pytest.raises(ra.RCError) as e:
         ra.attn_decode_append(desc, q, q[:, :8], q[:, :8], kv, 2, out, None, ws)
     assert e.value.status == ra.RC_ERR_UNSUPPORTED
+
+
+def _fp8_oracle_rows(pool, rows, q_bits, ctx_of_row, Hq, Hkv, scale):
+    """The FP8 oracle over gathered rows of the dequantised pool."""
+    from oracle import fp8_oracle as f8
+    if not hasattr(pool, "kd"):
+        pool.kd = f8.dequantize(pool.k8.cpu().numpy(), pool.ks.cpu().numpy())
+        pool.vd = f8.dequantize(pool.v8.cpu().numpy(), pool.vs.cpu().numpy())
+    sel = np.concatenate(rows)
+    offs = np.zeros(len(rows), np.int64)
+    offs[1:] = np.cumsum([len(r) for r in rows])[:-1]
+    return f8.attention(q_bits, pool.kd[sel], pool.vd[sel], offs, np.asarray(ctx_of_row, np.int64), Hq, Hkv, scale)
+
+
+@pytest.mark.parametrize("Hq,Hkv,reqs", [
+    (32, 8, [(1792, 40), (0, 17), (100, 130), (1792, 64), (0, 1)]),
+    (64, 8, [(2048, 33), (300, 8), (0, 200)]),
+    (16, 8, [(63, 65)]),
+])
+def test_extend_fp8_vs_oracle(cuda, Hq, Hkv, reqs):
+    n_slots = 8000
+    pool = Fp8Pool(n_slots, Hkv, cuda, 7 * Hq, magnitudes=False)
+    lens = [p + n for p, n in reqs]
+    rows, table, start, length = _tables(lens, n_slots, 5, cuda)
+    g = torch.Generator().manual_seed(4)
+    ns = [n for _, n in reqs]
+    T = sum(ns)
+    D = 128
+    q = rand_bf16(g, (T, Hq, D), cuda)
+    qo = torch.tensor(np.concatenate([[0], np.cumsum(ns)]).astype(np.int32), device=cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    out = torch.empty(T, Hq, D, dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty(T, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_extend(desc, q, qo, kv, len(reqs), max(ns), out, lse)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    row_of, ctx = [], []
+    for b, (p, n) in enumerate(reqs):
+        for i in range(n):
+            row_of.append(rows[b])
+            ctx.append(p + i + 1)
+    ref, ref_lse = _fp8_oracle_rows(pool, row_of, bits(q), ctx, Hq, Hkv, scale)
+    check(bits(out), ref, lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 8), (64, 8)])
+def test_cascade_fp8_equals_flat_and_oracle(cuda, Hq, Hkv):
+    """FP8 pool: cascade decode == flat decode == the FP8 oracle."""
+    n_slots, D = 20000, 128
+    pool = Fp8Pool(n_slots, Hkv, cuda, 99 + Hq, magnitudes=False)
+    rng = np.random.default_rng(8)
+    perm = rng.permutation(n_slots).astype(np.int32)
+    root, mids = perm[:700], [perm[700:900], perm[900:1157]]
+    off = 1157
+    rows = []
+    for b in range(40):
+        tail_len = int(rng.integers(1, 150))
+        tail = perm[off:off + tail_len]
+        off += tail_len
+        mid = mids[b % 2] if b < 30 else np.zeros(0, np.int32)
+        rows.append(np.concatenate([root, mid, tail]).astype(np.int32))
+    B = len(rows)
+    lens = [len(r) for r in rows]
+    _, table, start, length = _tables(lens, n_slots, 0, cuda)
+    table.copy_(torch.from_numpy(np.concatenate(rows)).to(cuda))
+    g = torch.Generator().manual_seed(6)
+    q = rand_bf16(g, (B, Hq, D), cuda)
+    scale = 1.0 / np.sqrt(D)
+    desc = ra.make_attn_desc(pool.desc, Hq, scale)
+    kv = ra.make_kv_table(table, start, length, max(lens))
+    ws = torch.empty(ra.attn_decode_workspace(desc, B, max(lens)), dtype=torch.uint8, device=cuda)
+    flat = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=cuda)
+    flat_lse = torch.empty(B, Hq, dtype=torch.float32, device=cuda)
+    ra.attn_decode(desc, q, kv, B, flat, flat_lse, ws)
+    prefix_rows = [r[:len(r) - 1] for r in rows]
+    segs, private = plan_cascade(prefix_rows)
+    assert len(segs) == 3
+    seg_slots = np.concatenate([s for s, _ in segs]).astype(np.int32)
+    seg_indptr = np.concatenate([[0], np.cumsum([len(s) for s, _ in segs])]).astype(np.int32)
+    seg_rows = np.concatenate([np.asarray(r, np.int32) for _, r in segs])
+    seg_row_indptr = np.concatenate([[0], np.cumsum([len(r) for _, r in segs])]).astype(np.int32)
+    pos_of = [[p for p, b in enumerate(seg_rows) if b == bb] for bb in range(B)]
+    req_indptr = np.concatenate([[0], np.cumsum([len(x) for x in pos_of])]).astype(np.int32)
+    req_pos = np.concatenate([np.asarray(x, np.int32) for x in pos_of])
+    T = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(cuda)
+    arrs = [T(seg_slots), T(seg_indptr), T(seg_row_indptr), T(seg_rows), T(req_indptr), T(req_pos)]
+    casc = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs),
+                           max_seg_len=max(len(x) for x, _ in segs))
+    pstart = T(start.cpu().numpy() + private)
+    plen = T(np.asarray(lens) - private)
+    kv2 = ra.make_kv_table(table, pstart, plen, int((np.asarray(lens) - private).max()))
+    ws2 = torch.empty(ra.attn_decode_workspace(desc, B, kv2.max_len, casc), dtype=torch.uint8, device=cuda)
+    cout = torch.empty_like(flat)
+    clse = torch.empty_like(flat_lse)
+    ra.attn_decode(desc, q, kv2, B, cout, clse, ws2, cascade=casc)
+    assert ra.rc_sync(pool.err) == ra.RC_OK
+    ref, ref_lse = _fp8_oracle_rows(pool, rows, bits(q), lens, Hq, Hkv, scale)
+    check(bits(flat), ref, flat_lse.cpu().numpy(), ref_lse)
+    check(bits(cout), ref, clse.cpu().numpy(), ref_lse)

@@ -26,12 +26,19 @@ pytestmark = pytest.mark.gpu
 MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 2e-3
 
 
-def oracle_positions(shape, hashes, positions):
-    """Oracle attention for query positions of one request (keys 0..pos)."""
+def oracle_positions(shape, hashes, positions, fp8=False):
+    """Oracle attention for query positions of one request (keys 0..pos).
+    fp8: K/V as an FP8 pool holds them (the oracle's own quantisation)."""
     n = int(max(positions)) + 1
     kb = hg.gen_values(hashes[:n], hg.KIND_K, shape.kv_heads, shape.head_dim_k)
     vb = None if shape.mla else hg.gen_values(hashes[:n], hg.KIND_V, shape.kv_heads, shape.head_dim_v)
     qb = hg.gen_values(hashes[np.asarray(positions)], hg.KIND_Q, shape.q_heads, shape.head_dim_k)
+    if fp8:
+        from oracle import fp8_oracle as f8
+        kd = f8.dequantize(*f8.quantize_rows(kb.reshape(n, shape.kv_heads, -1)))
+        vd = f8.dequantize(*f8.quantize_rows(vb.reshape(n, shape.kv_heads, -1)))
+        return f8.attention(qb.reshape(len(positions), shape.q_heads, -1), kd, vd, np.zeros(len(positions), np.int64),
+                            np.asarray(positions, np.int64) + 1, shape.q_heads, shape.kv_heads, shape.scale)
     return oracle.attention(qb, kb, vb, np.zeros(len(positions), np.int64), np.asarray(positions, np.int64) + 1,
                             shape.q_heads, shape.kv_heads, shape.head_dim_k, shape.head_dim_v, shape.scale,
                             latent=shape.mla)
@@ -49,9 +56,9 @@ def compare(out_bits, lse, ref, ref_lse, stats):
     assert np.abs(lse.astype(np.float64) - ref_lse).max() <= LSE_ABS
 
 
-def run(trace, runner_fn, pool, cuda, cascade=True, policy=ra.RC_LPM, cache_cls=ra.RadixCache, **kw):
+def run(trace, runner_fn, pool, cuda, cascade=True, policy=ra.RC_LPM, cache_cls=ra.RadixCache, kv_fp8=False, **kw):
     model = SynthModel(trace.shape, trace.seed, trace.vocab, device=cuda)
-    eng = DeviceEngine(trace.shape, pool, device=cuda)
+    eng = DeviceEngine(trace.shape, pool, device=cuda, kv_fp8=kv_fp8)
     cache = cache_cls(pool)
     log = []
     runner = wl.Runner(cache, model, eng, policy=policy, cascade=cascade, collect=True, log=log,
@@ -61,19 +68,19 @@ def run(trace, runner_fn, pool, cuda, cascade=True, policy=ra.RC_LPM, cache_cls=
     return runner, model, cache, log, res
 
 
-def check_requests(runner, model, rids, shape, stats, max_decode_steps=None):
+def check_requests(runner, model, rids, shape, stats, max_decode_steps=None, fp8=False):
     for rid in rids:
         h = model.hashes(rid)
         if rid in runner.extend_out:
             pos, o, l = runner.extend_out[rid]
-            ref, ref_l = oracle_positions(shape, h, pos)
+            ref, ref_l = oracle_positions(shape, h, pos, fp8)
             compare(o, l, ref, ref_l, stats)
         dec = runner.decode_out.get(rid, [])
         if max_decode_steps is not None:
             dec = [d for i, d in enumerate(dec) if i in max_decode_steps]
         if dec:
             pos = [p for p, _, _ in dec]
-            ref, ref_l = oracle_positions(shape, h, pos)
+            ref, ref_l = oracle_positions(shape, h, pos, fp8)
             compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]), ref, ref_l, stats)
 
 
@@ -197,3 +204,18 @@ def test_multimodal_image_keys_vs_oracle(cuda, cache_kind):
     orunner = wl.Runner(omake(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=olog)
     wl.run_multimodal(orunner, tr, bo.image_key, batch=4)
     assert olog == log
+
+
+@pytest.mark.parametrize("cascade", [True, False])
+def test_few_shot_fp8_pool_vs_oracle(cuda, cascade):
+    """The few-shot workload (reduced) with an E4M3 pool: prefill over the
+    cached examples, decode steps with kv_store quantising each new token;
+    sampled requests against the oracle over the oracle's own quantisation of
+    the same K/V."""
+    tr = traces.few_shot(n_questions=40, max_new=5)
+    runner, model, cache, log, reqs = run(tr, wl.run_few_shot, 1 << 16, cuda, cascade=cascade, kv_fp8=True)
+    if cascade:
+        assert runner.last_layout.use_cascade
+    stats = {}
+    check_requests(runner, model, [r.rid for r in reqs[::6]], tr.shape, stats, fp8=True)
+    assert stats["sum"] / stats["n"] <= MEAN_ABS
