@@ -335,6 +335,75 @@ def latent_path(dev, hbm, bf16, peak_src, steps: int = 8):
             "peak_source": f"{peak_src} HBM copy and bf16 dense burst"}
 
 
+def fp8_path(dev, hbm, peak_src, trace_fn, args, steps: int = 3, warmup: int = 2):
+    """The benchmark's step (same workload, same launch configuration) over an
+    E4M3 pool: prefill quantises the new tokens (kv_store) and reads codes
+    (tcgen05 kernel, f16 products), every decode step stores the new token's
+    codes and scales (kv_store) and attends over codes (cascade + table pass).
+    Timed with CUDA events around the steps; attn_decode per call on every 4th
+    step (the event pair also covers that step's kv_store).  Bytes per call:
+    unique rows x (codes + scale) for K and V, indices, Q, O, and the new
+    token (bf16 read, codes and scales written)."""
+    import torch
+    import radixattention_prefix_shared_tree_gb300 as ra
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
+    from synth.model import SynthModel
+
+    tr0 = trace_fn(0)
+    sh = tr0.shape
+    base = SynthModel(sh, tr0.seed, tr0.vocab, device=dev)
+    model = ReplayModel(base, torch)
+    pool = args.pool_slots or tr0.pool_slots
+    eng = DeviceEngine(sh, pool, device=dev, kv_fp8=True)
+    runner = wl.Runner(ra.RadixCache(pool), model, eng, cascade=True)
+    runner.model = base
+    runner.serve([runner.request(tr0.warm, 0)])
+    runner.model = model
+    batches = []
+    for s in range(warmup + steps):
+        tr = trace_fn(1000 + s)
+        reqs = [runner.request(tr.prompt(i), tr.max_new) for i in range(len(tr.questions))]
+        model.prepare(reqs, WARM_LEN)
+        batches.append(reqs)
+    for s in range(warmup):
+        runner.serve(batches[s])
+    torch.cuda.synchronize()
+    eng.timing_every = 4
+    eng.start_timing(4 * steps * (args.max_new + 8) + 64)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for s in range(warmup, warmup + steps):
+        runner.serve(batches[s])
+    ev1.record()
+    torch.cuda.synchronize()
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+    ms = ev0.elapsed_time(ev1) / steps
+    R8 = 2 * sh.kv_heads * (sh.head_dim_k + 4)
+    evs = eng.events.get("attn_decode", [])
+    durs = [a.elapsed_time(b) * 1e-3 for a, b, _ in evs]
+    by = []
+    for _, _, info in evs:
+        lay, t = info[1], info[2]
+        L = lay.L + t + 1
+        tail = (L - lay.private).sum()
+        seg = sum(len(x) for x, _ in lay.segments) if lay.use_cascade else 0
+        B = lay.batch_size
+        qo = B * sh.q_heads * (sh.head_dim_k + sh.head_dim_v) * 2
+        store = B * (2 * sh.kv_heads * sh.head_dim_k * 2 + R8)
+        by.append((seg + tail) * R8 + (seg + tail) * 4 + qo + store)
+    sec = sum(durs) / max(len(durs), 1)
+    u = float(np.mean(by)) if by else 0.0
+    ext = eng.events.get("attn_extend", [])
+    ext_us = 1e3 * sum(a.elapsed_time(b) for a, b, _ in ext) / max(len(ext), 1)
+    return {"config": "the benchmark's workload and launch configuration over an E4M3 pool "
+                      "(one fp32 scale per (slot, KV head) row); %d timed steps" % steps,
+            "tokens_per_s": args.questions * args.max_new / (ms * 1e-3), "ms_per_step": ms,
+            "attn_decode_us": sec * 1e6, "attn_extend_us": ext_us, "bytes_per_call": u,
+            "hbm": {"achieved_gbs": u / sec / 1e9, "peak": hbm, "frac": u / sec / 1e9 / hbm},
+            "peak_source": f"{peak_src} HBM copy"}
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -565,7 +634,8 @@ def main():
     if rank == 0 and not args.no_paths:
         n_req = args.steps * args.questions
         paths = {"host_tree_us_per_request": {n: 1e6 * v / n_req for n, v in host_t.items()},
-                 "latent_decode": latent_path(dev, hbm, bf16, peak_src)}
+                 "latent_decode": latent_path(dev, hbm, bf16, peak_src),
+                 "fp8_kv": fp8_path(dev, hbm, peak_src, trace_fn, args)}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -257,9 +257,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(sK + rc::swz<CH>(g_lane, ks) + 4 * t_lane);
                     const uint32_t w1 =
                         *reinterpret_cast<const uint32_t*>(sK + rc::swz<CH>(g_lane + 8, ks) + 4 * t_lane);
-                    rc::mma_f16_16816(ks & 1 ? s2 : s, rc::e4m3x2_to_f16x2(w0), rc::e4m3x2_to_f16x2(w1),
-                                      rc::e4m3x2_to_f16x2(w0 >> 16), rc::e4m3x2_to_f16x2(w1 >> 16), qb[ks][0],
-                                      qb[ks][1]);
+                    uint32_t a0, a1, a2, a3;
+                    rc::e4m3x4_to_f16x4(w0, a0, a2);
+                    rc::e4m3x4_to_f16x4(w1, a1, a3);
+                    rc::mma_f16_16816(ks & 1 ? s2 : s, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
                 }
             } else {
                 const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -339,10 +340,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
                 const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                const uint32_t lo = rc::prmt(x0[mt >> 1], x1[mt >> 1], sel);
-                const uint32_t hi = rc::prmt(x8[mt >> 1], x9[mt >> 1], sel);
-                rc::mma_f16_16816(o[mt], rc::e4m3x2_to_f16x2(lo), rc::e4m3x2_to_f16x2(lo >> 16),
-                                  rc::e4m3x2_to_f16x2(hi), rc::e4m3x2_to_f16x2(hi >> 16), pb0, pb1);
+                uint32_t a0, a1, a2, a3;
+                rc::e4m3x4_to_f16x4(rc::prmt(x0[mt >> 1], x1[mt >> 1], sel), a0, a1);
+                rc::e4m3x4_to_f16x4(rc::prmt(x8[mt >> 1], x9[mt >> 1], sel), a2, a3);
+                rc::mma_f16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
             }
         } else {
             const uint32_t pb0 = rc::movmatrix_trans(rc::pack_bf16(p0, p1));

@@ -430,27 +430,32 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             unsigned char* sV = sK + KV_BYTES;
             if constexpr (FP8) {
                 // 16 E4M3 codes per load (8 keys x 64 bytes per instruction,
-                // so the 16-byte f16 stores of 8 keys are 128 contiguous bytes)
+                // so the 16-byte f16 stores of 8 keys are 128 contiguous bytes);
+                // the K and V loads of the tile are all in flight together
+                uint4 w2[2][TN / 8][2];
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const unsigned char* src = reinterpret_cast<const unsigned char*>(m ? p.pool_v : p.pool_k);
-                    unsigned char* dst = m ? sV : sK;
-                    uint4 w[TN / 8][2];
+                for (int kg = 0; kg < TN / 8; ++kg) {
+                    const int key = kg * 8 + klo;
+                    int slot = __shfl_sync(0xffffffffu, sl[kg >> 2], (kg & 3) * 8 + klo);
+                    bool live = t * TN + key < key_count;
+                    if (live && (slot < 0 || (int64_t)slot >= p.n_slots)) {
+                        rc::flag_error(p.err, rc::kErrBadSlot);
+                        live = false;
+                    }
+                    const int64_t base = ((int64_t)(live ? slot : 0) * p.kv_heads + kvh) * D;
 #pragma unroll
-                    for (int kg = 0; kg < TN / 8; ++kg) {
-                        const int key = kg * 8 + klo;
-                        int slot = __shfl_sync(0xffffffffu, sl[kg >> 2], (kg & 3) * 8 + klo);
-                        bool live = t * TN + key < key_count;
-                        if (live && (slot < 0 || (int64_t)slot >= p.n_slots)) {
-                            if (m == 0) rc::flag_error(p.err, rc::kErrBadSlot);
-                            live = false;
-                        }
-                        const int64_t base = ((int64_t)(live ? slot : 0) * p.kv_heads + kvh) * D;
+                    for (int m = 0; m < 2; ++m) {
+                        const unsigned char* src = reinterpret_cast<const unsigned char*>(m ? p.pool_v : p.pool_k);
 #pragma unroll
                         for (int cg = 0; cg < 2; ++cg)
-                            w[kg][cg] = live ? __ldg(reinterpret_cast<const uint4*>(src + base + (cg * 4 + csub) * 16))
-                                             : make_uint4(0, 0, 0, 0);
+                            w2[m][kg][cg] = live ? __ldg(reinterpret_cast<const uint4*>(src + base + (cg * 4 + csub) * 16))
+                                                 : make_uint4(0, 0, 0, 0);
                     }
+                }
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    unsigned char* dst = m ? sV : sK;
+                    auto& w = w2[m];
 #pragma unroll
                     for (int kg = 0; kg < TN / 8; ++kg) {
                         const int key = kg * 8 + klo;
@@ -458,12 +463,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                         for (int cg = 0; cg < 2; ++cg) {
                             const int c8 = cg * 4 + csub;  // 16-code chunk: f16 chunks 2*c8, 2*c8+1
                             const uint4 x = w[kg][cg];
-                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8, CH)) =
-                                make_uint4(rc::e4m3x2_to_f16x2(x.x), rc::e4m3x2_to_f16x2(x.x >> 16),
-                                           rc::e4m3x2_to_f16x2(x.y), rc::e4m3x2_to_f16x2(x.y >> 16));
-                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8 + 1, CH)) =
-                                make_uint4(rc::e4m3x2_to_f16x2(x.z), rc::e4m3x2_to_f16x2(x.z >> 16),
-                                           rc::e4m3x2_to_f16x2(x.w), rc::e4m3x2_to_f16x2(x.w >> 16));
+                            uint4 f0, f1;
+                            rc::e4m3x4_to_f16x4(x.x, f0.x, f0.y);
+                            rc::e4m3x4_to_f16x4(x.y, f0.z, f0.w);
+                            rc::e4m3x4_to_f16x4(x.z, f1.x, f1.y);
+                            rc::e4m3x4_to_f16x4(x.w, f1.z, f1.w);
+                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8, CH)) = f0;
+                            *reinterpret_cast<uint4*>(dst + tc::cm_offset(key, 2 * c8 + 1, CH)) = f1;
                         }
                     }
                 }

@@ -114,8 +114,19 @@ RC_DEV uint32_t pack_f16(float lo, float hi) {
 // Two E4M3 codes (low byte first) to two f16 (low half first); exact, since
 // every E4M3 value is an f16 value.
 RC_DEV uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+    uint32_t d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}\n"
+        : "=r"(d)
+        : "r"(two_codes));
+    return d;
+}
+// Four E4M3 codes (one word, low byte first) to two f16 pairs: lo gets codes
+// 0 and 1, hi codes 2 and 3.
+RC_DEV void e4m3x4_to_f16x4(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}\n"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
 }
 
 // A bf16 pair to an f16 pair (exact while |x| is within f16's range).
