@@ -6,21 +6,26 @@
 //
 // CTA = (key chunk, value half, request).  Both value halves compute
 // S = Q K^T over the full 576-wide key; each accumulates O for its 256 of the
-// 512 value columns, which is what TMEM holds next to two S buffers.
-// Seven warps with fixed roles:
+// 512 value columns.  Q's first 384 columns are the A operand of S from
+// tensor memory, its last 192 from shared memory: TMEM then holds two S
+// buffers (columns 0 and 32, P over their first 16), Q (64..255) and O
+// (256..511), and shared memory has room for four K/V stages next to the rest
+// of Q.  Nine warps with fixed roles:
 //   warps 0-3  softmax: one thread per head (TMEM lane); read S, write P (bf16)
 //              back over it, rescale the head's O in TMEM when its max grows by
 //              more than 2^8;
-//   warps 4, 5 producers of the even and odd tiles (stage 0 and 1): gather 32
-//              latent rows per tile by slot id with 16-byte cp.async (no-swizzle
-//              core-matrix layout), each lane arriving on the stage's barrier
-//              when its copies land;
-//   warp 6     MMA issuer (one thread) and TMEM owner.
+//   warps 4-7  producers, one per stage (tile t goes to stage t mod 4): gather
+//              32 latent rows per tile by slot id with 16-byte cp.async
+//              (no-swizzle core-matrix layout), each lane arriving on the
+//              stage's barrier when its copies land, and asking L2 for the rows
+//              of the warp's next tile one lap ahead;
+//   warp 8     MMA issuer (one thread) and TMEM owner.
 // Per 32-key tile: S = Q K^T (M 128, N 32, K 576 in 36 steps) into one of two
 // S buffers; O += P V (M 128, N 256, K 32) with P read from TMEM and V the
 // value half of the same shared-memory tile read as an MN-major operand.  The
-// next tile's S is issued before this tile's P.V.  TMEM: S buffers at columns
-// 0 and 32 (P over their first 16), O at 256..511.  Every wait is bounded and
+// issuer never holds a ready P.V behind a tile that is still loading: it
+// issues P(t).V as soon as the softmax hands P(t) over, and S(t+1) as soon as
+// tile t+1 has landed, whichever comes first.  Every wait is bounded and
 // flags RC_ERR_TIMEOUT when it gives up; a parity wait never has three
 // possible phases (see the last-tile handling).
 #pragma once
@@ -32,14 +37,20 @@ namespace rc_mla_tc {
 constexpr int DK = 576, DV = 512, DVH = 256;
 constexpr int M = 128;        // query heads per CTA (all)
 constexpr int TN = 32;        // keys per tile
-constexpr int NS = 2;         // K/V stages
+constexpr int NS = 4;         // K/V stages (one producer warp each)
 constexpr int CK = DK / 8;    // 72 chunks of 16 bytes per latent row
-constexpr int THREADS = 224;
-constexpr int Q_BYTES = M * DK * 2;
+constexpr int QT = 384;       // Q columns held in TMEM (24 K steps)
+constexpr int CQ = (DK - QT) / 8;  // 24 chunks of Q per head in shared memory
+constexpr int W_MMA = 4 + NS;      // warp index of the MMA issuer
+constexpr int THREADS = 32 * (W_MMA + 1);
+constexpr uint32_t COL_Q = 2 * TN, COL_O = 256;  // TMEM columns
+constexpr int Q_BYTES = M * (DK - QT) * 2;
 constexpr int TILE_BYTES = TN * DK * 2;
-constexpr uint32_t SB = CK * 128;  // bytes between 8-row groups of Q and of a tile
+constexpr uint32_t SB = CK * 128;   // bytes between 8-row groups of a tile
+constexpr uint32_t SBQ = CQ * 128;  // bytes between 8-head groups of Q
 constexpr int kBars = 1 + 2 * NS + 2 + 2 + 1;
 constexpr uint32_t kWaitIter = 1u << 24;
+static_assert(COL_Q + QT / 2 <= COL_O, "Q and the S buffers overlap O in TMEM");
 
 __host__ __device__ constexpr int smem_bytes() { return Q_BYTES + NS * TILE_BYTES + kBars * 8 + 16; }
 
@@ -65,11 +76,11 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
     constexpr uint32_t idS = tc::idesc_bf16(M, TN, false);
     constexpr uint32_t idPV = tc::idesc_bf16(M, DVH, true);
     extern __shared__ __align__(1024) unsigned char smem[];
-    unsigned char* sQ = smem;                      // [128 heads][576], no swizzle
+    unsigned char* sQ = smem;                      // [128 heads][Q columns 384..575], no swizzle
     unsigned char* sKV = sQ + Q_BYTES;             // [NS][32 keys][576]
     uint64_t* bar = reinterpret_cast<uint64_t*>(sKV + NS * TILE_BYTES);
     uint64_t* q_full = bar + 0;                    // count 4 (softmax warps)
-    uint64_t* kv_full = bar + 1;                   // [NS], count 32 (producer lanes, through cp.async)
+    uint64_t* kv_full = bar + 1;                   // [NS], count 32 (the stage's producer lanes, through cp.async)
     uint64_t* kv_empty = bar + 1 + NS;             // [NS], count 1 (MMA commit)
     uint64_t* s_full = bar + 1 + 2 * NS;           // [2], count 1
     uint64_t* p_full = s_full + 2;                 // [2], count 4
@@ -109,16 +120,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
 
     // producer: slot ids of the first tile, before the set-up
     int sl = -1;
-    if ((warp == 4 || warp == 5) && (warp - 4) * TN + lane < count) sl = __ldg(keys + (warp - 4) * TN + lane);
+    if (warp >= 4 && warp < W_MMA && (warp - 4) * TN + lane < count) sl = __ldg(keys + (warp - 4) * TN + lane);
+    const __nv_bfloat16* qb = p.q + (int64_t)b * M * DK;
     if (warp < 4) {
-        // Q (all 128 heads): 8 consecutive lanes write 8 rows of one 16-byte
-        // column, 128 contiguous bytes of the core-matrix layout
-        const __nv_bfloat16* qb = p.q + (int64_t)b * M * DK;
-        for (int gi = tid; gi < M * CK; gi += 128) {
+        // Q columns 384..575 of all 128 heads: 8 consecutive lanes write 8
+        // rows of one 16-byte column, 128 contiguous bytes of the core-matrix
+        // layout
+        for (int gi = tid; gi < M * CQ; gi += 128) {
             const int j = gi & 7, rest = gi >> 3;
-            const int c = rest % CK, rg = rest / CK;
+            const int c = rest % CQ, rg = rest / CQ;
             const int r = rg * 8 + j;
-            rc::cp_async16(rc::smem_u32(sQ + tc::cm_offset(r, c, CK)), qb + (int64_t)r * DK + c * 8, 16u);
+            rc::cp_async16(rc::smem_u32(sQ + tc::cm_offset(r, c, CQ)), qb + (int64_t)r * DK + QT + c * 8, 16u);
         }
         rc::cp_async_commit();
     }
@@ -135,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
         tc::mbar_init(o_done, 1);
         tc::fence_mbar_init();
     }
-    if (warp == 6) {
+    if (warp == W_MMA) {
         tc::tmem_alloc(tslot, 512);
         tc::tmem_relinquish();
     }
@@ -148,9 +160,29 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
     if (warp < 4) {
         // ================================================ softmax (one head per thread)
         const uint32_t tl = tbase + ((uint32_t)(warp * 32) << 16);
-        const uint32_t tO = tl + 256;
+        const uint32_t tO = tl + COL_O;
+        {
+            // Q columns 0..383 of this thread's head into its TMEM lane, two
+            // bf16 per column (the even column in the low half), 64 per store
+            const uint4* qrow = reinterpret_cast<const uint4*>(qb + (int64_t)tid * DK);
+#pragma unroll 1
+            for (int g = 0; g < QT / 64; ++g) {
+                uint32_t r[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 v = __ldg(qrow + g * 8 + i);
+                    r[4 * i] = v.x;
+                    r[4 * i + 1] = v.y;
+                    r[4 * i + 2] = v.z;
+                    r[4 * i + 3] = v.w;
+                }
+                tc::tmem_st32_issue(tl + COL_Q + g * 32, r);
+                tc::tmem_st_wait();
+            }
+        }
         rc::cp_async_wait<0>();
         tc::fence_proxy_async();
+        tc::fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(q_full);
         const float sc = p.scale_log2;
@@ -271,17 +303,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
                 p.part_lse[bh * p.n_chunks + chunk] = lse2;
             }
         }
-    } else if (warp == 4 || warp == 5) {
-        // ================================================ producers (even / odd tiles)
+    } else if (warp < W_MMA) {
+        // ================================================ producers (stage = warp - 4)
         // lane -> (key within an 8-key group, 16-byte column within a group
         // of 4): 8 lanes write 128 contiguous bytes of the core-matrix layout
         const int klo = lane & 7, csub = lane >> 3;
-        for (int t = warp - 4; t < n_tiles && ok; t += 2) {
-            const int s = t % NS;
+        const int s = warp - 4;
+        for (int t = s; t < n_tiles && ok; t += NS) {
             int sl_next = -1;
             {
-                const int key = (t + 2) * TN + lane;
-                if (t + 2 < n_tiles && key < count) sl_next = __ldg(keys + key);
+                const int key = (t + NS) * TN + lane;
+                if (t + NS < n_tiles && key < count) sl_next = __ldg(keys + key);
             }
             if (t >= NS) ok = __all_sync(0xffffffffu, tc::mbar_wait(&kv_empty[s], ((t / NS) + 1) & 1, kWaitIter));
             if (!ok) break;
@@ -305,54 +337,79 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
                 }
             }
             tc::cp_async_mbar_arrive(&kv_full[s]);
+            // the rows of this warp's next tile (NS tiles on) start for L2 now
+            if (sl_next >= 0 && (int64_t)sl_next < p.n_slots)
+                rc::prefetch_l2(p.pool + (int64_t)sl_next * DK, (uint32_t)(DK * 2));
             sl = sl_next;
         }
         rc::cp_async_wait<0>();
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     } else if (lane == 0) {
-        // ================================================ MMA (warp 6)
+        // ================================================ MMA (one thread)
         const uint32_t q0 = rc::smem_u32(sQ);
         auto issue_s = [&](int t) {
             const uint32_t k0s = rc::smem_u32(sKV + (t % NS) * TILE_BYTES);
+            const uint32_t d = tbase + (t & 1) * TN;
+            // Q columns 0..383 from TMEM (8 columns per K step of 16)
 #pragma unroll 4
-            for (int k = 0; k < DK / 16; ++k)
-                tc::mma_bf16(tbase + (t & 1) * TN, tc::smem_desc(q0 + k * 256, 128, SB),
-                             tc::smem_desc(k0s + k * 256, 128, SB), idS, k > 0);
+            for (int k = 0; k < QT / 16; ++k)
+                tc::mma_bf16_ts(d, tbase + COL_Q + k * 8, tc::smem_desc(k0s + k * 256, 128, SB), idS, k > 0);
+            // columns 384..575 from shared memory
+#pragma unroll 4
+            for (int k = 0; k < (DK - QT) / 16; ++k)
+                tc::mma_bf16(d, tc::smem_desc(q0 + k * 256, 128, SBQ),
+                             tc::smem_desc(k0s + (QT / 16 + k) * 256, 128, SB), idS, true);
             tc::commit(&s_full[t & 1]);
         };
         ok = tc::mbar_wait(q_full, 0, kWaitIter);
-        if (ok) {
-            ok = tc::mbar_wait(&kv_full[0], 0, kWaitIter);
-            tc::fence_after();
-            tc::fence_proxy_async();  // the rows arrived through the generic proxy
-            if (ok) issue_s(0);
-        }
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            const int s = t % NS;
-            if (t + 1 < n_tiles) {
-                ok = tc::mbar_wait(&kv_full[(t + 1) % NS], ((t + 1) / NS) & 1, kWaitIter);
+        tc::fence_after();
+        // t: next P.V to issue; ns: S products issued.  S(ns) may go once
+        // P(ns-2).V is issued (it overwrites that S buffer), i.e. ns <= t + 1.
+        int ns = 0;
+        uint32_t idle = 0;
+        uint64_t t0 = 0;
+        for (int t = 0; t < n_tiles && ok;) {
+            bool moved = false;
+            if (ns > t && tc::mbar_test(&p_full[t & 1], (t >> 1) & 1)) {
                 tc::fence_after();
-                tc::fence_proxy_async();
-                if (!ok) break;
-                issue_s(t + 1);
-            }
-            ok = tc::mbar_wait(&p_full[t & 1], (t >> 1) & 1, kWaitIter);
-            tc::fence_after();
-            if (!ok) break;
-            // value half vh of the tile: columns [256 vh, 256 vh + 256) = chunks [32 vh, 32 vh + 32)
-            const uint32_t v0 = rc::smem_u32(sKV + s * TILE_BYTES) + vh * (DVH / 8) * 128;
+                // value half vh of the tile: columns [256 vh, 256 vh + 256) = chunks [32 vh, 32 vh + 32)
+                const int s = t % NS;
+                const uint32_t v0 = rc::smem_u32(sKV + s * TILE_BYTES) + vh * (DVH / 8) * 128;
 #pragma unroll
-            for (int j = 0; j < TN / 16; ++j)
-                tc::mma_bf16_ts(tbase + 256, tbase + (t & 1) * TN + j * 8, tc::smem_desc(v0 + j * 2 * SB, SB, 128),
-                                idPV, t > 0 || j > 0);
-            tc::commit(o_done);
-            tc::commit(&kv_empty[s]);
+                for (int j = 0; j < TN / 16; ++j)
+                    tc::mma_bf16_ts(tbase + COL_O, tbase + (t & 1) * TN + j * 8,
+                                    tc::smem_desc(v0 + j * 2 * SB, SB, 128), idPV, t > 0 || j > 0);
+                tc::commit(o_done);
+                tc::commit(&kv_empty[s]);
+                ++t;
+                moved = true;
+            }
+            if (ns < n_tiles && ns <= t + 1 && tc::mbar_test(&kv_full[ns % NS], (ns / NS) & 1)) {
+                tc::fence_after();
+                tc::fence_proxy_async();  // the rows arrived through the generic proxy
+                issue_s(ns);
+                ++ns;
+                moved = true;
+            }
+            if (moved) {
+                idle = 0;
+                t0 = 0;
+                continue;
+            }
+            // nothing ready: probe again at once (a sleep here costs more than
+            // the softmax hand-off it waits for)
+            if ((++idle & 1023) == 0) {
+                uint64_t now;
+                asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+                if (t0 == 0) t0 = now;
+                else if (now - t0 > tc::kWaitNs || idle >= kWaitIter) ok = false;
+            }
         }
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 6) {
+    if (warp == W_MMA) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }

@@ -52,6 +52,11 @@ RC_DEV uint64_t l2_policy_evict_last() {
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
     return p;
 }
+// Bring `bytes` (a multiple of 16) at a 16-byte aligned global address into
+// L2 ahead of the copies that will read them; nothing lands in shared memory.
+RC_DEV void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
+}
 // 4-byte asynchronous copy (slot ids); src_bytes = 0 writes zero.
 RC_DEV void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");

@@ -126,6 +126,19 @@ RC_DEV bool mbar_wait(uint64_t* mbar, uint32_t parity, uint32_t max_iter) {
     return false;
 }
 
+// One non-blocking probe: has the phase of the given parity completed?
+RC_DEV bool mbar_test(uint64_t* mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(rc::smem_u32(mbar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // TMEM allocation by one full warp; the address lands in *smem_slot.
 RC_DEV void tmem_alloc(uint32_t* smem_slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
