@@ -52,6 +52,12 @@ def parse():
     ap.add_argument("--pool-slots", type=int, default=0, help="KV pool size (default: the workload's 2^21)")
     ap.add_argument("--no-paths", action="store_true",
                     help="skip the per-path measurements (latent decode, host tree calls)")
+    ap.add_argument("--latent-only", action="store_true",
+                    help="run only the latent decode path (128 requests) and print its measurement; with "
+                         "--latent-shared/--latent-private/--latent-steps a smaller case for profiling")
+    ap.add_argument("--latent-shared", type=int, default=4096, help="latent path: shared prefix tokens")
+    ap.add_argument("--latent-private", type=int, default=28672, help="latent path: max private tokens")
+    ap.add_argument("--latent-steps", type=int, default=8, help="latent path: decode steps")
     return ap.parse_args()
 
 
@@ -287,7 +293,7 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
 
 
 # -------------------------------------------------------------------- main
-def latent_path(dev, hbm, bf16, peak_src, steps: int = 8):
+def latent_path(dev, hbm, bf16, peak_src, steps: int = 8, shared_len: int = 4096, private_max: int = 28672):
     """Latent (MLA) decode at its full configuration: 128 requests, a
     4,096-token shared prefix + U[0, 28,672] private tokens each, one
     576-wide latent head, 128 query heads.  The contexts are stored
@@ -302,7 +308,7 @@ def latent_path(dev, hbm, bf16, peak_src, steps: int = 8):
     from synth import traces
     from synth.model import SynthModel
 
-    tr = traces.mla_long(steps=steps)
+    tr = traces.mla_long(shared_len=shared_len, private_max=private_max, steps=steps)
     sh = tr.shape
     model = SynthModel(sh, tr.seed, tr.vocab, device=dev)
     eng = DeviceEngine(sh, tr.pool_slots, device=dev)
@@ -325,8 +331,8 @@ def latent_path(dev, hbm, bf16, peak_src, steps: int = 8):
         flops.append(ctx.sum() * 2 * sh.q_heads * (sh.head_dim_k + sh.head_dim_v))
     sec = sum(durs) / len(durs)
     u, lg, f = np.mean(uniq), np.mean(logical), np.mean(flops)
-    return {"config": "128 requests, 4096 shared + U[0,28672] private tokens, latent 576 (512+64), "
-                      "128 query heads, bf16; %d decode steps" % len(durs),
+    return {"config": "128 requests, %d shared + U[0,%d] private tokens, latent 576 (512+64), "
+                      "128 query heads, bf16; %d decode steps" % (shared_len, private_max, len(durs)),
             "us_per_step": sec * 1e6, "tokens_per_s": len(reqs) / sec,
             "unique_bytes": float(u), "logical_bytes": float(lg), "flops": float(f),
             "hbm": {"achieved_unique_gbs": u / sec / 1e9, "achieved_read_gbs": lg / sec / 1e9, "peak": hbm,
@@ -447,6 +453,11 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
+    if args.latent_only:
+        hbm, bf16, _, peak_src = peaks()
+        print(json.dumps(latent_path(dev, hbm, bf16, peak_src, steps=args.latent_steps,
+                                     shared_len=args.latent_shared, private_max=args.latent_private)), flush=True)
+        return
     import radixattention_prefix_shared_tree_gb300 as ra
     from radixattention_prefix_shared_tree_gb300 import workloads as wl
     from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
