@@ -210,10 +210,10 @@ def torch_empty_like(torch, t):
 # -------------------------------------------------------------- algorithmic
 # DRAM traffic of one attn_decode call over its algorithmic bytes, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum of the cascade and the
-# table-pass kernel) of this workload's decode steps 125 and 126: 211.76 MB and
-# 212.76 MB of DRAM traffic for 195.77 MB and 196.82 MB of algorithmic bytes.
+# table-pass kernel) of this workload's decode steps 125 and 126: 211.78 MB and
+# 212.95 MB of DRAM traffic for 195.77 MB and 196.82 MB of algorithmic bytes.
 # Traffic grows with the keys read, so the ratio scales it to the average call.
-DECODE_TRAFFIC_RATIO = 1.0813
+DECODE_TRAFFIC_RATIO = 1.0818
 
 
 def decode_bytes(lay, t, shape, stored=True):
