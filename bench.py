@@ -158,17 +158,73 @@ class ReplayModel:
         self.ready[tuple(r.rid for r in reqs)] = entry
         return entry
 
+    # e2e: steps whose inputs move host -> device in one copy (a chunk); the
+    # device holds two chunks, so chunk c+1 moves while chunk c computes
+    CHUNK = 8
+
     def to_host(self, key):
-        """e2e: keep this step's inputs in pinned host memory only."""
+        """e2e: keep this batch's inputs in pinned host memory only; the device
+        gets them chunk by chunk on a copy stream, one chunk ahead of use."""
+        torch = self.torch
         e = self.ready[key]
         pin = lambda t: t.cpu().pin_memory() if t is not None else None
         e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()},
                      "dec": {k: pin(v) for k, v in e["dec"].items()}}
-        e["ext"] = {k: (torch_empty_like(self.torch, v)) for k, v in e["ext"].items()}
-        e["dec_dev"] = {k: (torch_empty_like(self.torch, v[0]) if v is not None else None)
-                        for k, v in e["dec"].items()}
+        e["ext"] = {k: (torch_empty_like(torch, v)) for k, v in e["ext"].items()}
+        K = self.CHUNK
+        e["ring"] = {k: (torch.empty((2 * K,) + tuple(v.shape[1:]), dtype=v.dtype, device=v.device)
+                         if v is not None else None) for k, v in e["dec"].items()}
+        # the step inputs as views of the ring, built once (indexing a tensor
+        # costs host time on every decode step otherwise)
+        e["views"] = [{k: (ring[h] if ring is not None else None) for k, ring in e["ring"].items()}
+                      for h in range(2 * K)]
+        e["moved"] = {}          # chunk -> event on the copy stream (its copy is done)
+        e["ext_moved"] = None    # event: the prefill inputs are on the device
         e["dec"] = None
         e["dec_steps"] = None
+
+    def start_streams(self):
+        torch = self.torch
+        self.h2d = torch.cuda.Stream()
+        self.h2d_ext = torch.cuda.Stream()
+
+    def _move_chunk(self, e, c):
+        """Queue chunk c's decode inputs (steps cK..cK+K-1) into ring half c mod 2
+        on the copy stream, after the compute stream is done with chunk c-2."""
+        torch = self.torch
+        K = self.CHUNK
+        T = next(v for v in e["host"]["dec"].values() if v is not None).shape[0]
+        a, b = c * K, min(T, (c + 1) * K)
+        if a >= T:
+            return
+        free = torch.cuda.Event()
+        free.record(torch.cuda.current_stream())
+        self.h2d.wait_event(free)
+        with torch.cuda.stream(self.h2d):
+            for k, ring in e["ring"].items():
+                if ring is not None:
+                    src = e["host"]["dec"][k][a:b]
+                    ring[(c % 2) * K:(c % 2) * K + (b - a)].copy_(src, non_blocking=True)
+                    self.h2d_bytes += src.numel() * src.element_size()
+        ev = torch.cuda.Event()
+        ev.record(self.h2d)
+        e["moved"][c] = ev
+
+    def prefetch_extend(self, key):
+        """Queue a later batch's prefill inputs on their own copy stream (they
+        move while the current batch decodes)."""
+        torch = self.torch
+        e = self.ready[key]
+        if "host" not in e or e["ext_moved"] is not None:
+            return
+        with torch.cuda.stream(self.h2d_ext):
+            for k, v in e["ext"].items():
+                if v is not None:
+                    v.copy_(e["host"]["ext"][k], non_blocking=True)
+                    self.h2d_bytes += v.numel() * v.element_size()
+        ev = torch.cuda.Event()
+        ev.record(self.h2d_ext)
+        e["ext_moved"] = ev
 
     def _entry(self, batch):
         # the same list object is passed for every step of a batch: check it once
@@ -184,22 +240,22 @@ class ReplayModel:
     def extend_inputs(self, batch):
         e = self._entry(batch)
         if "host" in e:
-            for k, v in e["ext"].items():
-                if v is not None:
-                    v.copy_(e["host"]["ext"][k], non_blocking=True)
-                    self.h2d_bytes += v.numel() * v.element_size()
+            key = tuple(r.rid for r in batch)
+            self.prefetch_extend(key)
+            self.torch.cuda.current_stream().wait_event(e["ext_moved"])
         return e["ext"]
 
     def decode_inputs(self, batch, t):
         e = self._entry(batch)
         if "host" in e:
-            out = {}
-            for k, v in e["dec_dev"].items():
-                if v is not None:
-                    v.copy_(e["host"]["dec"][k][t], non_blocking=True)
-                    self.h2d_bytes += v.numel() * v.element_size()
-                out[k] = v
-            return out
+            K = self.CHUNK
+            c, i = divmod(t, K)
+            if i == 0:
+                if c not in e["moved"]:
+                    self._move_chunk(e, c)
+                self.torch.cuda.current_stream().wait_event(e["moved"][c])
+                self._move_chunk(e, c + 1)   # after the compute stream's chunk c-1
+            return e["views"][(c % 2) * K + i]
         return e["dec_steps"][t]
 
 
@@ -599,30 +655,80 @@ def main():
             model.to_host(key)
             keys.append(key)
         torch.cuda.synchronize()
-        sh = shape
+        # Inputs move host -> device on copy streams one chunk (8 steps) ahead,
+        # the next batch's prefill inputs during this batch's decode; outputs
+        # move device -> host on a third stream, a chunk at a time from a ring
+        # the decode steps write into (the ring half is reused only after its
+        # copy has finished).  Every byte of every step crosses inside the
+        # timed region; the copies overlap the kernels instead of queueing
+        # behind them.
+        model.start_streams()
+        d2h_stream = torch.cuda.Stream()
+        K = model.CHUNK
+        runner.decode_out_slots = 2 * K
         d2h = [0]
-        ext_host = {}
+        st = {"batch": 0, "done": [None, None]}
+        # pinned output buffers, allocated once before the timed region (a
+        # page-locked allocation costs milliseconds): the largest prefill
+        # output of these batches and one chunk of decode outputs
+        sh = shape
+        ext_rows = max(model.ready[k]["host"]["ext"]["q"].shape[0] for k in keys)
+        host_ext = torch.empty(ext_rows, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16).pin_memory()
+        host_dec = torch.empty(K, args.questions, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16).pin_memory()
 
-        def copy_out(out):
-            h = ext_host.get(out.shape)
-            if h is None:
-                h = ext_host[out.shape] = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-            h.copy_(out, non_blocking=True)
+        def after_compute():
+            ev = torch.cuda.Event()
+            ev.record(torch.cuda.current_stream())
+            d2h_stream.wait_event(ev)
+
+        def copy_extend(out):
+            after_compute()
+            with torch.cuda.stream(d2h_stream):
+                host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+            out.record_stream(d2h_stream)
             d2h[0] += out.numel() * out.element_size()
+            if st["batch"] + 1 < len(keys):
+                model.prefetch_extend(keys[st["batch"] + 1])
 
-        runner.on_decode = copy_out
-        runner.on_extend = copy_out
+        def copy_decode(out, t, n_steps):
+            if (t + 1) % K and t + 1 != n_steps:
+                return
+            c = t // K
+            outs = runner.decode_outs
+            a, m = (c % 2) * K, t - c * K + 1
+            after_compute()
+            with torch.cuda.stream(d2h_stream):
+                host_dec[:m].copy_(outs[a:a + m], non_blocking=True)
+            outs.record_stream(d2h_stream)
+            d2h[0] += m * out.numel() * out.element_size()
+            done = torch.cuda.Event()
+            done.record(d2h_stream)
+            st["done"][c % 2] = done
+            # chunk c+1 writes the other ring half: chunk c-1's copy must be done
+            prev = st["done"][(c + 1) % 2]
+            if prev is not None:
+                torch.cuda.current_stream().wait_event(prev)
+            if t + 1 == n_steps:
+                st["batch"] += 1
+                st["done"] = [None, None]
+
+        runner.on_decode = copy_decode
+        runner.on_extend = copy_extend
         model.h2d_bytes = 0
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
+        h0 = time.perf_counter()
         for s in range(n_main, n_main + n_e2e):
             step(batches[s])
+        torch.cuda.current_stream().wait_stream(d2h_stream)
         e1.record()
+        host_s = time.perf_counter() - h0   # time the host took to queue the work
         torch.cuda.synchronize()
         runner.on_decode = runner.on_extend = None
+        runner.decode_out_slots = 1
         ems = e0.elapsed_time(e1)
         if world > 1:
             t = torch.tensor([ems], device=dev)
@@ -630,7 +736,7 @@ def main():
             ems = float(t.item())
         e2e = {"value": n_e2e * args.questions * args.max_new * world / (ems / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": model.h2d_bytes // n_e2e, "d2h_bytes_per_step": d2h[0] // n_e2e,
-               "ms_per_step": ems / n_e2e}
+               "ms_per_step": ems / n_e2e, "host_queue_ms_per_step": 1e3 * host_s / n_e2e}
 
     cpu = None
     if rank == 0 and world == 1:

@@ -37,8 +37,10 @@ class Runner:
         self.decode_out = {}   # rid -> list of (position, out [Hq, dv], lse [Hq])
         self.next_rid = 0
         self.collect_rids = None  # collect only these requests' outputs (None: all)
-        self.on_decode = None   # optional callback(out) after each decode step
+        self.on_decode = None   # optional callback(out, t, n_steps) after each decode step
         self.on_extend = None   # optional callback(out) after the prefill
+        self.decode_out_slots = 1  # decode step t writes slot t mod this of `decode_outs`
+        self.decode_outs = None
 
     def request(self, prompt, max_new: int) -> Request:
         r = new_request(self.model, self.next_rid, prompt, max_new)
@@ -90,14 +92,18 @@ class Runner:
         self.last_layout = lay
         sh = eng.shape
         B = len(batch)
-        out = torch.empty(B, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
+        R = max(1, self.decode_out_slots)
+        outs = torch.empty(R, B, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
+        self.decode_outs = outs
+        views = [outs[i] for i in range(R)]
         lse = torch.empty(B, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
         eng.prepare_decode(lay)
         for t in range(lay.max_new):
+            out = views[t % R]
             inp = self.model.decode_inputs(batch, t)
             eng.decode_step(lay, t, inp["q"], inp["k"], inp["v"], out, lse)
             if self.on_decode is not None:
-                self.on_decode(out)
+                self.on_decode(out, t, lay.max_new)
             if self.collect:
                 if self.collect_rids is None:
                     idx = list(range(B))
