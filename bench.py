@@ -549,8 +549,12 @@ def main():
             raise RuntimeError("batch did not fit")
         return admitted
 
+    # a served batch is dropped at once, as a serving loop would: its slot
+    # rows' memory goes back to the allocator (fresh pages cost the next
+    # admission round page faults)
     for s in range(args.warmup):
         step(batches[s])
+        batches[s] = None
     torch.cuda.synchronize()
     assert ra.rc_sync(eng.err) == ra.RC_OK
 
@@ -588,6 +592,7 @@ def main():
     ev0.record()
     for s in range(args.warmup, n_main):
         step(batches[s])
+        batches[s] = None
     ev1.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
@@ -723,6 +728,7 @@ def main():
         h0 = time.perf_counter()
         for s in range(n_main, n_main + n_e2e):
             step(batches[s])
+            batches[s] = None
         torch.cuda.current_stream().wait_stream(d2h_stream)
         e1.record()
         host_s = time.perf_counter() - h0   # time the host took to queue the work
