@@ -295,6 +295,7 @@ class DeviceEngine:
     def __init__(self, shape, pool_slots: int, device="cuda", kv_fp8: bool = False):
         import torch
         self.torch = torch
+        self._lib = lib()    # raises if the library is missing
         self.shape = shape
         self.device = torch.device(device)
         self.kv_fp8 = bool(kv_fp8)
@@ -422,6 +423,7 @@ class DeviceEngine:
         dec_max = lay.dec_max.tolist() if T else []
         lay.ws_bytes = self._decode_ws(B, set(dec_max), casc)
         lay.ws = self.workspace(lay.ws_bytes)
+        lay.ws_ptr = lay.ws.data_ptr()
         lay.casc_ref = C.byref(casc) if casc is not None else None
         lay.slot_ptrs = [lay.decode_slots[t].data_ptr() for t in range(T)]
         # one table descriptor, its length row and bound set per step
@@ -466,7 +468,7 @@ class DeviceEngine:
         """One decode step: the new token's K/V goes into its slot and the
         step's attention runs -- fused into one call (attn_decode_append)
         for GQA pools, kv_store + attn_decode for the latent layout."""
-        L = lib()
+        L = self._lib
         B = lay.batch_size
         ev = None
         if self.timing and t % self.timing_every == 0:
@@ -478,7 +480,7 @@ class DeviceEngine:
         if self.fuse_store and v is not None:
             st = L.attn_decode_append(lay.desc_ref, q.data_ptr(), k.data_ptr(), v.data_ptr(), lay.kv_ref, B,
                                       lay.casc_ref, out.data_ptr(), lse.data_ptr() if lse is not None else None,
-                                      lay.ws.data_ptr(), lay.ws_bytes, lay.stream)
+                                      lay.ws_ptr, lay.ws_bytes, lay.stream)
             if st != RC_OK:
                 raise RCError("attn_decode_append", st)
             kernels = lay.decode_kernels
