@@ -68,6 +68,7 @@ def lib():
         L.oracle_attention.argtypes = [I64, VP, VP, VP, VP, VP, C.c_int, C.c_int, C.c_int, C.c_int,
                                        I64, I64, C.c_double, VP, VP]
         L.oracle_num_threads.restype = C.c_int
+        L.oracle_set_threads.argtypes = [C.c_int]
         _lib = L
     return _lib
 
@@ -148,6 +149,11 @@ class OracleTree:
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of later attention() calls (n <= 0: all the host's cores)."""
+    lib().oracle_set_threads(int(n))
 
 
 def attention(q, k, v, kv_off, ctx, q_heads, kv_heads, dk, dv, scale, latent=False):

@@ -73,6 +73,16 @@ int oracle_num_threads() {
 #endif
 }
 
+// Threads of later oracle_attention calls from this thread (n <= 0: all the
+// host's cores again); lets the caller time the oracle on one core too.
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 // Many query rows at once.  Query row r (q + r*Hq*dk) sees keys
 // kv_off[r] .. kv_off[r] + ctx[r] - 1 of the token-major arrays
 // k [tokens][Hkv][dk] and v [tokens][Hkv][dv] (v may alias k with
