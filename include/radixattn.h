@@ -438,6 +438,17 @@ rc_status rc_sync(rc_stream_t stream, int32_t* err);
 /* Static string for a status. */
 const char* rc_strerror(rc_status status);
 
+/* Self-test of the failure path every kernel's waits share (the pages have no
+ * counterpart: this is how a device wait that never completes is reported
+ * without faulting the GPU).  Launches one warp on `stream` that waits, with
+ * the same bounded mbarrier wait the kernels use, on a barrier nothing ever
+ * arrives at; after about a second the wait gives up and the warp ORs the
+ * timeout bit into `err` (device int32, caller-owned) and returns, so the
+ * context stays usable.  A following rc_sync(stream, err) returns
+ * RC_ERR_TIMEOUT and clears the word.  Errors: RC_ERR_ARG (err NULL),
+ * RC_ERR_CUDA (launch failed). */
+rc_status rc_probe_wait_timeout(int32_t* err, rc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

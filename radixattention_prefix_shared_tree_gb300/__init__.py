@@ -93,6 +93,7 @@ SIGNATURES = {
     "attn_extend_workspace": (I32, [P(rc_attn_desc), I32, I32, I32, P(C.c_size_t)]),
     "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
     "rc_sync": (I32, [VP, VP]),
+    "rc_probe_wait_timeout": (I32, [VP, VP]),
     "rc_strerror": (C.c_char_p, [I32]),
     "rc_image_key": (I32, [VP, I64, I32, VP]),
     "bc_create": (I32, [I64, I32, P(VP)]),
@@ -521,3 +522,9 @@ def attn_extend(desc: rc_attn_desc, q, qo_indptr, kv: rc_kv_table, batch: int, m
 
 def rc_sync(err=None, stream=None) -> int:
     return lib().rc_sync(_stream(stream), _tp(err))
+
+
+def rc_probe_wait_timeout(err, stream=None) -> int:
+    """Launch the bounded-wait self-test (see the header); rc_sync(err) then
+    returns RC_ERR_TIMEOUT."""
+    return lib().rc_probe_wait_timeout(_tp(err), _stream(stream))

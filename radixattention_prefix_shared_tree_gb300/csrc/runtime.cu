@@ -2,6 +2,7 @@
 // device error word, and the cached SM count used to size grids.
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace rc_host {
 
@@ -18,6 +19,30 @@ int sm_count() {
 }
 
 }  // namespace rc_host
+
+namespace {
+
+// One warp waits, with the bounded mbarrier wait every kernel here uses, on a
+// barrier that no thread ever arrives at.  When the wait gives up (about a
+// second) the warp ORs the timeout bit into the error word and leaves.
+__global__ void __launch_bounds__(32) wait_probe_kernel(int32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        tc::mbar_init(&bar, 1);
+        tc::fence_mbar_init();
+    }
+    __syncwarp();
+    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(&bar, 0, 1u << 24));
+    if (!ok && threadIdx.x == 0) rc::flag_error(err, rc::kErrTimeout);
+}
+
+}  // namespace
+
+extern "C" rc_status rc_probe_wait_timeout(int32_t* err, rc_stream_t stream) {
+    if (!err) return RC_ERR_ARG;
+    wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(err);
+    return rc_host::launch_status(cudaGetLastError());
+}
 
 extern "C" rc_status rc_sync(rc_stream_t stream, int32_t* err) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -52,6 +52,7 @@ def test_strerror_and_argument_checks(built):
     assert L.attn_extend(None, None, None, None, 0, 0, None, None, None, 0, None) == ra.RC_ERR_ARG
     n = C.c_size_t(0)
     assert L.attn_decode_workspace(None, 1, 1, None, C.byref(n)) == ra.RC_ERR_ARG
+    assert L.rc_probe_wait_timeout(None, None) == ra.RC_ERR_ARG
     h = C.c_void_p()
     assert L.rc_create(-1, C.byref(h)) == ra.RC_ERR_ARG
     assert L.rc_create(10, None) == ra.RC_ERR_ARG
