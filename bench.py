@@ -11,8 +11,15 @@ rc_insert of prompt + outputs and
 rc_release.  Every step serves a new batch of questions (inputs already in
 HBM, ~0.55 GB per step, larger than L2).
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
-instead, on a bounded sample of the same workload.
+Prints one JSON line (rank 0): ``value`` with the inputs resident in HBM;
+``e2e`` with every step's inputs moved from pinned host memory and its outputs
+read back inside the timed region (on copy streams, overlapping the kernels);
+``roofline`` of the dominant entry point against the measured peaks;
+``cpu_baseline`` the oracle on the host cores (all of them, and one);
+per-kernel rates and, unless ``--no-paths``, the latent (MLA) decode path, the
+FP8 pool and the host tree calls.  ``--latent-only`` runs just the latent path
+(smaller with ``--latent-shared/--latent-private``).  ``--impl reference``
+times the CPU oracle instead, on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
