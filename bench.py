@@ -385,6 +385,25 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
             "value_one_core": n_dec_total / est1, "est_s_per_step": est}
 
 
+# ---------------------------------------------------------------- replicas
+def slowest_rank(ms: float, world: int, device) -> float:
+    """The job's time over N replicas: every rank times the same region
+    (barriers on both sides) and the slowest one counts.  One all-reduce of
+    a scalar; no data moves between replicas."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units of all replicas per second of the slowest one (weak scaling)."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 # -------------------------------------------------------------------- main
 def latent_path(dev, hbm, bf16, peak_src, steps: int = 8, shared_len: int = 4096, private_max: int = 28672):
     """Latent (MLA) decode at its full configuration: 128 requests, a
@@ -644,17 +663,13 @@ def main():
         dist.barrier()
     clk = clocks.stop()
     eng.timing = False
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank(ev0.elapsed_time(ev1), world, dev)
     launches = eng.launches - launches0
     st1 = cache.stats()
     assert ra.rc_sync(eng.err) == ra.RC_OK
 
     tokens = args.steps * args.questions * args.max_new
-    value = tokens * world / (ms / 1e3)
+    value = whole_job_rate(tokens, world, ms)
 
     # per-call durations (events on the launching stream)
     hbm, bf16, bf16_sus, peak_src = peaks()
@@ -781,12 +796,8 @@ def main():
         torch.cuda.synchronize()
         runner.on_decode = runner.on_extend = None
         runner.decode_out_slots = 1
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": n_e2e * args.questions * args.max_new * world / (ems / 1e3), "unit": UNIT,
+        ems = slowest_rank(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_rate(n_e2e * args.questions * args.max_new, world, ems), "unit": UNIT,
                "h2d_bytes_per_step": model.h2d_bytes // n_e2e, "d2h_bytes_per_step": d2h[0] // n_e2e,
                "ms_per_step": ems / n_e2e, "host_queue_ms_per_step": 1e3 * host_s / n_e2e}
 
