@@ -114,7 +114,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
         }
         return;
     }
-    if (p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout)) return;
+    // one decision for the whole CTA: the word can change between two
+    // threads' reads, and a CTA split here would stall at its first barrier
+    if (__syncthreads_or(p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout))) return;
     const int32_t* keys = p.table + row0 + k0;
     const int n_tiles = (count + TN - 1) / TN;
 

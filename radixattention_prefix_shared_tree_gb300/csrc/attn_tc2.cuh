@@ -145,8 +145,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             return;
         }
     }
-    // a wait gave up in an earlier CTA: the results are void, leave at once
-    if (p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout)) return;
+    // a wait gave up in an earlier CTA: the results are void, leave at once,
+    // all threads alike (the word can change between two threads' reads, and
+    // a CTA split here would stall at its first barrier)
+    if (__syncthreads_or(p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout))) return;
     const int n_tiles = (key_count + TN - 1) / TN;
     // query tiles with at least one valid row
     const int n_qt = min(QT, ((min(n_rows_tok - tok0, TPC) * G) + TM - 1) / TM);
