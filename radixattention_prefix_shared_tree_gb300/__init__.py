@@ -409,7 +409,11 @@ def _stream(stream):
 def make_pool_desc(k, v, err=None, mla: bool = False, head_dim_v: int | None = None, k_scale=None,
                    v_scale=None) -> rc_pool_desc:
     """Descriptor of a pool held in torch tensors: k [n_slots, Hkv, dk] (or [n_slots, dk] latent).
-    With k_scale / v_scale (fp32 [n_slots, Hkv]) the pool is FP8: k, v hold E4M3 codes (uint8)."""
+    With k_scale / v_scale (fp32 [n_slots, Hkv]) the pool is FP8: k, v hold E4M3 codes (uint8).
+    The kernels index the pool as dense row-major arrays, so every tensor must be contiguous."""
+    for name, t in (("k", k), ("v", v), ("k_scale", k_scale), ("v_scale", v_scale)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"make_pool_desc: {name} must be contiguous (dense row-major [n_slots, ...])")
     d = rc_pool_desc()
     d.k = k.data_ptr()
     d.v = v.data_ptr() if v is not None else None

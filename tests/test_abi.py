@@ -68,3 +68,20 @@ def test_host_calls_reject_bad_arguments(built):
     assert c.free([16]) == ra.RC_ERR_ARG
     assert c.sched_order(7, [[1]])[0] == ra.RC_ERR_ARG
     assert c.evict(-3)[0] == ra.RC_ERR_ARG
+
+
+def test_pool_descriptor_rejects_non_contiguous_tensors():
+    import pytest
+    import torch
+    k = torch.zeros(64, 8, 128, dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    d = ra.make_pool_desc(k, v)
+    assert (d.n_slots, d.kv_heads, d.head_dim_k, d.head_dim_v) == (64, 8, 128, 128)
+    head_major = torch.zeros(8, 64, 128, dtype=torch.bfloat16).permute(1, 0, 2)   # [n_slots, H, d] view
+    with pytest.raises(ValueError):
+        ra.make_pool_desc(head_major, v)
+    with pytest.raises(ValueError):
+        ra.make_pool_desc(k, head_major)
+    codes = torch.zeros(64, 8, 128, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        ra.make_pool_desc(codes, codes, k_scale=torch.zeros(8, 64).t(), v_scale=torch.zeros(64, 8))
