@@ -396,8 +396,14 @@ class BlockCache:
 
 # ---------------------------------------------------------------- device calls
 def _tp(t):
-    """Device pointer of a torch tensor (None -> NULL)."""
-    return None if t is None else C.c_void_p(t.data_ptr())
+    """Device pointer of a torch tensor (None -> NULL).  The kernels read and
+    write dense row-major arrays, so a strided view is refused rather than
+    misread."""
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(t.shape)} strides {t.stride()}")
+    return C.c_void_p(t.data_ptr())
 
 
 def _stream(stream):

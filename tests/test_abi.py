@@ -85,3 +85,15 @@ def test_pool_descriptor_rejects_non_contiguous_tensors():
     codes = torch.zeros(64, 8, 128, dtype=torch.uint8)
     with pytest.raises(ValueError):
         ra.make_pool_desc(codes, codes, k_scale=torch.zeros(8, 64).t(), v_scale=torch.zeros(64, 8))
+
+
+def test_device_calls_refuse_strided_views(built):
+    import pytest
+    import torch
+    q = torch.zeros(4, 32, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ra._tp(q[:, :8])
+    with pytest.raises(ValueError):
+        ra._tp(q.transpose(0, 1))
+    assert ra._tp(None) is None
+    assert ra._tp(q[1]).value == q[1].data_ptr()

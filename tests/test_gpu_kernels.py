@@ -522,8 +522,9 @@ def test_fp8_pool_rejected_where_unsupported(cuda):
     q = torch.zeros(2, 32, 128, dtype=torch.bfloat16, device=cuda)
     out = torch.empty_like(q)
     ws = torch.empty(1 << 20, dtype=torch.uint8, device=cuda)
+    kv_new = torch.zeros(2, 8, 128, dtype=torch.bfloat16, device=cuda)
     with pytest.raises(ra.RCError) as e:
-        ra.attn_decode_append(desc, q, q[:, :8], q[:, :8], kv, 2, out, None, ws)
+        ra.attn_decode_append(desc, q, kv_new, kv_new, kv, 2, out, None, ws)
     assert e.value.status == ra.RC_ERR_UNSUPPORTED
 
 
