@@ -70,7 +70,8 @@ typedef struct CUstream_st* rc_stream_t;  /* a cudaStream_t; NULL = legacy defau
 /* ------------------------------------------------------------------ host */
 
 /* Create a cache over a pool of `pool_slots` slots (ids 0..pool_slots-1), all
- * free.  `pool_slots` in [0, 2^31-1].  *out receives the handle.
+ * free [N49 s.4: the cache and the running requests share one pool of KV
+ * slots].  `pool_slots` in [0, 2^31-1].  *out receives the handle.
  * Errors: RC_ERR_ARG (bad size or null out), RC_ERR_NOMEM (host allocation). */
 rc_status rc_create(int64_t pool_slots, rc_cache** out);
 void rc_destroy(rc_cache* cache);
@@ -124,8 +125,9 @@ rc_status rc_evict(rc_cache* cache, int64_t n_tokens, int64_t* freed,
  * Errors: RC_ERR_ARG, RC_ERR_NOMEM (fewer than n free; nothing taken). */
 rc_status rc_alloc(rc_cache* cache, int64_t n, int32_t* out);
 
-/* Give caller-held slots back to the pool.  Errors: RC_ERR_ARG (id out of
- * range), RC_ERR_STATE (slot not held by the caller, or repeated). */
+/* Give caller-held slots back to the pool [N49 s.4: one shared pool; slots a
+ * request took and will not insert return to it].  Errors: RC_ERR_ARG (id out
+ * of range), RC_ERR_STATE (slot not held by the caller, or repeated). */
 rc_status rc_free(rc_cache* cache, const int32_t* slots, int64_t n);
 
 /* Serving order of n pending prompts [N49 s.5].  RC_FCFS: 0..n-1.
@@ -198,6 +200,9 @@ rc_status rc_cascade_plan(rc_cache* cache, const rc_node* nodes, int32_t n, int3
                           int64_t* n_seg_slots, int32_t* total_rows, int32_t* max_seg_len,
                           int32_t* max_seg_rows);
 
+/* Counters of the cache (a library extra: the pages define the hit rates
+ * these counts give [N49 s.6, SG evaluation], not an interface for them).
+ * Errors: RC_ERR_ARG (null cache or out). */
 typedef struct rc_stats_t {
     int64_t pool_slots, free_slots, caller_slots, tree_tokens, nodes;
     int64_t match_calls, match_tokens, match_hits, match_hit_tokens;
@@ -406,6 +411,8 @@ rc_status attn_decode_append(const rc_attn_desc* desc, const void* q, const void
  * attn_decode_workspace) returns RC_ERR_SCRATCH and launches nothing.
  * The first call on a device looks up that device's scratch address (with
  * the device current), so make the first call before any stream capture.
+ * The address is kept per device ordinal: it assumes the CUDA runtime's
+ * primary context of that device and no cudaDeviceReset afterwards.
  * All calls share the one array, which keeps the last call's contents (the
  * partials are written in full before they are read, so nothing needs
  * clearing): calls that can overlap on the GPU (other streams, other host
@@ -431,7 +438,8 @@ rc_status attn_extend(const rc_attn_desc* desc, const void* q, const int32_t* qo
                       float* lse, void* ws, size_t ws_bytes, rc_stream_t stream);
 
 /* Wait for `stream`, then read and clear the device error word `err` (may be
- * NULL).  Returns RC_ERR_DEVICE / RC_ERR_TIMEOUT if a kernel flagged one,
+ * NULL).  A library extra (the pages have no counterpart): it is how errors
+ * that kernels detect reach the host, since device calls return at enqueue.  Returns RC_ERR_DEVICE / RC_ERR_TIMEOUT if a kernel flagged one,
  * RC_ERR_CUDA if the stream reported an error, RC_OK otherwise. */
 rc_status rc_sync(rc_stream_t stream, int32_t* err);
 

@@ -62,6 +62,8 @@ def lib():
         L.oracle_alloc.argtypes = [VP, I64, VP]
         L.oracle_free.argtypes = [VP, VP, I64]
         L.oracle_sched_order.argtypes = [VP, C.c_int, VP, VP, I32, VP]
+        L.oracle_admit.argtypes = [VP, C.c_int, VP, VP, VP, I32, I32, VP, P(I32), VP, VP, VP, VP]
+        L.oracle_commit.argtypes = [VP, C.c_int, VP, VP, VP, I32, VP, VP]
         L.oracle_dump.restype = I64
         L.oracle_dump.argtypes = [VP, C.c_char_p, I64]
         L.oracle_stats.argtypes = [VP, VP]
@@ -145,6 +147,69 @@ class OracleTree:
         v = np.zeros(16, np.int64)
         lib().oracle_stats(self._h, _ptr(v))
         return dict(zip(STAT_FIELDS, (int(x) for x in v)))
+
+
+class OracleServer:
+    """The oracle's own scheduling round and commits (oracle_admit,
+    oracle_commit) over an OracleTree, with the method names a serving loop
+    calls: admit(pending, policy, max_batch) -> (admitted, waiting),
+    commit_prompts(batch), finish(batch).  Requests are any objects with
+    tokens (prompt followed by the generated tokens), prompt_len, max_new; it
+    sets matched, first, node and slots on the admitted ones."""
+
+    def __init__(self, tree: OracleTree):
+        self.cache = tree
+
+    @staticmethod
+    def _rows(reqs):
+        lens = np.fromiter((r.prompt_len for r in reqs), np.int64, len(reqs))
+        mnew = np.fromiter((r.max_new for r in reqs), np.int64, len(reqs))
+        toks = _i32(np.concatenate([np.asarray(r.tokens[:r.prompt_len + r.max_new], np.int32) for r in reqs])
+                    if reqs else [])
+        off = np.concatenate([[0], np.cumsum(lens + mnew)]).astype(np.int64)
+        return toks, lens, mnew, off
+
+    def admit(self, pending: list, policy: int = LPM, max_batch: int | None = None):
+        if not pending:
+            return [], []
+        n = len(pending)
+        toks, lens, mnew, off = self._rows(pending)
+        slots = np.zeros(max(int(off[-1]), 1), np.int32)
+        order = np.zeros(n, np.int32)
+        matched, first, node = np.zeros(n, np.int64), np.zeros(n, np.int64), np.zeros(n, np.int64)
+        cnt = C.c_int32(0)
+        st = lib().oracle_admit(self.cache._h, int(policy), _ptr(toks), _ptr(lens), _ptr(mnew), n, int(max_batch or 0),
+                                _ptr(order), C.byref(cnt), _ptr(matched), _ptr(first), _ptr(node), _ptr(slots))
+        if st != OK:
+            raise RuntimeError(f"oracle_admit returned {st}")
+        admitted = []
+        for i in order[:cnt.value].tolist():
+            r = pending[i]
+            r.matched, r.first, r.node = int(matched[i]), int(first[i]), int(node[i])
+            r.slots = slots[off[i]:off[i + 1]].copy()
+            admitted.append(r)
+        took = set(order[:cnt.value].tolist())
+        return admitted, [r for i, r in enumerate(pending) if i not in took]
+
+    def _commit(self, batch, mode):
+        if not batch:
+            return
+        toks, lens, mnew, off = self._rows(batch)
+        slots = _i32(np.concatenate([np.asarray(r.slots, np.int32) for r in batch]))
+        node = np.fromiter((r.node for r in batch), np.int64, len(batch))
+        st = lib().oracle_commit(self.cache._h, mode, _ptr(toks), _ptr(lens), _ptr(mnew), len(batch), _ptr(slots),
+                                 _ptr(node))
+        if st != OK:
+            raise RuntimeError(f"oracle_commit returned {st}")
+        for i, r in enumerate(batch):
+            r.slots = slots[off[i]:off[i + 1]].copy()
+            r.node = int(node[i])
+
+    def commit_prompts(self, batch: list):
+        self._commit(batch, 0)
+
+    def finish(self, batch: list):
+        self._commit(batch, 1)
 
 
 def num_threads() -> int:

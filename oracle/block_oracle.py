@@ -214,6 +214,78 @@ class OracleBlockCache:
         bisect.insort(self.free_list, s)
 
 
+class OracleBlockServer:
+    """The scheduling round and the commits of a serving loop over this block
+    cache, written out here as the radix oracle's oracle_admit and
+    oracle_commit state them (note 49, sections 4 and 5): order the prompts;
+    in that order match with a pin; a request that will decode starts at
+    min(matched, prompt_len - 1), a prefill-only one at matched; take slots
+    for the uncached part plus max_new, evicting the shortfall first when
+    fewer are free; a request that still does not fit drops its pin and ends
+    the round; max_batch (> 0) ends it too.  After prefill the prompt is
+    inserted (pinned if the request will decode) and the admission pin
+    dropped; at finish prompt + outputs are inserted unpinned and the pin
+    dropped.  Only whole blocks enter the cache, so the slots of a request's
+    partial last block go back to the pool when the request is done with
+    them (after prefill for a prefill-only request, else at finish)."""
+
+    def __init__(self, cache: OracleBlockCache):
+        self.cache = cache
+
+    def admit(self, pending: list, policy: int = 1, max_batch: int | None = None):
+        c = self.cache
+        st, order = c.sched_order(policy, [r.tokens[:r.prompt_len] for r in pending])
+        assert st == OK
+        admitted = []
+        for i in order.tolist():
+            if max_batch and len(admitted) >= max_batch:
+                break
+            r = pending[i]
+            st, m, mslots, node = c.match(r.tokens[:r.prompt_len], True)
+            assert st == OK
+            first = min(m, r.prompt_len - 1) if r.max_new > 0 else m
+            need = r.prompt_len - first + r.max_new
+            if len(c.free_list) < need:
+                c.evict(need - len(c.free_list))
+            st, new = c.alloc(need)
+            if st != OK:
+                assert c.release(node) == OK
+                break
+            r.matched, r.first, r.node = m, first, node
+            r.slots = _arr(list(mslots[:first]) + list(new))
+            admitted.append(r)
+        took = {id(r) for r in admitted}
+        return admitted, [r for r in pending if id(r) not in took]
+
+    def _done_with(self, r, n):
+        k = n % self.cache.B
+        if k:
+            assert self.cache.free(r.slots[n - k:n]) == OK
+
+    def commit_prompts(self, batch: list):
+        for r in batch:
+            L = r.prompt_len
+            st, present, node, canon = self.cache.insert(r.tokens[:L], r.slots[:L], r.max_new > 0)
+            assert st == OK
+            r.slots[:L] = canon
+            assert self.cache.release(r.node) == OK
+            r.node = node if r.max_new > 0 else -1
+            if r.max_new == 0:
+                self._done_with(r, L)
+
+    def finish(self, batch: list):
+        for r in batch:
+            if r.max_new == 0:
+                continue
+            n = r.prompt_len + r.max_new
+            st, present, node, canon = self.cache.insert(r.tokens[:n], r.slots[:n], False)
+            assert st == OK
+            r.slots[:n] = canon
+            assert self.cache.release(r.node) == OK
+            r.node = -1
+            self._done_with(r, n)
+
+
 def _arr(x):
     import numpy as np
     return np.asarray(x, dtype=np.int32)

@@ -355,6 +355,126 @@ int oracle_sched_order(void* h, int policy, const int32_t* flat_tokens, const in
     return O_OK;
 }
 
+// One scheduling round, in the order the pages give its steps:
+//  1. the pending prompts are ordered, longest cached prefix first or by
+//     arrival (note 49, section 5);
+//  2. in that order each request looks up its prompt and pins the matched
+//     path, since a running request holds its path (section 4);
+//  3. a request that will decode recomputes at least its last prompt token,
+//     so that one new token carries the query: its first computed position is
+//     min(matched, prompt_len - 1) (prefill-only requests start at matched);
+//  4. it needs slots for every position it will compute: the uncached prompt
+//     tail plus max_new decode tokens;
+//  5. when fewer slots are free, least-recently-used unpinned leaves are
+//     evicted for the shortfall (section 4: cache and running requests share
+//     one pool, eviction makes room);
+//  6. if the slots still cannot be had, the request drops its pin and the
+//     round ends there: no later request overtakes it; the round also ends
+//     when max_batch requests (> 0) are in.
+// Token rows: row i of the flat arrays starts at the sum over j < i of
+// prompt_len[j] + max_new[j] and holds the prompt (only the prompt is read
+// here).  slots row i receives the matched slots for positions [0, first)
+// and the new ones for [first, prompt_len + max_new).  out_order lists the
+// admitted requests in admission order.
+int oracle_admit(void* h, int policy, const int32_t* flat_tokens, const int64_t* prompt_len,
+                 const int64_t* max_new, int32_t n, int32_t max_batch, int32_t* out_order,
+                 int32_t* n_admitted, int64_t* matched, int64_t* first_pos, int64_t* node,
+                 int32_t* slots) {
+    Tree& t = *(Tree*)h;
+    if (n < 0 || !n_admitted || (n > 0 && (!prompt_len || !max_new || !out_order || !matched ||
+                                           !first_pos || !node || !slots)))
+        return O_ARG;
+    *n_admitted = 0;
+    std::vector<int64_t> row_off((size_t)n + 1, 0);
+    for (int32_t i = 0; i < n; ++i) {
+        if (prompt_len[i] < 0 || max_new[i] < 0 || (max_new[i] > 0 && prompt_len[i] == 0)) return O_ARG;
+        row_off[(size_t)i + 1] = row_off[(size_t)i] + prompt_len[i] + max_new[i];
+        node[i] = -1;
+        matched[i] = 0;
+        first_pos[i] = 0;
+    }
+    // step 1 (the ordering reads prompts only: gather them)
+    std::vector<int32_t> prompts;
+    for (int32_t i = 0; i < n; ++i)
+        prompts.insert(prompts.end(), flat_tokens + row_off[(size_t)i], flat_tokens + row_off[(size_t)i] + prompt_len[i]);
+    std::vector<int32_t> order((size_t)n);
+    int st = oracle_sched_order(h, policy, prompts.data(), prompt_len, n, order.data());
+    if (st != O_OK) return st;
+    int32_t count = 0;
+    for (int32_t k = 0; k < n; ++k) {
+        if (max_batch > 0 && count >= max_batch) break;
+        const int32_t i = order[(size_t)k];
+        const int32_t* tok = flat_tokens + row_off[(size_t)i];
+        const int64_t len = prompt_len[i];
+        // step 2
+        std::vector<int32_t> mslots((size_t)std::max<int64_t>(len, 1));
+        int64_t m = 0, nd = -1;
+        st = oracle_match(h, tok, len, 1, &m, mslots.data(), &nd);
+        if (st != O_OK) return st;
+        // steps 3 and 4
+        const int64_t first = max_new[i] > 0 ? std::min<int64_t>(m, len - 1) : m;
+        const int64_t need = len - first + max_new[i];
+        // step 5
+        const int64_t free_now = (int64_t)t.free_slots.size();
+        if (free_now < need) {
+            int64_t freed = 0, cnt = 0;
+            st = oracle_evict(h, need - free_now, &freed, nullptr, 0, &cnt);
+            if (st != O_OK) return st;
+        }
+        // step 6
+        std::vector<int32_t> fresh((size_t)std::max<int64_t>(need, 1));
+        st = oracle_alloc(h, need, fresh.data());
+        if (st == O_NOMEM) {
+            st = oracle_release(h, nd);
+            if (st != O_OK) return st;
+            break;
+        }
+        if (st != O_OK) return st;
+        int32_t* row = slots + row_off[(size_t)i];
+        for (int64_t j = 0; j < first; ++j) row[j] = mslots[(size_t)j];
+        for (int64_t j = 0; j < need; ++j) row[first + j] = fresh[(size_t)j];
+        matched[i] = m;
+        first_pos[i] = first;
+        node[i] = nd;
+        out_order[count++] = i;
+    }
+    *n_admitted = count;
+    return O_OK;
+}
+
+// The inserts around a batch's run (note 49, section 2: a prompt, once
+// computed, is in the tree so concurrent requests can share it; a finished
+// request's whole path, outputs included, stays cached).  Rows as in
+// oracle_admit, for the n requests of this call; node[i] is the pin the
+// request holds and is updated.
+//  mode 0, after prefill: insert the prompt with the row's slots (pinned if
+//    the request will decode), drop the admission pin, and take the tree's
+//    slots for the prompt (the caller's duplicates went back to the pool);
+//  mode 1, at finish (requests that decoded): insert prompt + generated
+//    tokens unpinned, drop the request's pin.
+int oracle_commit(void* h, int mode, const int32_t* flat_tokens, const int64_t* prompt_len,
+                  const int64_t* max_new, int32_t n, int32_t* slots, int64_t* node) {
+    if (n < 0 || (mode != 0 && mode != 1) || (n > 0 && (!flat_tokens || !prompt_len || !max_new || !slots || !node)))
+        return O_ARG;
+    int64_t off = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        const int64_t row_len = prompt_len[i] + max_new[i];
+        const int32_t* tok = flat_tokens + off;
+        int32_t* row = slots + off;
+        off += row_len;
+        if (mode == 1 && max_new[i] == 0) continue;
+        const int64_t len = mode == 0 ? prompt_len[i] : row_len;
+        const int pin = mode == 0 && max_new[i] > 0;
+        int64_t present = 0, nd = -1;
+        int st = oracle_insert(h, tok, row, len, pin, &present, &nd, row);
+        if (st != O_OK) return st;
+        st = oracle_release(h, node[i]);
+        if (st != O_OK) return st;
+        node[i] = pin ? nd : -1;
+    }
+    return O_OK;
+}
+
 // Text dump: one line per node in depth-first order, children by first token:
 // "id parent ref last_access ntok: tokens... | slots...".  Returns the length.
 int64_t oracle_dump(void* h, char* buf, int64_t cap) {

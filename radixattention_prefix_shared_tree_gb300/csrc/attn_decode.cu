@@ -4,20 +4,21 @@
 // section 2).  Memory-bound: every K/V row of the context is read once per KV
 // head per step, so the design goal is to stream rows at HBM speed.
 //
-//  1. split-K pass (flat): CTA = (key chunk, KV head, request).  The G query
-//     heads of the KV head share each K/V row (grouped-query head grouping).
-//     K/V rows are gathered by slot with 16-byte cp.async into a 3-stage
-//     shared-memory ring; the products run on mma.sync with the keys on the M
-//     side and the G heads on the N side (so G = 4 or 8 wastes at most half of
-//     an n8 tile instead of 12 of 16 rows), and P is moved from accumulator
-//     layout to operand layout in registers with movmatrix.  Each warp runs its
-//     own online softmax over a quarter of every tile; the four warps merge at
-//     the end.  Output: a normalised partial and its log-sum-exp per
-//     (request, head, chunk).
-//  2. cascade pass (optional): each shared prefix segment is read once for all
-//     requests below it (mq_attn.cuh), producing one more partial per
-//     (request, head) and segment.
-//  3. merge pass: per (request, head), combine all partials by log-sum-exp.
+//  1. cascade pass (when the batch shares prefixes): each shared segment is
+//     read once for all rows below it by the tcgen05 many-row kernel
+//     (attn_tc2.cuh), one partial per (row, head, segment, key chunk).
+//  2. table pass: one warp per item (request, KV head[, key chunk]).  The G
+//     query heads of the KV head share each K/V row (grouped-query head
+//     grouping).  Each warp gathers its keys by slot with 16-byte cp.async
+//     into its own two-stage ring of 16-key tiles; the products run on
+//     mma.sync with the keys on the M side and the G heads on the N side (so
+//     G = 4 or 8 wastes at most half of an n8 tile instead of 12 of 16 rows),
+//     and P moves from accumulator to operand layout with movmatrix.  With
+//     one chunk per row the warp's epilogue folds in the row's cascade
+//     partials and writes the output (fused); otherwise it writes a
+//     normalised partial and its log-sum-exp per (request, head, chunk).
+//  3. merge pass (split rows only): per (request, head), combine all
+//     partials by log-sum-exp.
 
 #include "attn_tc2.cuh"
 #include "common.cuh"
@@ -408,7 +409,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
         // (every chunk of every segment it reads; partial (e, c) of head h
         // sits at row (req_seg_pos[e] * Hq + h) * seg_chunks + c)
         int e0 = 0, n_parts = 0;
-        if (p.req_seg_indptr) {
+        // (none after a cascade kernel gave up on a bounded wait: unwritten)
+        if (p.req_seg_indptr && !(p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout))) {
             e0 = p.req_seg_indptr[b];
             n_parts = (p.req_seg_indptr[b + 1] - e0) * p.seg_chunks;
         }
@@ -506,19 +508,26 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
                                                    const float* __restrict__ seg_lse, int32_t seg_chunks,
                                                    const int32_t* __restrict__ req_seg_indptr,
                                                    const int32_t* __restrict__ req_seg_pos, int32_t q_heads,
+                                                   const int32_t* __restrict__ start, int64_t table_len,
                                                    __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                    int32_t* err) {
     constexpr int PER = D / 32;
     const int bh = blockIdx.x;
     const int b = bh / q_heads, h = bh % q_heads;
     const int lane = threadIdx.x;
-    int nc = (len[b] + chunk - 1) / chunk;
+    const int64_t row0 = start[b];
+    const int L = len[b];
+    // a row the split pass rejected (outside the table) wrote no partials
+    int nc = (row0 < 0 || L < 0 || row0 + L > table_len) ? 0 : (L + chunk - 1) / chunk;
     if (nc > n_chunks) {  // len[b] above the caller's max_len: the split pass skipped keys
         if (lane == 0 && h == 0) rc::flag_error(err, rc::kErrBadSlot);
         nc = n_chunks;
     }
-    const int s0 = req_seg_indptr ? req_seg_indptr[b] : 0;
-    const int ns = req_seg_indptr ? req_seg_indptr[b + 1] - s0 : 0;
+    // a cascade kernel that gave up on a bounded wait (or met the flag of an
+    // earlier one) left its partials unwritten: use none of them
+    const bool casc_ok = !(err && (*reinterpret_cast<volatile int32_t*>(err) & rc::kErrTimeout));
+    const int s0 = req_seg_indptr && casc_ok ? req_seg_indptr[b] : 0;
+    const int ns = req_seg_indptr && casc_ok ? req_seg_indptr[b + 1] - s0 : 0;
     float m = -INFINITY;
     for (int i = 0; i < ns; ++i)
         for (int c = 0; c < seg_chunks; ++c)
@@ -549,7 +558,7 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
     for (int j = 0; j < PER; ++j) out[(int64_t)bh * D + lane + 32 * j] = __float2bfloat16_rn(acc[j] * inv);
-    if (lse && lane == 0) lse[bh] = (m + log2f(wsum)) * rc::kLn2;
+    if (lse && lane == 0) lse[bh] = wsum > 0.f ? (m + log2f(wsum)) * rc::kLn2 : -INFINITY;
 }
 
 // ------------------------------------------------------------------ planning
@@ -605,7 +614,7 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     const size_t rows = (size_t)batch * d->q_heads;
     pl->tail_o = pl->fused ? 0 : align256(rows * pl->n_chunks * dv * sizeof(float));
     pl->tail_lse = pl->fused ? 0 : align256(rows * pl->n_chunks * sizeof(float));
-    const size_t srows = casc ? (size_t)casc->total_seg_rows * d->q_heads * pl->seg_chunks : 0;
+    const size_t srows = casc && casc->n_seg > 0 ? (size_t)casc->total_seg_rows * d->q_heads * pl->seg_chunks : 0;
     pl->seg_o = align256(srows * dv * sizeof(float));
     pl->seg_lse = align256(srows * sizeof(float));
     pl->total = pl->tail_o + pl->tail_lse + pl->seg_o + pl->seg_lse;
@@ -811,10 +820,12 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
     if (D == 128)
         merge_kernel<128><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                              pl.seg_chunks, ri, rp, desc->q_heads, o, lse, P.err);
+                                              pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o,
+                                              lse, P.err);
     else
         merge_kernel<64><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                             pl.seg_chunks, ri, rp, desc->q_heads, o, lse, P.err);
+                                             pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o,
+                                             lse, P.err);
     return rc_host::launch_status(cudaGetLastError());
 }
 
@@ -872,8 +883,9 @@ extern "C" rc_status attn_decode_static(const rc_attn_desc* desc, const void* q,
                                         rc_stream_t stream) {
     if (!desc || !kv || batch < 0) return RC_ERR_ARG;
     if (batch == 0) return RC_OK;
+    const rc_cascade* cc = casc && casc->n_seg > 0 ? casc : nullptr;  // as attn_decode plans it
     size_t need = 0;
-    rc_status s = attn_decode_workspace(desc, batch, kv->max_len, casc, &need);
+    rc_status s = attn_decode_workspace(desc, batch, kv->max_len, cc, &need);
     if (s != RC_OK) return s;
     if (need > (size_t)RC_STATIC_SCRATCH_BYTES) return RC_ERR_SCRATCH;
     void* ws = nullptr;

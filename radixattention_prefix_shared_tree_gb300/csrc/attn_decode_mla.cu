@@ -256,11 +256,17 @@ __global__ void __launch_bounds__(32) mla_merge_kernel(const Params p) {
     const int bh = blockIdx.x;
     const int b = bh / p.q_heads;
     const int lane = threadIdx.x;
-    int nc = (p.len[b] + p.chunk - 1) / p.chunk;
+    const int64_t row0 = p.start[b];
+    const int L = p.len[b];
+    // a row the split pass rejected (outside the table) wrote no partials
+    int nc = (row0 < 0 || L < 0 || row0 + L > p.table_len) ? 0 : (L + p.chunk - 1) / p.chunk;
     if (nc > p.n_chunks) {
         if (lane == 0 && bh % p.q_heads == 0) rc::flag_error(p.err, rc::kErrBadSlot);
         nc = p.n_chunks;
     }
+    // a split kernel that gave up on a bounded wait (or met the flag of an
+    // earlier one) left its partials unwritten: use none of them
+    if (p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout)) nc = 0;
     float m = -INFINITY;
     for (int c = 0; c < nc; ++c) m = fmaxf(m, p.part_lse[(int64_t)bh * p.n_chunks + c]);
     float acc[PER];

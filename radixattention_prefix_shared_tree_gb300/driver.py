@@ -133,7 +133,10 @@ class Scheduler:
             r.slots = np.concatenate([mslots[:first], new]).astype(np.int32)
             self._rec("admit", r.rid, tuple(int(x) for x in new[:4]), len(new))
             admitted.append(r)
-        return admitted, waiting
+        # the waiting requests keep their arrival order (the next round's
+        # longest-prefix-first order breaks ties by it), as rc_admit's caller does
+        took = {id(r) for r in admitted}
+        return admitted, [r for r in pending if id(r) not in took]
 
     # ---- native batch path: the same rules, one C call per round
     def _admit_native(self, pending, policy, max_batch):

@@ -24,8 +24,11 @@ def new_request(model, rid: int, prompt, max_new: int) -> Request:
 
 class Runner:
     def __init__(self, cache, model, engine=None, policy: int = RC_LPM, cascade: bool = True,
-                 collect: bool = False, prefill_attention: bool = True, log: list | None = None):
-        self.sched = Scheduler(cache, log)
+                 collect: bool = False, prefill_attention: bool = True, log: list | None = None,
+                 sched=None):
+        # sched: any object with admit / commit_prompts / finish (default: the
+        # driver's Scheduler over `cache`)
+        self.sched = sched if sched is not None else Scheduler(cache, log)
         self.cache = cache
         self.model = model
         self.engine = engine

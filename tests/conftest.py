@@ -38,3 +38,13 @@ def cuda(built):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Every attention comparison's count of elements above 1e-2 and the
+    largest excess (tests/tolerance.py records them)."""
+    mod = sys.modules.get("tests.tolerance")
+    if mod is None:
+        return
+    for line in mod.summary_lines():
+        terminalreporter.write_line(line)

@@ -190,20 +190,25 @@ def test_random_traces_bit_exact(built, seed, B, vocab, pool):
 
 
 def test_workload_host_trace_bit_exact(built):
-    """The multimodal workload (small) through the scheduler: every host
-    result equal, oracle block cache vs product block cache."""
+    """The multimodal workload (small): the oracle block cache served by the
+    oracle's own scheduling round (OracleBlockServer) against the product
+    block cache under the driver's scheduler; every admitted request's
+    matched length, first position and slot row, and the final statistics,
+    equal."""
+    from radixattention_prefix_shared_tree_gb300.driver import Scheduler
     tr = traces.multimodal(n_images=4, per_image=4, image_tokens=40, image_bytes=64, max_new=5)
-    logs = []
-    for make, key in ((lambda n: bo.OracleBlockCache(n, 16), bo.image_key),
-                      (lambda n: ra.BlockCache(n, 16), ra.rc_image_key)):
-        log = []
-        runner = wl.Runner(make(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"),
-                           engine=None, log=log)
-        wl.run_multimodal(runner, tr, key, batch=3)
-        logs.append((log, runner.cache.stats()))
-    assert logs[0] == logs[1]
-    st = logs[1][1]
+    outs = []
+    for oracle_side in (True, False):
+        cache = bo.OracleBlockCache(tr.pool_slots, 16) if oracle_side else ra.BlockCache(tr.pool_slots, 16)
+        sched = bo.OracleBlockServer(cache) if oracle_side else Scheduler(cache, [])
+        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), engine=None, sched=sched)
+        served = wl.run_multimodal(runner, tr, bo.image_key if oracle_side else ra.rc_image_key, batch=3)
+        outs.append(([(r.rid, r.matched, r.first, tuple(int(x) for x in r.slots)) for r in served],
+                     runner.cache.stats()))
+    assert outs[0] == outs[1]
+    st = outs[1][1]
     assert st["caller"] == 0  # every partial block went back
+    assert st["match_hit_tokens"] > 0 and st["evicted_nodes"] >= 0
 
 
 def test_host_api_errors(built):

@@ -28,14 +28,13 @@ def _check(runner, model, shape, rids, steps=None):
         if rid in runner.extend_out:
             pos, o, l = runner.extend_out[rid]
             pick = np.unique(np.linspace(0, len(pos) - 1, min(len(pos), 24)).astype(int))
-            ref, ref_l = oracle_positions(shape, h, pos[pick])
-            compare(o[pick], l[pick], ref, ref_l, stats)
+            compare(o[pick], l[pick], oracle_positions(shape, h, pos[pick]), stats)
         dec = runner.decode_out.get(rid, [])
         if steps is not None:
             dec = [d for i, d in enumerate(dec) if i in steps]
         if dec:
-            ref, ref_l = oracle_positions(shape, h, [p for p, _, _ in dec])
-            compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]), ref, ref_l, stats)
+            compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]),
+                    oracle_positions(shape, h, [p for p, _, _ in dec]), stats)
     assert stats["n"] > 0 and stats["sum"] / stats["n"] <= MEAN_ABS
     return stats
 
@@ -52,8 +51,10 @@ def _gpu_run(tr, fn, pool, cuda, rids, cascade=True):
 
 
 def _oracle_host(tr, fn, pool):
+    """The same trace through the oracle tree and the oracle's own
+    scheduling round and commits (none of the driver's code)."""
     tree = oracle.OracleTree(pool)
-    runner = wl.Runner(tree, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"))
+    runner = wl.Runner(tree, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), sched=oracle.OracleServer(tree))
     fn(runner, tr)
     return tree
 

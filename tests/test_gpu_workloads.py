@@ -20,40 +20,58 @@ from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
 from synth import hashgen as hg
 from synth import traces
 from synth.model import SynthModel
+from tests import tolerance as tol
 
 pytestmark = pytest.mark.gpu
 
-MAX_ABS, MEAN_ABS, LSE_ABS = 1e-2, 1e-3, 2e-3
+MAX_ABS, MEAN_ABS, LSE_ABS = tol.MAX_ABS, tol.MEAN_ABS, tol.LSE_ABS
 
 
 def oracle_positions(shape, hashes, positions, fp8=False):
-    """Oracle attention for query positions of one request (keys 0..pos).
+    """Oracle attention for query positions of one request (keys 0..pos):
+    (out, lse, A), A = the same attention over |V| (the bound's weight).
     fp8: K/V as an FP8 pool holds them (the oracle's own quantisation)."""
     n = int(max(positions)) + 1
     kb = hg.gen_values(hashes[:n], hg.KIND_K, shape.kv_heads, shape.head_dim_k)
     vb = None if shape.mla else hg.gen_values(hashes[:n], hg.KIND_V, shape.kv_heads, shape.head_dim_v)
     qb = hg.gen_values(hashes[np.asarray(positions)], hg.KIND_Q, shape.q_heads, shape.head_dim_k)
+    zeros, ctx = np.zeros(len(positions), np.int64), np.asarray(positions, np.int64) + 1
     if fp8:
         from oracle import fp8_oracle as f8
         kd = f8.dequantize(*f8.quantize_rows(kb.reshape(n, shape.kv_heads, -1)))
         vd = f8.dequantize(*f8.quantize_rows(vb.reshape(n, shape.kv_heads, -1)))
-        return f8.attention(qb.reshape(len(positions), shape.q_heads, -1), kd, vd, np.zeros(len(positions), np.int64),
-                            np.asarray(positions, np.int64) + 1, shape.q_heads, shape.kv_heads, shape.scale)
-    return oracle.attention(qb, kb, vb, np.zeros(len(positions), np.int64), np.asarray(positions, np.int64) + 1,
-                            shape.q_heads, shape.kv_heads, shape.head_dim_k, shape.head_dim_v, shape.scale,
-                            latent=shape.mla)
+        qr = qb.reshape(len(positions), shape.q_heads, -1)
+        out, lse = f8.attention(qr, kd, vd, zeros, ctx, shape.q_heads, shape.kv_heads, shape.scale)
+        a_abs, _ = f8.attention(qr, kd, np.abs(vd), zeros, ctx, shape.q_heads, shape.kv_heads, shape.scale)
+        return out, lse, a_abs
+    out, lse = oracle.attention(qb, kb, vb, zeros, ctx, shape.q_heads, shape.kv_heads, shape.head_dim_k,
+                                shape.head_dim_v, shape.scale, latent=shape.mla)
+    if shape.mla:   # V = the first head_dim_v columns of the latent row
+        k3 = kb.reshape(n, 1, shape.head_dim_k)
+        va = tol.abs_bits(k3[:, :, :shape.head_dim_v])
+        a_abs, _ = oracle.attention(qb, k3, va, zeros, ctx, shape.q_heads, 1, shape.head_dim_k, shape.head_dim_v,
+                                    shape.scale)
+    else:
+        a_abs, _ = oracle.attention(qb, kb, tol.abs_bits(vb), zeros, ctx, shape.q_heads, shape.kv_heads,
+                                    shape.head_dim_k, shape.head_dim_v, shape.scale)
+    return out, lse, a_abs
 
 
-def compare(out_bits, lse, ref, ref_lse, stats):
+def compare(out_bits, lse, refs, stats, fp8=False):
+    """Elementwise bound of tests/tolerance.py; the mean bound is checked by
+    the caller over all compared elements (stats)."""
+    ref, ref_lse, a_abs = refs
     got = hg.bf16_bits_to_f32(out_bits).astype(np.float64)
-    err = np.abs(got - ref)
+    err = tol.check_values(got, ref, a_abs, u_p=tol.U_F16 if fp8 else tol.U_BF16, mean=np.inf,
+                           label="fp8" if fp8 else "out")
     stats["max"] = max(stats.get("max", 0.0), float(err.max()))
     stats["sum"] = stats.get("sum", 0.0) + float(err.sum())
     stats["n"] = stats.get("n", 0) + err.size
-    # bf16 outputs: 1e-2, or one bf16 ulp of the exact value where larger
-    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -126))) - 7)
-    assert (err <= np.maximum(MAX_ABS, ulp)).all()
-    assert np.abs(lse.astype(np.float64) - ref_lse).max() <= LSE_ABS
+    tol.check_lse(lse, ref_lse)
+
+
+def _rows(reqs):
+    return sorted((r.rid, r.matched, r.first, tuple(int(x) for x in r.slots)) for r in reqs)
 
 
 def run(trace, runner_fn, pool, cuda, cascade=True, policy=ra.RC_LPM, cache_cls=ra.RadixCache, kv_fp8=False, **kw):
@@ -73,15 +91,14 @@ def check_requests(runner, model, rids, shape, stats, max_decode_steps=None, fp8
         h = model.hashes(rid)
         if rid in runner.extend_out:
             pos, o, l = runner.extend_out[rid]
-            ref, ref_l = oracle_positions(shape, h, pos, fp8)
-            compare(o, l, ref, ref_l, stats)
+            compare(o, l, oracle_positions(shape, h, pos, fp8), stats, fp8)
         dec = runner.decode_out.get(rid, [])
         if max_decode_steps is not None:
             dec = [d for i, d in enumerate(dec) if i in max_decode_steps]
         if dec:
             pos = [p for p, _, _ in dec]
-            ref, ref_l = oracle_positions(shape, h, pos, fp8)
-            compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]), ref, ref_l, stats)
+            compare(np.stack([o for _, o, _ in dec]), np.stack([l for _, _, l in dec]),
+                    oracle_positions(shape, h, pos, fp8), stats, fp8)
 
 
 def test_tiny_config_all_outputs_vs_oracle(cuda):
@@ -90,12 +107,13 @@ def test_tiny_config_all_outputs_vs_oracle(cuda):
     stats = {}
     check_requests(runner, model, [r.rid for r in reqs], tr.shape, stats)
     assert stats["sum"] / stats["n"] <= MEAN_ABS
-    # the same trace through the oracle tree: identical host results
-    olog = []
-    orunner = wl.Runner(oracle.OracleTree(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"),
-                        log=olog)
-    wl.run_tiny(orunner, tr)
-    assert olog == log
+    # the same trace through the oracle tree and the oracle's own scheduling
+    # round: every request's match, first position and slot row, and the tree
+    ot = oracle.OracleTree(tr.pool_slots)
+    orunner = wl.Runner(ot, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), sched=oracle.OracleServer(ot))
+    oreqs = wl.run_tiny(orunner, tr)
+    assert _rows(oreqs) == _rows(reqs)
+    assert ot.dump() == cache.dump() and ot.stats() == cache.stats()
 
 
 def test_few_shot_reduced_cascade_and_flat(cuda):
@@ -199,11 +217,16 @@ def test_multimodal_image_keys_vs_oracle(cuda, cache_kind):
     assert stats["sum"] / stats["n"] <= MEAN_ABS
     # later questions about an image reuse its run
     assert cache.stats()["match_hit_tokens"] > len(reqs) * len(tr.system)
-    omake = oracle.OracleTree if cache_kind == "radix" else (lambda n: bo.OracleBlockCache(n, 16))
-    olog = []
-    orunner = wl.Runner(omake(tr.pool_slots), SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=olog)
-    wl.run_multimodal(orunner, tr, bo.image_key, batch=4)
-    assert olog == log
+    # the oracle cache with the oracle's own scheduling round
+    if cache_kind == "radix":
+        oc = oracle.OracleTree(tr.pool_slots)
+        osched = oracle.OracleServer(oc)
+    else:
+        oc = bo.OracleBlockCache(tr.pool_slots, 16)
+        osched = bo.OracleBlockServer(oc)
+    orunner = wl.Runner(oc, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), sched=osched)
+    oreqs = wl.run_multimodal(orunner, tr, bo.image_key, batch=4)
+    assert _rows(oreqs) == _rows(reqs) and oc.stats() == cache.stats()
 
 
 @pytest.mark.parametrize("cascade", [True, False])

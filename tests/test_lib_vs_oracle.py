@@ -12,6 +12,7 @@ import pytest
 import oracle
 import radixattention_prefix_shared_tree_gb300 as ra
 from radixattention_prefix_shared_tree_gb300 import workloads as wl
+from radixattention_prefix_shared_tree_gb300.driver import Scheduler
 from synth import traces
 from synth.model import SynthModel
 from tests import scenarios as sc
@@ -59,108 +60,141 @@ def test_cyclic_trace_same_log(built, grouped):
     assert hits == (5 if grouped else 0)
 
 
-def _host_run(make_cache, trace_fn, runner_fn, seed, vocab, shape, pool, policy=ra.RC_LPM):
-    cache = make_cache(pool)
-    log = []
-    model = SynthModel(shape, seed, vocab, device="cpu")
-    runner = wl.Runner(cache, model, engine=None, policy=policy, log=log)
-    res = runner_fn(runner, trace_fn())
-    return log, cache.dump(), cache.stats(), res
+class Recorder:
+    """Wraps a scheduling object: records every round's admitted requests in
+    admission order (rid, matched, first position, pinned node, slot row) and
+    the waiting ones, every commit's nodes and slot rows, and the cache's
+    statistics (and, with dumps=True, its full dump) after each commit."""
+
+    def __init__(self, sched, cache, dumps=True):
+        self.sched, self.cache, self.dumps, self.rec = sched, cache, dumps, []
+
+    def _state(self):
+        return self.cache.dump() if self.dumps else tuple(sorted(self.cache.stats().items()))
+
+    def admit(self, pending, policy, max_batch=None):
+        a, w = self.sched.admit(pending, policy, max_batch)
+        self.rec.append(("admit", [(r.rid, r.matched, r.first, r.node, tuple(int(x) for x in r.slots)) for r in a],
+                         sorted(r.rid for r in w)))
+        return a, w
+
+    def commit_prompts(self, batch):
+        self.sched.commit_prompts(batch)
+        self.rec.append(("prefill", [(r.rid, r.node, tuple(int(x) for x in r.slots[:r.prompt_len])) for r in batch],
+                         self._state()))
+
+    def finish(self, batch):
+        self.sched.finish(batch)
+        self.rec.append(("finish", [(r.rid, r.node, tuple(int(x) for x in r.slots)) for r in batch], self._state()))
+
+
+def _served(kind, trace_fn, runner_fn, pool, policy=ra.RC_LPM, dumps=True):
+    """One host run of a workload.  kind: "oracle" (the oracle tree with the
+    oracle's own admission round and commits), "native" (the library's
+    rc_admit / rc_commit), "per_call" (the driver's per-call scheduler over
+    the library's tree)."""
+    tr = trace_fn()
+    if kind == "oracle":
+        cache = oracle.OracleTree(pool(tr))
+        inner = oracle.OracleServer(cache)
+    else:
+        cache = ra.RadixCache(pool(tr))
+        inner = Scheduler(cache, None if kind == "native" else [])
+    rec = Recorder(inner, cache, dumps)
+    runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), policy=policy, sched=rec)
+    res = runner_fn(runner, tr)
+    return rec.rec, cache.dump(), cache.stats(), res
+
+
+def _three_way(trace_fn, runner_fn, pool, policy=ra.RC_LPM, dumps=True):
+    """The oracle's admission round against the library's native batch path
+    and the driver's per-call path: every round's records identical."""
+    outs = {k: _served(k, trace_fn, runner_fn, pool, policy, dumps) for k in ("oracle", "native", "per_call")}
+    for k in ("native", "per_call"):
+        a, b = outs["oracle"], outs[k]
+        assert len(a[0]) == len(b[0]), k
+        for i, (x, y) in enumerate(zip(a[0], b[0])):
+            assert x == y, f"{k}: record {i} ({x[0]}) differs"
+        assert a[1] == b[1] and a[2] == b[2], k
+    return outs["oracle"]
 
 
 def test_tiny_workload_host_trace(built):
     tr = traces.tiny()
-    outs = [_host_run(m, traces.tiny, wl.run_tiny, tr.seed, tr.vocab, tr.shape, tr.pool_slots)
-            for m in (oracle.OracleTree, ra.RadixCache)]
-    assert outs[0][:3] == outs[1][:3]
-    st = outs[1][2]
+    rec, dump, st, res = _three_way(traces.tiny, wl.run_tiny, lambda t: t.pool_slots)
     # every request after the first finds the 32-token system prompt
     assert st["match_hits"] == len(tr.prompts) - 1
 
 
 @pytest.mark.parametrize("policy", [ra.RC_LPM, ra.RC_FCFS])
 def test_few_shot_workload_host_trace(built, policy):
-    small = lambda: traces.few_shot(n_questions=64, max_new=16)
-    tr = small()
-    outs = [_host_run(m, small, wl.run_few_shot, tr.seed, tr.vocab, tr.shape, 1 << 16, policy)
-            for m in (oracle.OracleTree, ra.RadixCache)]
-    assert outs[0][:3] == outs[1][:3]
-    st = outs[1][2]
-    assert st["match_hit_tokens"] == 64 * len(tr.warm)
+    rec, dump, st, res = _three_way(lambda: traces.few_shot(n_questions=64, max_new=16), wl.run_few_shot,
+                                    lambda t: 1 << 16, policy)
+    assert st["match_hit_tokens"] == 64 * len(traces.few_shot(n_questions=1).warm)
 
 
 def test_chat_workload_host_trace_with_eviction(built):
-    small = lambda: traces.chat(n_sessions=24, n_turns=5, umin=16, umax=64, max_new=16)
-    tr = small()
-    tr.max_batch = 8
-    outs = []
-    for make in (oracle.OracleTree, ra.RadixCache):
-        cache = make(tr.pool_slots)
-        log = []
-        model = SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu")
-        runner = wl.Runner(cache, model, log=log)
-        served, rounds = wl.run_chat(runner, tr)
-        outs.append((log, cache.dump(), cache.stats(), rounds))
-    assert outs[0] == outs[1]
-    st = outs[1][2]
+    def small():
+        tr = traces.chat(n_sessions=24, n_turns=5, umin=16, umax=64, max_new=16)
+        tr.max_batch = 8
+        return tr
+    rec, dump, st, (served, rounds) = _three_way(small, wl.run_chat, lambda t: t.pool_slots)
     assert st["evicted_nodes"] > 0          # the pool holds 75% of the working set
     assert st["match_hits"] > 0
+    # some rounds stopped at a request that did not fit (the first misfit rule)
+    assert any(r[0] == "admit" and r[2] for r in rec)
+
+
+def test_chat_admission_misfit_stops_round(built):
+    """A pool so small that most rounds end at a misfit after evicting: the
+    shortfall eviction and the no-overtaking rule, round by round."""
+    def tight():
+        tr = traces.chat(n_sessions=12, n_turns=4, umin=40, umax=90, max_new=24)
+        tr.pool_slots = 700
+        return tr
+    rec, dump, st, (served, rounds) = _three_way(tight, wl.run_chat, lambda t: t.pool_slots)
+    stops = sum(1 for r in rec if r[0] == "admit" and r[2])
+    assert stops >= 3 and st["evicted_nodes"] > 0
 
 
 def test_agent_tree_host_trace(built):
-    small = lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8)
-    tr = small()
-    outs = [_host_run(m, small, wl.run_agent, tr.seed, tr.vocab, tr.shape, 4096)
-            for m in (oracle.OracleTree, ra.RadixCache)]
-    assert outs[0][:3] == outs[1][:3]
+    _three_way(lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8), wl.run_agent, lambda t: 4096)
 
 
 def test_full_chat_host_trace_bit_exact(built):
     """The chat workload at full size (256 sessions x 8 turns, pool = 75% of
-    the working set): eviction log, hits and final tree identical."""
-    tr = traces.chat()
-    outs = []
-    for make in (oracle.OracleTree, ra.RadixCache):
-        cache = make(tr.pool_slots)
-        log = []
-        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=log)
-        served, rounds = wl.run_chat(runner, tr)
-        outs.append((log, cache.stats(), rounds))
-    assert outs[0] == outs[1]
-    assert outs[1][1]["evicted_tokens"] > 0
+    the working set): every round's admissions, slots, evictions (through the
+    statistics after each commit) and the final tree identical."""
+    rec, dump, st, (served, rounds) = _three_way(traces.chat, wl.run_chat, lambda t: t.pool_slots, dumps=False)
+    assert st["evicted_tokens"] > 0 and rounds >= 8
 
 
-def _native_vs_per_call(trace_fn, runner_fn, pool):
-    """The scheduler's native batch path (rc_admit / rc_commit) against its
-    per-call path (which the tests above pin to the oracle)."""
-    out = []
-    for log in (None, []):
-        tr = trace_fn()
-        cache = ra.RadixCache(pool(tr))
-        runner = wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), log=log)
-        res = runner_fn(runner, tr)
-        reqs = res[0] if isinstance(res, tuple) else res
-        rows = sorted((r.rid, r.matched, r.first, tuple(int(x) for x in r.slots)) for r in reqs)
-        out.append((cache.dump(), cache.stats(), rows))
-    assert out[0] == out[1]
+def test_fully_cached_prompt_recomputes_last_token(built):
+    """The reading that a request whose whole prompt is cached and that will
+    decode recomputes its last prompt token (one new token carries the
+    query), while a prefill-only request computes nothing: fixed by hand on
+    the oracle's round, then the library's rounds equal it."""
+    t = oracle.OracleTree(64)
+    srv = oracle.OracleServer(t)
 
+    class R:
+        def __init__(self, rid, toks, plen, mnew):
+            self.rid, self.tokens, self.prompt_len, self.max_new = rid, np.asarray(toks, np.int32), plen, mnew
+            self.node, self.slots = -1, None
 
-def test_native_batch_scheduler_equals_per_call_few_shot(built):
-    _native_vs_per_call(lambda: traces.few_shot(n_questions=40, max_new=8), wl.run_few_shot, lambda tr: 1 << 15)
-
-
-def test_native_batch_scheduler_equals_per_call_chat_with_eviction(built):
-    def small():
-        tr = traces.chat(n_sessions=20, n_turns=4, umin=16, umax=64, max_new=16)
-        tr.max_batch = 7
-        return tr
-    _native_vs_per_call(small, wl.run_chat, lambda tr: tr.pool_slots)
-
-
-def test_native_batch_scheduler_equals_per_call_tiny_and_agent(built):
-    _native_vs_per_call(traces.tiny, wl.run_tiny, lambda tr: tr.pool_slots)
-    _native_vs_per_call(lambda: traces.agent_tree(root_len=64, branch_len=8, max_new=8), wl.run_agent,
-                        lambda tr: 4096)
+    a = R(0, [5, 6, 7, 8], 4, 0)
+    adm, _ = srv.admit([a], ra.RC_FCFS)
+    assert adm == [a] and (a.matched, a.first) == (0, 0) and list(a.slots) == [0, 1, 2, 3]
+    srv.commit_prompts([a])
+    b = R(1, [5, 6, 7, 8, 50, 51], 4, 2)       # prompt fully cached, decodes 2
+    c = R(2, [5, 6, 7, 8], 4, 0)               # prompt fully cached, prefill only
+    adm, _ = srv.admit([b, c], ra.RC_FCFS)
+    assert (b.matched, b.first) == (4, 3) and list(b.slots) == [0, 1, 2, 4, 5, 6]
+    assert (c.matched, c.first) == (4, 4) and list(c.slots) == [0, 1, 2, 3]
+    srv.commit_prompts([b, c])
+    assert list(b.slots[:4]) == [0, 1, 2, 3]    # slot 4 duplicated position 3 and was freed
+    srv.finish([b, c])
+    assert t.stats()["free"] == 64 - 6 and t.stats()["insert_dup_freed"] == 1
 
 
 @pytest.mark.parametrize("which", ["few_shot", "agent"])
@@ -197,3 +231,35 @@ def test_tree_cascade_plan_equals_slot_row_plan(built, which):
     for b in range(len(admitted)):   # the inverse map lists row b's entries
         pos = plan["req_seg_pos"][plan["req_seg_indptr"][b]:plan["req_seg_indptr"][b + 1]]
         assert all(plan["seg_rows"][p] == b for p in pos)
+
+
+def test_admission_evicts_shortfall_and_misfit_stops(built):
+    """Eviction for room and the first-misfit rule, fixed by hand on the
+    oracle's round (note 49, section 4: evict least-recently-used unpinned
+    leaves to make room in the shared pool; section 5 serving order), then
+    the library's native round must give the same."""
+    class R:
+        def __init__(self, rid, toks, mnew=0):
+            self.rid, self.tokens, self.prompt_len, self.max_new = rid, np.asarray(toks, np.int32), len(toks) - mnew, mnew
+            self.node, self.slots = -1, None
+
+    results = []
+    for kind in ("oracle", "native"):
+        cache = oracle.OracleTree(10) if kind == "oracle" else ra.RadixCache(10)
+        srv = oracle.OracleServer(cache) if kind == "oracle" else Scheduler(cache)
+        for rid, toks in ((0, [1, 2, 3]), (1, [4, 5, 6, 7])):      # two cached leaves, A older than B
+            r = R(rid, toks)
+            adm, _ = srv.admit([r], ra.RC_FCFS)
+            srv.commit_prompts(adm)
+            srv.finish(adm)
+        c, d, e = R(2, [9] * 5), R(3, [8] * 6), R(4, [7])
+        adm, wait = srv.admit([c, d, e], ra.RC_FCFS)
+        results.append(([r.rid for r in adm], [r.rid for r in wait], list(c.slots), cache.stats(), cache.dump()))
+    o = results[0]
+    # C needs 5 with 3 free: evicts the shortfall (2) = leaf A (3 slots), takes the 5 smallest free ids
+    assert o[0] == [2] and o[2] == [0, 1, 2, 7, 8]
+    # D needs 6 with 1 free: evicts B (4), still short, no candidate left: unpinned, round ends;
+    # E would fit now but does not overtake D
+    assert o[1] == [3, 4]
+    assert o[3]["evicted_nodes"] == 2 and o[3]["free"] == 5 and o[3]["caller"] == 5 and o[3]["pins"] == 1
+    assert results[1] == o
