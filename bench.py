@@ -51,9 +51,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="few_shot", choices=["few_shot", "chat", "agent", "mla"],
+                    help="workload: few_shot (the default line) or one of the other configurations")
     ap.add_argument("--policy", default="lpm", choices=["lpm", "fcfs"])
     ap.add_argument("--no-cascade", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-overlap", dest="overlap", action="store_false",
+                    help="serve batch by batch (no host work for batch k+1 during batch k's decode)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle sample")
     ap.add_argument("--questions", type=int, default=N_QUESTIONS)
     ap.add_argument("--max-new", type=int, default=MAX_NEW)
@@ -152,16 +156,25 @@ class ReplayModel:
     def hashes(self, rid):
         return self.base.hashes(rid)
 
-    def prepare(self, reqs, first: int):
+    def prepare(self, reqs, first, ext_kinds=("q", "k", "v")):
+        """Generate a batch's inputs in serving order.  first: the first
+        computed position of every request (one int, or one per request);
+        ext_kinds: the prefill rows' kinds (K only for a store without
+        attention)."""
         torch = self.torch
-        ext_h = np.concatenate([self.base.hashes(r.rid)[first:r.prompt_len] for r in reqs])
+        firsts = tuple([int(first)] * len(reqs) if np.isscalar(first) else (int(f) for f in first))
+        ext_h = np.concatenate([self.base.hashes(r.rid)[f:r.prompt_len] for r, f in zip(reqs, firsts)])
         T = reqs[0].max_new
-        dec_h = np.stack([self.base.hashes(r.rid)[r.prompt_len:r.prompt_len + T] for r in reqs], axis=1)
-        ext = self.base.rows(ext_h)
-        dec = self.base.rows(dec_h.reshape(-1))
+        ext = self.base.rows(ext_h, kinds=ext_kinds)
+        ext = {k: ext.get(k) for k in ("q", "k", "v")}
         B = len(reqs)
-        dec = {k: (v.view(T, B, *v.shape[1:]) if v is not None else None) for k, v in dec.items()}
-        entry = {"ext": ext, "dec": dec, "first": first,
+        if T:
+            dec_h = np.stack([self.base.hashes(r.rid)[r.prompt_len:r.prompt_len + T] for r in reqs], axis=1)
+            dec = self.base.rows(dec_h.reshape(-1))
+            dec = {k: (v.view(T, B, *v.shape[1:]) if v is not None else None) for k, v in dec.items()}
+        else:
+            dec = {}
+        entry = {"ext": ext, "dec": dec, "first": firsts,
                  "dec_steps": [{k: (v[t] if v is not None else None) for k, v in dec.items()} for t in range(T)]}
         self.ready[tuple(r.rid for r in reqs)] = entry
         return entry
@@ -190,6 +203,14 @@ class ReplayModel:
         e["ext_moved"] = None    # event: the prefill inputs are on the device
         e["dec"] = None
         e["dec_steps"] = None
+
+    def rearm(self):
+        """e2e: every host-resident batch's inputs are to be moved again (a
+        replay of the whole workload serves the same batches once more)."""
+        for e in self.ready.values():
+            if "host" in e:
+                e["moved"] = {}
+                e["ext_moved"] = None
 
     def start_streams(self):
         torch = self.torch
@@ -240,10 +261,12 @@ class ReplayModel:
             return self._last[1]
         key = tuple(r.rid for r in batch)
         e = self.ready.get(key)
-        if e is None or any(r.first != e["first"] for r in batch):
+        if e is None or tuple(r.first for r in batch) != e["first"]:
             raise RuntimeError("batch differs from the prepared one (order or cached prefix)")
         self._last = (batch, e)
         return e
+
+    next_key = None   # e2e: batch key -> the key served after it (its prefill inputs move early)
 
     def extend_inputs(self, batch):
         e = self._entry(batch)
@@ -251,7 +274,11 @@ class ReplayModel:
             key = tuple(r.rid for r in batch)
             self.prefetch_extend(key)
             self.torch.cuda.current_stream().wait_event(e["ext_moved"])
+            if self.next_key is not None and self.next_key.get(key) is not None:
+                self.prefetch_extend(self.next_key[key])
         return e["ext"]
+
+    extend_kv = extend_inputs   # a store without attention reads the prepared K (and V)
 
     def decode_inputs(self, batch, t):
         e = self._entry(batch)
@@ -285,17 +312,31 @@ DECODE_TRAFFIC_RATIO = 1.0818
 DECODE_TRAFFIC_CURRENT = False
 
 
+def row_bytes(shape):
+    """K+V bytes of one token: 2 x KV heads x head_dim x 2 B; one 576-wide
+    latent row (K and V share it) for the latent layout."""
+    return shape.head_dim_k * 2 if shape.mla else 2 * shape.kv_heads * shape.head_dim_k * 2
+
+
 def decode_bytes(lay, t, shape, stored=True):
     """Unique K/V rows touched (shared segments once) x row bytes + indices + Q + O,
-    + the new token's K/V written to the pool when the call stores it."""
-    R = 2 * shape.kv_heads * shape.head_dim_k * 2
+    + the new token's K/V written to the pool when the call stores it (the
+    latent layout stores it with kv_store inside the same timed call: read
+    and written)."""
+    R = row_bytes(shape)
     L = lay.L + t + 1
     tail = (L - lay.private).sum()
     seg = sum(len(s) for s, _ in lay.segments) if lay.use_cascade else 0
     B = lay.batch_size
     qo = B * shape.q_heads * (shape.head_dim_k + shape.head_dim_v) * 2
-    store = B * R if stored else 0
+    store = (2 if shape.mla else 1) * B * R if stored else 0
     return int((seg + tail) * R + (seg + tail) * 4 + qo + store), int(L.sum() * R)
+
+
+def decode_flops(lay, t, shape):
+    """Scores and P.V of one decode step: 2 x Hq x (dk + dv) per key."""
+    L = lay.L + t + 1
+    return int(L.sum()) * 2 * shape.q_heads * (shape.head_dim_k + shape.head_dim_v)
 
 
 def extend_flops(lay, shape):
@@ -306,8 +347,58 @@ def extend_flops(lay, shape):
     return tot
 
 
+def kernel_summary(eng, shape, traffic_ratio=None, traffic_note=None):
+    """Per entry point: launches, time, algorithmic work and rate from the
+    CUDA events recorded around its calls; the roofline object of the one
+    with the largest total time (decode: HBM, and for the latent layout the
+    tensor fraction beside it; extend: bf16 tensor, sustained peak since it
+    runs inside a long step)."""
+    hbm, bf16, bf16_sus, peak_src = peaks()
+    summary = {}
+    for name, evs in eng.events.items():
+        if not evs:
+            continue
+        durs = [a.elapsed_time(b) for a, b, _ in evs]
+        info = [i for _, _, i in evs]
+        tot = sum(durs)
+        d = {"launches": len(durs), "total_ms": tot, "avg_us": 1e3 * tot / max(len(durs), 1)}
+        sec = d["avg_us"] * 1e-6
+        if name == "attn_decode":
+            b = [decode_bytes(i[1], i[2], shape) for i in info]
+            uniq = sum(x for x, _ in b) / len(b)
+            logical = sum(y for _, y in b) / len(b)
+            d.update(bytes_per_launch=uniq, logical_bytes_per_launch=logical,
+                     gbs=uniq / sec / 1e9, logical_gbs=logical / sec / 1e9)
+            if shape.mla:
+                f = sum(decode_flops(i[1], i[2], shape) for i in info) / len(info)
+                d.update(flops_per_launch=f, tflops=f / sec / 1e12)
+        elif name == "attn_extend":
+            f = sum(extend_flops(i[1], shape) for i in info) / len(info)
+            d.update(flops_per_launch=f, tflops=f / sec / 1e12)
+        elif name == "kv_store":
+            by = sum(2 * i[1] * row_bytes(shape) for i in info) / len(info)
+            d.update(bytes_per_launch=by, gbs=by / sec / 1e9)
+        summary[name] = d
+    dom = max(summary, key=lambda k: summary[k]["total_ms"])
+    dd = summary[dom]
+    if dom == "attn_extend":
+        roof = {"bound": "tensor", "achieved": dd["tflops"], "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": dd["tflops"] / bf16_sus, "traffic": None, "kernel": dom,
+                "peak_source": f"{peak_src} bf16 dense sustained"}
+    else:
+        traffic = traffic_ratio * dd["bytes_per_launch"] if (dom == "attn_decode" and traffic_ratio) else None
+        roof = {"bound": "hbm", "achieved": dd["gbs"], "peak": hbm, "unit": "GB/s", "frac": dd["gbs"] / hbm,
+                "traffic": traffic, "kernel": dom, "peak_source": f"{peak_src} HBM copy"}
+        if traffic is None and traffic_note:
+            roof["traffic_note"] = traffic_note
+        if dom == "attn_decode" and "tflops" in dd:   # the latent layout sits at the ridge: both fractions
+            roof["tensor"] = {"achieved": dd["tflops"], "peak": bf16_sus, "unit": "TFLOP/s",
+                              "frac": dd["tflops"] / bf16_sus, "peak_source": f"{peak_src} bf16 dense sustained"}
+    return summary, roof
+
+
 # ------------------------------------------------------------------ oracle
-def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
+def oracle_baseline(trace_fn, shape, seed, vocab, budget_s, one_core=True, seed_rows=0):
     """The oracle as it stands, on a bounded sample of one step, scaled to the
     metric's unit: host tree calls of a whole step (full), attention of sampled
     extend rows and decode tokens (timed until the budget is spent)."""
@@ -318,7 +409,7 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
     tr = trace_fn(0)
     model = SynthModel(shape, seed, vocab, device="cpu")
     tree = oracle.OracleTree(1 << 21)
-    runner = wl.Runner(tree, model)
+    runner = wl.Runner(tree, model, sched=oracle.OracleServer(tree))
     runner.serve([runner.request(tr.warm, 0)])
     reqs = [runner.request(tr.prompt(i), tr.max_new) for i in range(len(tr.questions))]
     t0 = time.perf_counter()
@@ -327,7 +418,7 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
     n_ext_total = sum(r.prompt_len - r.first for r in admitted)
     n_dec_total = len(admitted) * tr.max_new
     # attention sample: inputs of two requests generated once on the CPU (not timed)
-    rng = np.random.default_rng(0)
+    rng = np.random.default_rng(seed_rows)
     pre = []
     for r in admitted[:2]:
         h = model.hashes(r.rid)
@@ -355,6 +446,12 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
     est = t_tree + t_att_ext / n_ext * n_ext_total + t_att_dec / n_dec * n_dec_total
     value = n_dec_total / est
     cores = oracle.num_threads()
+    if not one_core:
+        sample = (f"oracle tree calls of one full step ({t_tree:.2f} s) + attention of {n_dec} decode tokens and "
+                  f"{n_ext} prefill rows ({t_att_dec + t_att_ext:.1f} s) on {cores} threads, scaled to "
+                  f"{n_dec_total} decode tokens and {n_ext_total} prefill rows per step")
+        return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                "est_s_per_step": est}
     # the same attention on one core (the tree calls are single-threaded
     # already): decode tokens for an eighth of the budget, then prefill rows
     # eight at a time for another eighth
@@ -388,6 +485,339 @@ def oracle_baseline(trace_fn, shape, seed, vocab, budget_s):
               f"{m_ext} prefill rows, {s_dec + s_ext:.1f} s): {n_dec_total / est1:.1f} {UNIT}")
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
             "value_one_core": n_dec_total / est1, "est_s_per_step": est}
+
+
+# ------------------------------------------------------------ other configs
+CONFIG_NAMES = ("few_shot", "chat", "agent", "mla")
+
+
+def config_setup(name):
+    """(trace, serving loop, runner options, workload description) of a
+    configuration other than the default few-shot one."""
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from synth import traces
+    if name == "chat":
+        tr = traces.chat()
+        desc = ("multi-turn chat: 256 sessions x 8 turns, user turns U[128,512], 128 generated tokens per turn, "
+                f"GQA 32q/8kv, head_dim 128, bf16, pool {tr.pool_slots} slots (0.75 of the working set, LRU "
+                "eviction), decode batch <= 256; one step = the whole trace on an empty cache")
+        return tr, lambda r, t: wl.run_chat(r, t, overlap=True), dict(cascade=True, prefill_attention=True), desc
+    if name == "agent":
+        tr = traces.agent_tree()
+        desc = ("agent branching tree: 2048-token root, fan-out 4 to depth 3, 256-token branches, 64 leaves "
+                f"decoding 256 tokens, GQA 64q/8kv, head_dim 128, bf16, pool {tr.pool_slots} slots; one step = "
+                "the whole tree on an empty cache")
+        return tr, lambda r, t: wl.run_agent(r, t, overlap=True), dict(cascade=True, prefill_attention=True), desc
+    if name == "mla":
+        tr = traces.mla_long()
+        desc = ("latent long-context decode: 128 requests, 4096 shared + U[0,28672] private tokens, latent 576 "
+                f"(512+64), 128 query heads, bf16, {tr.steps} decode steps, pool {tr.pool_slots} slots; one step = "
+                "store the contexts, then every decode step, on an empty cache")
+        return tr, lambda r, t: wl.run_mla(r, t, overlap=True), dict(cascade=False, prefill_attention=False), desc
+    raise ValueError(name)
+
+
+class MemoSequences:
+    """The model's sequence() results recorded once (the host pre-run) and
+    handed back in the same call order on every replay: a replay serves the
+    same requests in the same order, and hashing every prompt again is the
+    model's work, not the serving path's."""
+
+    def __init__(self, base):
+        self.base = base
+        self.memo = []
+        self.i = 0
+        self.recording = True
+
+    def sequence(self, prompt, max_new):
+        if self.recording:
+            r = self.base.sequence(prompt, max_new)
+            self.memo.append((len(prompt), r))
+            return r
+        n, r = self.memo[self.i]
+        if n != len(prompt):
+            raise RuntimeError("a replay asked for another sequence than the pre-run")
+        self.i += 1
+        return r
+
+    def replay(self):
+        self.recording = False
+        self.i = 0
+
+    def __getattr__(self, name):
+        return getattr(self.base, name)
+
+
+def host_prerun(tr, fn, model, pool):
+    """Run the workload's host calls alone (the library's tree, no device):
+    the batches it serves, in order, with each request's first position."""
+    import radixattention_prefix_shared_tree_gb300 as ra
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from radixattention_prefix_shared_tree_gb300.driver import Scheduler
+    sched = Scheduler(ra.RadixCache(pool))
+    batches = []
+    admit = sched.admit
+
+    def rec(pending, policy, max_batch=None):
+        a, w = admit(pending, policy, max_batch)
+        if a:
+            batches.append(list(a))
+        return a, w
+
+    sched.admit = rec
+    fn(wl.Runner(sched.cache, model, sched=sched), tr)
+    return batches
+
+
+def row_work(batches):
+    """Keys attended, summed over every computed row (prefill rows and decode
+    tokens) of the served batches: what the oracle's attention costs scale
+    with.  Returns (prefill rows, decode tokens, sum of keys)."""
+    n_ext = n_dec = keys = 0
+    for b in batches:
+        for r in b:
+            n = r.prompt_len - r.first
+            n_ext += n
+            keys += n * (r.first + r.prompt_len + 1) // 2
+            n_dec += r.max_new
+            keys += r.max_new * r.prompt_len + r.max_new * (r.max_new + 1) // 2
+    return n_ext, n_dec, keys
+
+
+def oracle_baseline_config(name, budget_s):
+    """The oracle on a bounded sample of one step of a configuration: its
+    tree with its own scheduling round over the whole workload (timed in
+    full), and its attention timed on sampled rows of sampled requests, the
+    cost per attended key scaled to every row the step computes."""
+    import oracle
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from synth import hashgen as hg
+    from synth.model import SynthModel
+    tr, fn, opts, _ = config_setup(name)
+    sh = tr.shape
+    model = SynthModel(sh, tr.seed, tr.vocab, device="cpu")
+    served = []
+
+    class Rec(oracle.OracleServer):
+        def admit(self, pending, policy=oracle.LPM, max_batch=None):
+            a, w = super().admit(pending, policy, max_batch)
+            if a:
+                served.append(list(a))
+            return a, w
+
+    tree = oracle.OracleTree(tr.pool_slots)
+    t0 = time.perf_counter()
+    fn(wl.Runner(tree, model, sched=Rec(tree)), tr)
+    t_tree = time.perf_counter() - t0
+    n_ext, n_dec, keys_total = row_work(served)
+    rng = np.random.default_rng(0)
+    dec_reqs = [r for b in served for r in b if r.max_new > 0]
+    pick = [dec_reqs[i] for i in rng.choice(len(dec_reqs), size=min(3, len(dec_reqs)), replace=False)]
+    pre = []
+    for r in pick:
+        h = model.hashes(r.rid)
+        n = r.prompt_len + r.max_new
+        kb = hg.gen_values(h[:n], hg.KIND_K, sh.kv_heads, sh.head_dim_k)
+        vb = None if sh.mla else hg.gen_values(h[:n], hg.KIND_V, sh.kv_heads, sh.head_dim_v)
+        pre.append((r, kb, vb, h))
+    spent = keys = 0.0
+    rows = 0
+    while spent < budget_s or rows < 2:
+        r, kb, vb, h = pre[int(rng.integers(0, len(pre)))]
+        if opts["prefill_attention"] and rng.random() < 0.3 and r.prompt_len > r.first:
+            pos = r.first + rng.choice(r.prompt_len - r.first, size=min(4, r.prompt_len - r.first), replace=False)
+        else:
+            pos = np.asarray([r.prompt_len + int(rng.integers(0, r.max_new))])
+        qb = hg.gen_values(h[pos], hg.KIND_Q, sh.q_heads, sh.head_dim_k)
+        a = time.perf_counter()
+        oracle.attention(qb, kb, vb, np.zeros(len(pos), np.int64), pos + 1, sh.q_heads, sh.kv_heads,
+                         sh.head_dim_k, sh.head_dim_v, sh.scale, latent=sh.mla)
+        spent += time.perf_counter() - a
+        keys += float((pos + 1).sum())
+        rows += len(pos)
+    if not opts["prefill_attention"]:   # the prefill only stores K/V: no attention rows
+        n_ext_att, keys_total = 0, keys_total - sum(
+            (r.prompt_len - r.first) * (r.first + r.prompt_len + 1) // 2 for b in served for r in b)
+    else:
+        n_ext_att = n_ext
+    est = t_tree + spent / keys * keys_total
+    cores = oracle.num_threads()
+    sample = (f"oracle tree with its own scheduling round over the whole step ({t_tree:.2f} s, one thread) + "
+              f"attention of {rows} sampled rows ({spent:.1f} s on {cores} threads), scaled by attended keys to "
+              f"the step's {n_dec} decode tokens and {n_ext_att} prefill rows")
+    return {"value": n_dec / est, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+            "est_s_per_step": est}
+
+
+class OutputsHome:
+    """e2e: every output of a replay goes back to pinned host memory inside
+    the timed region, on a copy stream: prefill outputs per batch, decode
+    outputs a chunk of steps at a time from a ring the steps write into (a
+    ring half is written again only after its copy has finished)."""
+
+    def __init__(self, torch, runner, K, ext_rows, batch, shape):
+        self.torch, self.runner, self.K = torch, runner, K
+        self.stream = torch.cuda.Stream()
+        self.host_ext = torch.empty(max(ext_rows, 1), shape.q_heads, shape.head_dim_v,
+                                    dtype=torch.bfloat16).pin_memory()
+        self.host_dec = torch.empty(K, batch, shape.q_heads, shape.head_dim_v, dtype=torch.bfloat16).pin_memory()
+        self.done = [None, None]
+        self.bytes = 0
+
+    def _after_compute(self):
+        ev = self.torch.cuda.Event()
+        ev.record(self.torch.cuda.current_stream())
+        self.stream.wait_event(ev)
+
+    def on_extend(self, out):
+        self._after_compute()
+        with self.torch.cuda.stream(self.stream):
+            self.host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+        out.record_stream(self.stream)
+        self.bytes += out.numel() * out.element_size()
+
+    def on_decode(self, out, t, n_steps):
+        K = self.K
+        if (t + 1) % K and t + 1 != n_steps:
+            return
+        c = t // K
+        outs = self.runner.decode_outs
+        a, m = (c % 2) * K, t - c * K + 1
+        B = outs.shape[1]
+        self._after_compute()
+        with self.torch.cuda.stream(self.stream):
+            self.host_dec[:m, :B].copy_(outs[a:a + m], non_blocking=True)
+        outs.record_stream(self.stream)
+        self.bytes += m * out.numel() * out.element_size()
+        done = self.torch.cuda.Event()
+        done.record(self.stream)
+        self.done[c % 2] = done
+        prev = self.done[(c + 1) % 2]
+        if prev is not None:
+            self.torch.cuda.current_stream().wait_event(prev)
+        if t + 1 == n_steps:
+            self.done = [None, None]
+
+
+def run_config(args, name, rank, world, local):
+    """One configuration other than the default: every step replays the
+    whole workload on an empty cache, with its inputs generated beforehand
+    in HBM (value) or held in pinned host memory and moved inside the timed
+    region (e2e)."""
+    import torch
+    import torch.distributed as dist
+    import radixattention_prefix_shared_tree_gb300 as ra
+    from radixattention_prefix_shared_tree_gb300 import workloads as wl
+    from radixattention_prefix_shared_tree_gb300.driver import DeviceEngine
+    from synth.model import SynthModel
+
+    dev = torch.device("cuda", local)
+    tr, fn, opts, desc = config_setup(name)
+    sh = tr.shape
+    config = {"workload": desc, "policy": "lpm", "cascade": opts["cascade"], "scheduler": "overlapped",
+              "l2": "inputs larger than L2 (every step reads the whole workload's inputs again, GBs)"}
+    memo = MemoSequences(SynthModel(sh, tr.seed, tr.vocab, device=dev))
+    batches = host_prerun(tr, fn, memo, tr.pool_slots)
+    memo.replay()
+    n_ext, n_dec, _ = row_work(batches)
+    model = ReplayModel(memo, torch)
+    kinds = ("q", "k", "v") if opts["prefill_attention"] else ("k", "v")
+    keys = []
+    for b in batches:
+        model.prepare(b, [r.first for r in b], ext_kinds=kinds)
+        keys.append(tuple(r.rid for r in b))
+    eng = DeviceEngine(sh, tr.pool_slots, device=dev)
+
+    def replay(hooks=None):
+        memo.replay()
+        runner = wl.Runner(ra.RadixCache(tr.pool_slots), model, eng, **opts)
+        if hooks is not None:
+            hooks.runner = runner
+            runner.decode_out_slots = 2 * model.CHUNK
+            runner.on_decode, runner.on_extend = hooks.on_decode, hooks.on_extend
+        fn(runner, tr)
+        return runner
+
+    for _ in range(args.warmup):
+        replay()
+    torch.cuda.synchronize()
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+    gc.collect()
+    gc.freeze()
+    rounds = len(batches)
+    max_new = max(r.max_new for b in batches for r in b)
+    eng.timing_every = 4
+    eng.start_timing(args.steps * rounds * 2 * (max_new // 4 + 8) + 64)
+    launches0 = eng.launches
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        runner = replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    eng.timing = False
+    ms = slowest_rank(ev0.elapsed_time(ev1), world, dev)
+    launches = eng.launches - launches0
+    assert ra.rc_sync(eng.err) == ra.RC_OK
+    st = runner.cache.stats()
+    summary, roof = kernel_summary(eng, sh, None, "null: no ncu DRAM capture of this configuration")
+    value = whole_job_rate(args.steps * n_dec, world, ms)
+
+    e2e = None
+    if not args.no_e2e:
+        for k in keys:
+            model.to_host(k)
+        model.next_key = {k: (keys[i + 1] if i + 1 < len(keys) else None) for i, k in enumerate(keys)}
+        model.start_streams()
+        ext_rows = max(int(model.ready[k]["host"]["ext"]["k"].shape[0]) for k in keys)
+        home = OutputsHome(torch, None, model.CHUNK, ext_rows if opts["prefill_attention"] else 1,
+                           max(len(b) for b in batches), sh)
+        model.h2d_bytes = 0
+        gc.collect()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        h0 = time.perf_counter()
+        for _ in range(args.steps):
+            model.rearm()
+            replay(home)
+        torch.cuda.current_stream().wait_stream(home.stream)
+        e1.record()
+        host_s = time.perf_counter() - h0
+        torch.cuda.synchronize()
+        assert ra.rc_sync(eng.err) == ra.RC_OK
+        ems = slowest_rank(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": whole_job_rate(args.steps * n_dec, world, ems), "unit": UNIT,
+               "h2d_bytes_per_step": model.h2d_bytes // args.steps, "d2h_bytes_per_step": home.bytes // args.steps,
+               "ms_per_step": ems / args.steps, "host_queue_ms_per_step": 1e3 * host_s / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1:
+        import oracle
+        oracle.build()
+        cb = oracle_baseline_config(name, args.cpu_seconds)
+        cpu = {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+                "clocks": clk,
+                "hit_rate": {"tokens": st["match_hit_tokens"] / max(st["match_tokens"], 1),
+                             "requests": st["match_hits"] / max(st["match_calls"], 1)},
+                "work_per_step": {"decode_tokens": n_dec, "prefill_rows": n_ext, "rounds": rounds,
+                                  "evicted_tokens": st["evicted_tokens"]},
+                "kernels": summary, "parallelism": "replicas" if world > 1 else "single"}
+        print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------- replicas
@@ -541,23 +971,48 @@ def main():
                           f"{args.questions} questions U[32,64], {args.max_new} decode steps, "
                           "GQA 32q/8kv, head_dim 128, bf16, pool 2^21 slots",
               "policy": args.policy, "cascade": not args.no_cascade,
+              "scheduler": "overlapped" if args.overlap else "serial",
               "l2": "inputs larger than L2 (a new batch per step, ~0.55 GB of Q/K/V each)"}
 
+    if args.impl == "reference" and args.config != "few_shot":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        cb = oracle_baseline_config(args.config, max(args.cpu_seconds, 5.0))
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
+                "steps": 1, "extrapolated": True, "warmup": 0, "ms_per_step": cb["est_s_per_step"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": config_setup(args.config)[3]},
+                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     if args.impl == "reference":
         if rank != 0:
             return
         import oracle
         oracle.build()
-        cb = oracle_baseline(trace_fn, shape, tr0.seed, tr0.vocab, max(args.cpu_seconds, 5.0))
-        steps_t = []
-        for _ in range(args.warmup + args.steps):
-            steps_t.append(cb["est_s_per_step"])
-        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": 0,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["est_s_per_step"] * 1e3,
+        # every step (warm-up included) is one bounded sample of a step: the
+        # oracle tree's calls of a whole step and attention of sampled rows,
+        # scaled to the step; the timed steps' estimates are averaged
+        per = max(args.cpu_seconds / max(args.steps, 1), 0.4)
+        ests, cb = [], None
+        for s_ in range(args.warmup + args.steps):
+            cb = oracle_baseline(trace_fn, shape, tr0.seed, tr0.vocab, per, one_core=False, seed_rows=s_)
+            if s_ >= args.warmup:
+                ests.append(cb["est_s_per_step"])
+        est = float(np.mean(ests))
+        tokens = args.questions * args.max_new
+        sample = (f"{args.steps} timed steps (+{args.warmup} warm-up), each a bounded sample of one step "
+                  f"(~{per:.1f} s of attention); the last: {cb['sample']}")
+        line = {"impl": "reference", "metric": METRIC, "value": tokens / est, "unit": UNIT, "n_gpus": 0,
+                "steps": args.steps, "extrapolated": True, "warmup": args.warmup, "ms_per_step": est * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
-                "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample", "value_one_core")},
-                "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                "cpu_baseline": {"value": tokens / est, "unit": UNIT, "cores": cb["cores"], "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": tokens / est, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
 
@@ -570,6 +1025,11 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
+    if args.config != "few_shot":
+        run_config(args, args.config, rank, world, local)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if args.latent_only:
         hbm, bf16, _, peak_src = peaks()
         print(json.dumps(latent_path(dev, hbm, bf16, peak_src, steps=args.latent_steps,
@@ -610,12 +1070,30 @@ def main():
             raise RuntimeError("batch did not fit")
         return admitted
 
+    def serve_steps(lo, hi):
+        """Steps lo..hi-1, one batch each: with the overlapped scheduler (the
+        default) a batch's admission runs on the worker thread while the
+        previous batch's decode steps are launched."""
+        if not args.overlap:
+            for s_ in range(lo, hi):
+                step(batches[s_])
+                batches[s_] = None
+            return
+        cur = [lo]
+
+        def after(admitted, waiting):
+            if waiting or len(admitted) != len(batches[cur[0]]):
+                raise RuntimeError("batch did not fit")
+            batches[cur[0]] = None
+            cur[0] += 1
+            return batches[cur[0]] if cur[0] < hi else None
+
+        runner.serve_rounds(batches[lo], after, None, overlap=True)
+
     # a served batch is dropped at once, as a serving loop would: its slot
     # rows' memory goes back to the allocator (fresh pages cost the next
     # admission round page faults)
-    for s in range(args.warmup):
-        step(batches[s])
-        batches[s] = None
+    serve_steps(0, args.warmup)
     torch.cuda.synchronize()
     assert ra.rc_sync(eng.err) == ra.RC_OK
 
@@ -658,9 +1136,7 @@ def main():
         setattr(runner.sched, n, timed(n, fn))
     w0 = time.perf_counter()
     ev0.record()
-    for s in range(args.warmup, n_main):
-        step(batches[s])
-        batches[s] = None
+    serve_steps(args.warmup, n_main)
     ev1.record()
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
@@ -678,44 +1154,11 @@ def main():
 
     # per-call durations (events on the launching stream)
     hbm, bf16, bf16_sus, peak_src = peaks()
-    calls = {}
-    for name, evs in eng.events.items():
-        durs = [a.elapsed_time(b) for a, b, _ in evs]
-        info = [i for _, _, i in evs]
-        calls[name] = (durs, info)
-    summary = {}
-    for name, (durs, info) in calls.items():
-        tot = sum(durs)
-        d = {"launches": len(durs), "total_ms": tot, "avg_us": 1e3 * tot / max(len(durs), 1)}
-        if name == "attn_decode":
-            b = [decode_bytes(i[1], i[2], shape) for i in info]
-            uniq = sum(x for x, _ in b) / len(b)
-            logical = sum(y for _, y in b) / len(b)
-            d.update(bytes_per_launch=uniq, logical_bytes_per_launch=logical,
-                     gbs=uniq / (d["avg_us"] * 1e-6) / 1e9, logical_gbs=logical / (d["avg_us"] * 1e-6) / 1e9)
-        elif name == "attn_extend":
-            f = sum(extend_flops(i[1], shape) for i in info) / len(info)
-            d.update(flops_per_launch=f, tflops=f / (d["avg_us"] * 1e-6) / 1e12)
-        elif name == "kv_store":
-            R = 2 * shape.kv_heads * shape.head_dim_k * 2
-            by = sum(2 * i[1] * R for i in info) / len(info)
-            d.update(bytes_per_launch=by, gbs=by / (d["avg_us"] * 1e-6) / 1e9)
-        summary[name] = d
-    dom = max(summary, key=lambda k: summary[k]["total_ms"])
-    dd = summary[dom]
-    if dom == "attn_extend":
-        roof = {"bound": "tensor", "achieved": dd["tflops"], "peak": bf16_sus, "unit": "TFLOP/s",
-                "frac": dd["tflops"] / bf16_sus, "traffic": None, "kernel": dom,
-                "peak_source": f"{peak_src} bf16 dense sustained"}
-    else:
-        traffic = (DECODE_TRAFFIC_RATIO * dd["bytes_per_launch"]
-                   if dom == "attn_decode" and DECODE_TRAFFIC_CURRENT else None)
-        roof = {"bound": "hbm", "achieved": dd["gbs"], "peak": hbm, "unit": "GB/s", "frac": dd["gbs"] / hbm,
-                "traffic": traffic, "kernel": dom, "peak_source": f"{peak_src} HBM copy"}
-        if dom == "attn_decode" and not DECODE_TRAFFIC_CURRENT:
-            roof["traffic_note"] = (f"null: the last ncu capture (steps 125-126) measured {DECODE_TRAFFIC_RATIO} x "
-                                    "the algorithmic bytes, before the cascade kernel gained a CTA-wide barrier at "
-                                    "entry (no memory access changed); not yet captured again")
+    note = (f"null: the last ncu capture (steps 125-126) measured {DECODE_TRAFFIC_RATIO} x the algorithmic bytes, "
+            "before the cascade kernel gained a CTA-wide barrier at entry (no memory access changed); not yet "
+            "captured again")
+    summary, roof = kernel_summary(eng, shape, DECODE_TRAFFIC_RATIO if DECODE_TRAFFIC_CURRENT else None,
+                                   None if DECODE_TRAFFIC_CURRENT else note)
 
     hit_tok = (st1["match_hit_tokens"] - st0["match_hit_tokens"]) / max(st1["match_tokens"] - st0["match_tokens"], 1)
     hit_req = (st1["match_hits"] - st0["match_hits"]) / max(st1["match_calls"] - st0["match_calls"], 1)
@@ -797,9 +1240,7 @@ def main():
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         h0 = time.perf_counter()
-        for s in range(n_main, n_main + n_e2e):
-            step(batches[s])
-            batches[s] = None
+        serve_steps(n_main, n_main + n_e2e)
         torch.cuda.current_stream().wait_stream(d2h_stream)
         e1.record()
         host_s = time.perf_counter() - h0   # time the host took to queue the work

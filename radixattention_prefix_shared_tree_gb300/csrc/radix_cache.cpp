@@ -130,13 +130,16 @@ struct rc_cache : rc_pool::SlotPool {
         return up;
     }
 
-    // Descend along tok[0..n).  With do_split the end of the match is made a
-    // node boundary and `path` receives root..end; `sl` (if given) receives
-    // the matched slots.  Returns the matched length.
-    int64_t descend(const int32_t* tok, int64_t n, bool do_split, std::vector<int32_t>* pth,
-                    std::vector<int32_t>* sl) {
+    // Descend along tok[0..n) without changing anything.  Returns the matched
+    // length; `pth` (if given) receives root..the last node matched whole;
+    // `sl` (if given, room for n) receives the matched slots.  A match that
+    // stops inside an edge leaves that child in *mid and its matched count in
+    // *mid_k (else *mid = -1).
+    int64_t walk(const int32_t* tok, int64_t n, std::vector<int32_t>* pth, int32_t* sl, int32_t* mid,
+                 int32_t* mid_k) const {
         int32_t cur = 0;
         if (pth) { pth->clear(); pth->push_back(0); }
+        if (mid) *mid = -1;
         int64_t i = 0;
         while (i < n) {
             auto it = edges.find(edge_key(cur, tok[i]));
@@ -146,13 +149,10 @@ struct rc_cache : rc_pool::SlotPool {
             const int32_t* rt = toks(r);
             int64_t lim = std::min<int64_t>(r.len, n - i);
             int64_t k = 1 + common_prefix(rt + 1, tok + i + 1, lim - 1);
-            if (sl) sl->insert(sl->end(), slot_arena.begin() + r.off, slot_arena.begin() + r.off + k);
+            if (sl) std::memcpy(sl + i, slot_arena.data() + r.off, (size_t)k * 4);
             i += k;
             if (k < r.len) {
-                if (do_split) {
-                    int32_t up = split(c, (int32_t)k);
-                    if (pth) pth->push_back(up);
-                }
+                if (mid) { *mid = c; *mid_k = (int32_t)k; }
                 break;
             }
             cur = c;
@@ -161,15 +161,24 @@ struct rc_cache : rc_pool::SlotPool {
         return i;
     }
 
-    void touch(const std::vector<int32_t>& pth) {
-        for (int32_t i : pth) {
-            recs[(size_t)i].stamp = clock;
-            lru_fix(i);
+    // walk() with the end of the match made a node boundary: a stop inside
+    // an edge splits it and the upper part ends `pth`.
+    int64_t descend(const int32_t* tok, int64_t n, std::vector<int32_t>* pth, int32_t* sl) {
+        int32_t mid = -1, k = 0;
+        int64_t m = walk(tok, n, pth, sl, &mid, &k);
+        if (mid >= 0) {
+            int32_t up = split(mid, k);
+            if (pth) pth->push_back(up);
         }
+        return m;
     }
-    void pin(const std::vector<int32_t>& pth) {
+
+    // Stamp the path with the clock (and pin it); one candidate-set update per node.
+    void touch(const std::vector<int32_t>& pth, bool and_pin) {
         for (int32_t i : pth) {
-            recs[(size_t)i].ref += 1;
+            Rec& r = recs[(size_t)i];
+            r.stamp = clock;
+            if (and_pin) r.ref += 1;
             lru_fix(i);
         }
     }
@@ -230,11 +239,8 @@ rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, i
                           int32_t* out_slots, rc_node* out_node) {
     if (!c || n < 0 || (n > 0 && !tok) || !matched || !out_node) return RC_ERR_ARG;
     c->clock += 1;
-    c->scratch_slots.clear();
-    int64_t m = c->descend(tok, n, true, &c->path, out_slots ? &c->scratch_slots : nullptr);
-    c->touch(c->path);
-    if (pin) c->pin(c->path);
-    if (out_slots && m) std::memcpy(out_slots, c->scratch_slots.data(), (size_t)m * 4);
+    int64_t m = c->descend(tok, n, &c->path, out_slots);
+    c->touch(c->path, pin != 0);
     *matched = m;
     *out_node = c->recs[(size_t)c->path.back()].id;
     c->match_calls += 1;
@@ -257,8 +263,9 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     if (!c || n < 0 || (n > 0 && (!tok || !slots)) || !already_present || !out_node) return RC_ERR_ARG;
     if (!slots_in_pool(c, slots, n)) return RC_ERR_ARG;
     std::vector<int32_t>& have = c->scratch_slots;
-    have.clear();
-    int64_t m = c->descend(tok, n, false, nullptr, &have);
+    if ((int64_t)have.size() < n) have.resize((size_t)n);
+    int32_t mid = -1, mid_k = 0;
+    int64_t m = c->walk(tok, n, &c->path, have.data(), &mid, &mid_k);   // look first, change nothing
     c->new_epoch();
     // positions whose slot is already the cached one need no check
     const int64_t same = common_prefix(slots, have.data(), m);
@@ -269,7 +276,7 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
         c->mark[(size_t)s] = c->epoch;
     }
     c->clock += 1;
-    c->descend(tok, n, true, &c->path, nullptr);
+    if (mid >= 0) c->path.push_back(c->split(mid, mid_k));   // the walk's end made a node boundary
     if (m < n) {
         int32_t parent = c->path.back();
         int64_t off = (int64_t)c->tok_arena.size();
@@ -295,8 +302,7 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     }
     c->n_held -= dup;
     c->n_free += dup;
-    c->touch(c->path);
-    if (pin) c->pin(c->path);
+    c->touch(c->path, pin != 0);
     if (out_slots) {
         if (m) std::memcpy(out_slots, have.data(), (size_t)m * 4);
         if (n > m && out_slots != slots) std::memmove(out_slots + m, slots + m, (size_t)(n - m) * 4);
@@ -383,7 +389,7 @@ rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, co
     if (policy == RC_LPM && n > 1) {
         std::vector<std::pair<int64_t, int32_t>> key((size_t)n);
         for (int32_t i = 0; i < n; ++i)
-            key[(size_t)i] = {-c->descend(prompts[i], lens[i], false, nullptr, nullptr), i};
+            key[(size_t)i] = {-c->walk(prompts[i], lens[i], nullptr, nullptr, nullptr, nullptr), i};
         std::sort(key.begin(), key.end());  // (-match, index): longest first, then arrival
         for (int32_t i = 0; i < n; ++i) out_order[i] = key[(size_t)i].second;
     }
@@ -410,15 +416,15 @@ rc_status rc_admit(rc_cache* c, int policy, rc_request* reqs, int32_t n, int32_t
     std::vector<int32_t> order((size_t)n);
     rc_status st = sched_order(c, policy, prompts.data(), lens.data(), n, order.data());
     if (st != RC_OK) return st;
-    std::vector<int32_t> mslots;
     int32_t count = 0;
     for (int32_t k = 0; k < n; ++k) {
         if (max_batch > 0 && count >= max_batch) break;
         rc_request& r = reqs[order[(size_t)k]];
-        mslots.resize((size_t)std::max<int64_t>(r.prompt_len, 1));
         int64_t m = 0;
         rc_node node = 0;
-        st = rc_match_prefix(c, r.tokens, r.prompt_len, 1, &m, mslots.data(), &node);
+        // the matched slots land in the row itself (room for prompt_len + max_new >= matched);
+        // the new ones then overwrite it from `first` on
+        st = rc_match_prefix(c, r.tokens, r.prompt_len, 1, &m, r.slots, &node);
         if (st != RC_OK) return st;
         const int64_t first = r.max_new > 0 ? std::min(m, r.prompt_len - 1) : m;
         const int64_t need = r.prompt_len - first + r.max_new;
@@ -436,7 +442,6 @@ rc_status rc_admit(rc_cache* c, int policy, rc_request* reqs, int32_t n, int32_t
             if (rs != RC_OK) return rs;
             break;  // the first request that does not fit stops the round
         }
-        if (first) std::memcpy(r.slots, mslots.data(), (size_t)first * 4);
         r.matched = m;
         r.first = first;
         r.node = node;

@@ -62,6 +62,55 @@ class Runner:
             self.sched.finish(admitted)
         return admitted, waiting
 
+    # -------------------------------------------------------- many rounds
+    def serve_rounds(self, pending: list, after, max_batch: int | None = None, overlap: bool = False):
+        """Rounds of continuous batching: serve `pending`, then
+        after(admitted, waiting) gives the next round's queue (None: done).
+
+        overlap=True is the overlapped scheduler (the SGLang engineering
+        article's zero-overhead batch scheduler, section 2: the CPU prepares
+        batch k+1 while the GPU runs batch k).  Round k's host calls that
+        follow its prefill -- the finish inserts of round k, then round k+1's
+        whole admission (order, match, pin, evict, alloc) -- run on a worker
+        thread while this thread launches round k's decode steps; the native
+        calls release the interpreter lock, so the two overlap.  The tree
+        sees the same calls in the same order as serve() round by round (the
+        decode launches touch no tree state, and every kernel of round k+1
+        is queued after round k's on the one stream, so slots round k+1
+        takes from round k are written only after round k has read them):
+        results are identical."""
+        if not overlap:
+            while pending:
+                admitted, waiting = self.serve(pending, max_batch)
+                pending = after(admitted, waiting)
+            return
+        from concurrent.futures import ThreadPoolExecutor
+        sched, policy = self.sched, self.policy
+        with ThreadPoolExecutor(1) as worker:
+            fut = worker.submit(sched.admit, pending, policy, max_batch)
+            while True:
+                admitted, waiting = fut.result()
+                nxt = after(admitted, waiting)
+                lay = None
+                if admitted:
+                    if self.engine is not None:
+                        self._prefill(admitted)
+                    sched.commit_prompts(admitted)
+                    dec = [r for r in admitted if r.max_new]
+                    if self.engine is not None and dec:
+                        lay = self._decode_layout(dec)     # reads the tree: before the worker goes on
+
+                def host_work(admitted=admitted, nxt=nxt):
+                    if admitted:
+                        sched.finish(admitted)
+                    return sched.admit(nxt, policy, max_batch) if nxt else ([], [])
+                fut = worker.submit(host_work)
+                if lay is not None:
+                    self._decode_steps(dec, lay)
+                if not nxt:
+                    fut.result()
+                    return
+
     def _prefill(self, batch):
         eng, torch = self.engine, self.engine.torch
         lay = eng.upload_batch(batch, cascade=False, parts=("extend",))
@@ -89,10 +138,18 @@ class Runner:
                 self.extend_out[r.rid] = (np.arange(r.first, r.prompt_len), o, lse[a:b].cpu().numpy())
 
     def _decode(self, batch):
-        eng, torch = self.engine, self.engine.torch
+        self._decode_steps(batch, self._decode_layout(batch))
+
+    def _decode_layout(self, batch):
+        """Slot tables and cascade segments of a decode batch, staged to the
+        device (the cascade plan is read off the tree's pinned paths)."""
         planner = getattr(self.cache, "cascade_plan", None)
-        lay = eng.upload_batch(batch, cascade=self.cascade, planner=planner, parts=("decode",))
+        lay = self.engine.upload_batch(batch, cascade=self.cascade, planner=planner, parts=("decode",))
         self.last_layout = lay
+        return lay
+
+    def _decode_steps(self, batch, lay):
+        eng, torch = self.engine, self.engine.torch
         sh = eng.shape
         B = len(batch)
         R = max(1, self.decode_out_slots)
@@ -153,7 +210,7 @@ def run_few_shot(runner: Runner, trace, warm: bool = True):
     return admitted
 
 
-def run_chat(runner: Runner, trace, max_rounds: int = 10_000):
+def run_chat(runner: Runner, trace, max_rounds: int = 10_000, overlap: bool = False):
     """Sessions grow turn by turn; each round admits the ready turns that fit."""
     n_sess = len(trace.user_turns)
     history = [np.zeros(0, np.int32) for _ in range(n_sess)]
@@ -163,12 +220,11 @@ def run_chat(runner: Runner, trace, max_rounds: int = 10_000):
         r = runner.request(trace.user_turns[s][0], trace.max_new)
         r.session = s
         pending[s] = r
-    rounds = 0
     served = []
-    while pending and rounds < max_rounds:
-        rounds += 1
-        queue = [pending[s] for s in sorted(pending)]
-        admitted, waiting = runner.serve(queue, trace.max_batch)
+    rounds = [0]
+
+    def after(admitted, waiting):
+        rounds[0] += 1
         if not admitted:
             raise RuntimeError("no progress: pool too small for any waiting turn")
         for r in admitted:
@@ -181,46 +237,65 @@ def run_chat(runner: Runner, trace, max_rounds: int = 10_000):
                 nr = runner.request(np.concatenate([history[s], trace.user_turns[s][turn[s]]]), trace.max_new)
                 nr.session = s
                 pending[s] = nr
-    return served, rounds
+        if not pending or rounds[0] >= max_rounds:
+            return None
+        return [pending[s] for s in sorted(pending)]
+
+    runner.serve_rounds([pending[s] for s in sorted(pending)], after, trace.max_batch, overlap)
+    return served, rounds[0]
 
 
-def run_agent(runner: Runner, trace):
+def run_agent(runner: Runner, trace, overlap: bool = False):
     """Root prompt, then each level of branches (prefill only), then all leaves decode."""
-    runner.serve([runner.request(trace.root, 0)])
     depth = len(trace.leaves[0])
-    for lvl in range(1, depth):
-        paths = sorted({leaf[:lvl] for leaf in trace.leaves})
-        reqs = [runner.request(trace.prompt(p), 0) for p in paths]
-        admitted, waiting = runner.serve(reqs)
+    levels = [[trace.root]] + [[trace.prompt(p) for p in sorted({leaf[:lvl] for leaf in trace.leaves})]
+                               for lvl in range(1, depth)]
+    out = []
+
+    def after(admitted, waiting):
         assert not waiting
-    reqs = [runner.request(trace.prompt(leaf), trace.max_new) for leaf in trace.leaves]
-    admitted, waiting = runner.serve(reqs)
-    assert not waiting
-    return admitted
+        out[:] = admitted
+        if levels:
+            return [runner.request(p, 0) for p in levels.pop(0)]
+        if out and out[0].max_new == 0 and not getattr(after, "leaves_done", False):
+            after.leaves_done = True
+            return [runner.request(trace.prompt(leaf), trace.max_new) for leaf in trace.leaves]
+        return None
+
+    first = [runner.request(p, 0) for p in levels.pop(0)]
+    runner.serve_rounds(first, after, None, overlap)
+    return out
 
 
-def run_mla(runner: Runner, trace, n_requests: int | None = None):
+def run_mla(runner: Runner, trace, n_requests: int | None = None, overlap: bool = False):
     """Latent-attention long-context decode: the shared prefix and every
     request's private context are stored (kv_store, no prefill attention),
     then all requests decode trace.steps tokens together."""
-    runner.serve([runner.request(trace.shared, 0)])
     n = len(trace.private) if n_requests is None else n_requests
-    reqs = [runner.request(trace.prompt(i), trace.steps) for i in range(n)]
-    admitted, waiting = runner.serve(reqs)
-    assert not waiting
-    return admitted
+    out = []
+    todo = [lambda: [runner.request(trace.prompt(i), trace.steps) for i in range(n)]]
+
+    def after(admitted, waiting):
+        assert not waiting
+        out[:] = admitted
+        return todo.pop(0)() if todo else None
+
+    runner.serve_rounds([runner.request(trace.shared, 0)], after, None, overlap)
+    return out
 
 
-def run_multimodal(runner: Runner, trace, key_fn, batch: int = 64):
+def run_multimodal(runner: Runner, trace, key_fn, batch: int = 64, overlap: bool = False):
     """Questions about images in arrival order, served in rounds of up to
     `batch` (the scheduler orders each round); an image's key run comes from
     key_fn(bytes, n_tokens)."""
     reqs = [runner.request(trace.prompt(i, key_fn), trace.max_new) for i in range(len(trace.questions))]
     served = []
-    pending = reqs
-    while pending:
-        admitted, pending = runner.serve(pending, batch)
+
+    def after(admitted, waiting):
         if not admitted:
             raise RuntimeError("no progress: pool too small for any waiting request")
         served.extend(admitted)
+        return waiting or None
+
+    runner.serve_rounds(reqs, after, batch, overlap)
     return served

@@ -242,3 +242,43 @@ def test_few_shot_fp8_pool_vs_oracle(cuda, cascade):
     stats = {}
     check_requests(runner, model, [r.rid for r in reqs[::6]], tr.shape, stats, fp8=True)
     assert stats["sum"] / stats["n"] <= MEAN_ABS
+
+
+def _decode_bits(runner):
+    return {rid: np.stack([o for _, o, _ in d]) for rid, d in runner.decode_out.items()}
+
+
+@pytest.mark.parametrize("which", ["few_shot_batches", "chat"])
+def test_overlapped_rounds_equal_serial(cuda, which):
+    """The overlapped scheduler (round k's finish and round k+1's admission
+    on a worker thread while round k's decode steps are launched) against
+    serving round by round: every decode and prefill output bit for bit, and
+    the same tree."""
+    outs = []
+    for overlap in (False, True):
+        if which == "chat":
+            tr = traces.chat(n_sessions=16, n_turns=4, umin=32, umax=128, max_new=8)
+            tr.max_batch = 6
+            model = SynthModel(tr.shape, tr.seed, tr.vocab, device=cuda)
+            eng = DeviceEngine(tr.shape, tr.pool_slots, device=cuda)
+            cache = ra.RadixCache(tr.pool_slots)
+            runner = wl.Runner(cache, model, eng, collect=True)
+            wl.run_chat(runner, tr, overlap=overlap)
+            assert cache.stats()["evicted_nodes"] > 0
+        else:
+            base = traces.few_shot(n_questions=32, max_new=6)
+            model = SynthModel(base.shape, base.seed, base.vocab, device=cuda)
+            eng = DeviceEngine(base.shape, 1 << 16, device=cuda)
+            cache = ra.RadixCache(1 << 16)
+            runner = wl.Runner(cache, model, eng, collect=True)
+            runner.serve([runner.request(base.warm, 0)])
+            batches = [[runner.request(t.prompt(i), t.max_new) for i in range(32)]
+                       for t in (traces.few_shot(n_questions=32, max_new=6, batch_salt=s) for s in range(1, 5))]
+            left = list(batches[1:])
+            runner.serve_rounds(batches[0], lambda a, w: (left.pop(0) if left else None), None, overlap)
+        assert ra.rc_sync(eng.err) == ra.RC_OK
+        outs.append((_decode_bits(runner), {k: v[1] for k, v in runner.extend_out.items()}, cache.dump()))
+    a, b = outs
+    assert a[0].keys() == b[0].keys() and a[1].keys() == b[1].keys() and a[2] == b[2]
+    assert all(np.array_equal(a[0][k], b[0][k]) for k in a[0])
+    assert all(np.array_equal(a[1][k], b[1][k]) for k in a[1])

@@ -263,3 +263,25 @@ def test_admission_evicts_shortfall_and_misfit_stops(built):
     assert o[1] == [3, 4]
     assert o[3]["evicted_nodes"] == 2 and o[3]["free"] == 5 and o[3]["caller"] == 5 and o[3]["pins"] == 1
     assert results[1] == o
+
+
+@pytest.mark.parametrize("which", ["chat", "multimodal"])
+def test_overlapped_rounds_equal_serial_host(built, which):
+    """The overlapped scheduler (round k's finish and round k+1's admission
+    on a worker thread) makes the same tree calls in the same order as
+    serving round by round: identical records, tree and statistics."""
+    outs = []
+    for overlap in (False, True):
+        if which == "chat":
+            tr = traces.chat(n_sessions=20, n_turns=4, umin=16, umax=64, max_new=16)
+            tr.max_batch = 7
+            run = lambda runner: wl.run_chat(runner, tr, overlap=overlap)
+        else:
+            tr = traces.multimodal(n_images=4, per_image=5, image_tokens=40, image_bytes=64, max_new=5)
+            run = lambda runner: wl.run_multimodal(runner, tr, ra.rc_image_key, batch=3, overlap=overlap)
+        cache = ra.RadixCache(tr.pool_slots)
+        rec = Recorder(Scheduler(cache), cache)
+        run(wl.Runner(cache, SynthModel(tr.shape, tr.seed, tr.vocab, device="cpu"), sched=rec))
+        outs.append((rec.rec, cache.dump(), cache.stats()))
+    assert outs[0] == outs[1]
+    assert any(r[0] == "admit" and r[2] for r in outs[0][0])   # rounds with waiting requests
