@@ -136,6 +136,20 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
     }
     const int32_t* keys = p.table + row0 + k0;
     const int n_tiles = (count + kWarpKeys - 1) / kWarpKeys;
+    // fused epilogue: the cascade partials this row folds in; the row offsets
+    // of the first 32 (lane j: partial j) are read now, ahead of the main loop
+    // (the segment tables are the caller's inputs, not the cascade's output)
+    int e0 = 0, n_parts = 0;
+    if (FUSED && p.req_seg_indptr) {
+        e0 = p.req_seg_indptr[b];
+        n_parts = (p.req_seg_indptr[b + 1] - e0) * p.seg_chunks;
+    }
+    auto part_row = [&](int j) -> int64_t {
+        return j < n_parts ? (int64_t)p.req_seg_pos[e0 + j / p.seg_chunks] * p.q_heads * p.seg_chunks +
+                                 (j % p.seg_chunks)
+                           : 0;
+    };
+    const int64_t first_row = part_row(lane);
     // attn_decode_append: the row's last key (position L-1) is the step's new
     // token.  The warp whose keys hold it gathers it from k_new/v_new and
     // writes it to its pool slot (lanes 0..CH-1 the K row, CH..2CH-1 the V row).
@@ -406,80 +420,58 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
         }
     } else {
         // the row's whole table part is here: fold in its cascade partials
-        // (every chunk of every segment it reads; partial (e, c) of head h
-        // sits at row (req_seg_pos[e] * Hq + h) * seg_chunks + c)
-        int e0 = 0, n_parts = 0;
-        // (none after a cascade kernel gave up on a bounded wait: unwritten)
-        if (p.req_seg_indptr && !(p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout))) {
-            e0 = p.req_seg_indptr[b];
-            n_parts = (p.req_seg_indptr[b + 1] - e0) * p.seg_chunks;
-        }
-        const int sc = p.seg_chunks;
-        // partial j of head h is row part_row(j) + h_off; resolved into a
-        // per-warp table (batches of 32) so the element loop has no chains
+        // (every chunk of every segment it reads; partial j of head h sits at
+        // row part_row(j) + (kvh * G + h) * seg_chunks).  Partials come in
+        // batches of 32: lane j loads partial j's G log-sum-exps in one
+        // round, then every lane loads the batch's rows in a second round
+        // (all independent loads), merged online against a running max.
         constexpr int kPB = 32;
         int64_t* sRow = reinterpret_cast<int64_t*>(sOwn + 8);   // [kPB]
-        float* sW = reinterpret_cast<float*>(sRow + kPB);        // [G][kPB]
-        float* sHead = sW + G * kPB;                             // [G][2]: final max, 1/weight sum
-        // pass 1: final max and weight sum per head over all partials
-        for (int h = 0; h < G; ++h) {
-            const int64_t hoff = (int64_t)(kvh * G + h) * sc;
-            float m = sOwn[h];
-            for (int j = lane; j < n_parts; j += 32) {
-                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc) + hoff;
-                m = fmaxf(m, p.seg_lse[row]);
-            }
-#pragma unroll
-            for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
-            float w = 0.f;
-            for (int j = lane; j < n_parts; j += 32) {
-                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc) + hoff;
-                const float l2 = p.seg_lse[row];
-                w += l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m);
-            }
-#pragma unroll
-            for (int k = 16; k > 0; k >>= 1) w += __shfl_xor_sync(0xffffffffu, w, k);
-            const float own = sOwn[h];
-            w += own == -INFINITY ? 0.f : rc::fast_exp2(own - m);
-            if (lane == 0) {
-                sHead[2 * h] = m;
-                sHead[2 * h + 1] = w > 0.f ? 1.f / w : 0.f;
-            }
-        }
-        __syncwarp();
-        // pass 2: own part, then the partials batch by batch
-        float acc[G][D / 32];
+        float* sL = reinterpret_cast<float*>(sRow + kPB);         // [G][kPB]
+        const int sc = p.seg_chunks;
+        float m_h[G], w_h[G], acc[G][D / 32];
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float own = sOwn[h];
-            const float wo = own == -INFINITY ? 0.f : rc::fast_exp2(own - sHead[2 * h]) * sHead[2 * h + 1];
+            m_h[h] = sOwn[h];
+            w_h[h] = sOwn[h] == -INFINITY ? 0.f : 1.f;
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) acc[h][k] = wo * sE[h * D + lane + 32 * k];
+            for (int k = 0; k < D / 32; ++k) acc[h][k] = m_h[h] == -INFINITY ? 0.f : sE[h * D + lane + 32 * k];
         }
-        for (int j0 = 0; j0 < n_parts; j0 += kPB) {
-            const int nb = min(kPB, n_parts - j0);
+        // none after a cascade kernel gave up on a bounded wait (unwritten)
+        const int n_use = (p.err && (*reinterpret_cast<volatile int32_t*>(p.err) & rc::kErrTimeout)) ? 0 : n_parts;
+        for (int j0 = 0; j0 < n_use; j0 += kPB) {
+            const int nb = min(kPB, n_use - j0);
+            const int64_t my_row = j0 == 0 ? first_row : part_row(j0 + lane);
             if (lane < nb) {
-                const int j = j0 + lane;
-                const int64_t row = (int64_t)p.req_seg_pos[e0 + j / sc] * p.q_heads * sc + (j % sc);
-                sRow[lane] = row;
+                sRow[lane] = my_row;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float l2 = p.seg_lse[row + (int64_t)(kvh * G + h) * sc];
-                    sW[h * kPB + lane] =
-                        l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - sHead[2 * h]) * sHead[2 * h + 1];
-                }
+                for (int h = 0; h < G; ++h) sL[h * kPB + lane] = p.seg_lse[my_row + (int64_t)(kvh * G + h) * sc];
             }
             __syncwarp();
-            for (int jj = 0; jj < nb; ++jj) {
-                const int64_t row = sRow[jj];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mb = m_h[h];
+                for (int j = 0; j < nb; ++j) mb = fmaxf(mb, sL[h * kPB + j]);
+                if (mb == -INFINITY) continue;   // nothing yet for this head
+                const float a = m_h[h] == -INFINITY ? 0.f : rc::fast_exp2(m_h[h] - mb);
+                w_h[h] *= a;
+#pragma unroll
+                for (int k = 0; k < D / 32; ++k) acc[h][k] *= a;
+                m_h[h] = mb;
+            }
+#pragma unroll 4
+            for (int j = 0; j < nb; ++j) {
+                const int64_t row = sRow[j];
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    const float w = sW[h * kPB + jj];
+                    const float l2 = sL[h * kPB + j];
+                    const float wj = l2 == -INFINITY ? 0.f : rc::fast_exp2(l2 - m_h[h]);
+                    w_h[h] += wj;
                     const float* src = p.seg_o + (row + (int64_t)(kvh * G + h) * sc) * D + lane;
 #pragma unroll
                     for (int k = 0; k < D / 32; ++k) {
                         const float v = src[32 * k];
-                        acc[h][k] += w == 0.f ? 0.f : w * v;
+                        acc[h][k] += wj == 0.f ? 0.f : wj * v;
                     }
                 }
             }
@@ -488,12 +480,12 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta, kCtasPerSm) decode_split_ke
 #pragma unroll
         for (int h = 0; h < G; ++h) {
             const int64_t orow = (int64_t)b * p.q_heads + kvh * G + h;
+            const float inv = w_h[h] > 0.f ? 1.f / w_h[h] : 0.f;
 #pragma unroll
             for (int k = 0; k < D / 32; ++k)
-                p.out[orow * D + lane + 32 * k] = __float2bfloat16_rn(acc[h][k]);
+                p.out[orow * D + lane + 32 * k] = __float2bfloat16_rn(acc[h][k] * inv);
             if (p.lse && lane == 0)
-                p.lse[orow] = sHead[2 * h + 1] > 0.f ? (sHead[2 * h] - log2f(sHead[2 * h + 1])) * rc::kLn2
-                                                     : -INFINITY;
+                p.lse[orow] = w_h[h] > 0.f ? (m_h[h] + log2f(w_h[h])) * rc::kLn2 : -INFINITY;
         }
     }
 }
@@ -528,32 +520,57 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
     const bool casc_ok = !(err && (*reinterpret_cast<volatile int32_t*>(err) & rc::kErrTimeout));
     const int s0 = req_seg_indptr && casc_ok ? req_seg_indptr[b] : 0;
     const int ns = req_seg_indptr && casc_ok ? req_seg_indptr[b + 1] - s0 : 0;
-    float m = -INFINITY;
-    for (int i = 0; i < ns; ++i)
-        for (int c = 0; c < seg_chunks; ++c)
-            m = fmaxf(m, seg_lse[((int64_t)req_seg_pos[s0 + i] * q_heads + h) * seg_chunks + c]);
-    for (int c = 0; c < nc; ++c) m = fmaxf(m, tail_lse[(int64_t)bh * n_chunks + c]);
+    // partials j < ns * seg_chunks: cascade (segment entry j / seg_chunks,
+    // chunk j % seg_chunks); then the nc chunks of the row's own table part.
+    // Batches of 32: lane j loads partial j's log-sum-exp (one round), then
+    // every lane reads the batch's rows (independent loads), merged online.
+    const int n_all = ns * seg_chunks + nc;
+    __shared__ float sL[32];
+    __shared__ const float* sSrc[32];
+    float m = -INFINITY, wsum = 0.f;
     float acc[PER];
 #pragma unroll
     for (int j = 0; j < PER; ++j) acc[j] = 0.f;
-    float wsum = 0.f;
-    for (int i = 0; i < ns; ++i) {
-        for (int c = 0; c < seg_chunks; ++c) {
-            const int64_t row = ((int64_t)req_seg_pos[s0 + i] * q_heads + h) * seg_chunks + c;
-            const float l2 = seg_lse[row];
-            if (l2 == -INFINITY) continue;
-            const float w = rc::fast_exp2(l2 - m);
-            wsum += w;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) acc[j] += w * seg_o[row * D + lane + 32 * j];
+    for (int j0 = 0; j0 < n_all; j0 += 32) {
+        const int nb = min(32, n_all - j0);
+        if (lane < nb) {
+            const int j = j0 + lane;
+            int64_t row;
+            const float* base;
+            const float* lbase;
+            if (j < ns * seg_chunks) {
+                row = ((int64_t)req_seg_pos[s0 + j / seg_chunks] * q_heads + h) * seg_chunks + j % seg_chunks;
+                base = seg_o;
+                lbase = seg_lse;
+            } else {
+                row = (int64_t)bh * n_chunks + (j - ns * seg_chunks);
+                base = tail_o;
+                lbase = tail_lse;
+            }
+            sL[lane] = lbase[row];
+            sSrc[lane] = base + row * D;
         }
-    }
-    for (int c = 0; c < nc; ++c) {
-        const int64_t row = (int64_t)bh * n_chunks + c;
-        const float w = rc::fast_exp2(tail_lse[row] - m);
-        wsum += w;
+        __syncwarp();
+        float mb = m;
+        for (int j = 0; j < nb; ++j) mb = fmaxf(mb, sL[j]);
+        if (mb != -INFINITY) {
+            const float a = m == -INFINITY ? 0.f : rc::fast_exp2(m - mb);
+            wsum *= a;
 #pragma unroll
-        for (int j = 0; j < PER; ++j) acc[j] += w * tail_o[row * D + lane + 32 * j];
+            for (int k = 0; k < PER; ++k) acc[k] *= a;
+            m = mb;
+#pragma unroll 4
+            for (int j = 0; j < nb; ++j) {
+                const float l2 = sL[j];
+                if (l2 == -INFINITY) continue;
+                const float w = rc::fast_exp2(l2 - m);
+                wsum += w;
+                const float* src = sSrc[j] + lane;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) acc[k] += w * src[32 * k];
+            }
+        }
+        __syncwarp();
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
 #pragma unroll
