@@ -301,15 +301,12 @@ def torch_empty_like(torch, t):
 # -------------------------------------------------------------- algorithmic
 # DRAM traffic of one attn_decode call over its algorithmic bytes, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum of the cascade and the
-# table-pass kernel) of this workload's decode steps 125 and 126: 211.78 MB and
-# 212.95 MB of DRAM traffic for 195.77 MB and 196.82 MB of algorithmic bytes.
-# Traffic grows with the keys read, so the ratio scales it to the average call.
-# That capture predates the cascade kernel's CTA-wide barrier at entry (no
-# memory access added or removed); until the counters are taken again on the
-# kernel as it stands, the line reports traffic as null and this ratio in a
-# note.
-DECODE_TRAFFIC_RATIO = 1.0818
-DECODE_TRAFFIC_CURRENT = False
+# table-pass kernel) of this workload's decode steps 124 and 125, kernels as
+# they stand: 212.40 MB and 213.44 MB of DRAM traffic for 194.72 MB and
+# 195.77 MB of algorithmic bytes.  Traffic grows with the keys read, so the
+# ratio scales it to the average call.
+DECODE_TRAFFIC_RATIO = 1.0905
+DECODE_TRAFFIC_CURRENT = True
 
 
 def row_bytes(shape):
