@@ -597,12 +597,14 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     const int64_t sms = rc_host::sm_count();
     // Table part: one warp per (row, KV head) when that already gives every
     // SM eight warps (the merge is then fused); otherwise split the keys so
-    // that there are about sixteen warps per SM.
+    // that the items just fill one wave of CTAs (a warp's time grows with its
+    // tiles, about 2.5 us per 16 keys when the gather saturates HBM, so the
+    // wave's longest item sets the call), down to 64 keys per chunk.
     const int64_t base = (int64_t)batch * hkv;
     int64_t splits = 1;
     if (base < 8 * sms) {
-        splits = base > 0 ? (16 * sms + base - 1) / base : 1;
-        const int64_t max_splits = max_len > 0 ? (max_len + 255) / 256 : 1;
+        splits = base > 0 ? (kWarpsPerCta * sms) / base : 1;
+        const int64_t max_splits = max_len > 0 ? (max_len + kDecKeys - 1) / kDecKeys : 1;
         if (splits > max_splits) splits = max_splits;
         if (splits < 1) splits = 1;
     }
@@ -612,7 +614,13 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
     pl->n_chunks = max_len > 0 ? (int)((max_len + chunk - 1) / chunk) : 1;
     pl->fused = pl->n_chunks == 1;
     // Cascade part: split each segment's keys so that the grid fills the SMs
-    // once (one CTA per SM: a second, partial wave would double the time).
+    // once (one CTA per SM: a second, partial wave would double the time),
+    // and in any case so that no CTA takes more than about kSegKeys keys: a
+    // CTA's time grows with its tiles, and with many segments (a grid of
+    // several waves anyway) a long one would otherwise run all its keys in
+    // one CTA while the short ones finish early.  Chunks past a segment's end
+    // are empty CTAs that leave at once.
+    constexpr int64_t kSegKeys = 512;
     pl->seg_chunk = 0;
     pl->seg_chunks = 1;
     if (casc && casc->n_seg > 0 && casc->max_seg_len > 0) {
@@ -620,6 +628,8 @@ rc_status plan_decode(const rc_attn_desc* d, int32_t batch, int32_t max_len, con
         const int64_t row_blocks = (casc->max_seg_rows * (int64_t)G + rc_tc2::ROWS - 1) / rc_tc2::ROWS;
         const int64_t cbase = (int64_t)casc->n_seg * row_blocks * hkv;
         int64_t sc = cbase > 0 ? sms / cbase : 1;
+        const int64_t sc_len = (casc->max_seg_len + kSegKeys - 1) / kSegKeys;
+        if (sc < sc_len) sc = sc_len;
         const int64_t sc_max = (casc->max_seg_len + 255) / 256;
         if (sc > sc_max) sc = sc_max;
         if (sc < 1) sc = 1;
