@@ -189,15 +189,30 @@ class ReplayModel:
         torch = self.torch
         e = self.ready[key]
         pin = lambda t: t.cpu().pin_memory() if t is not None else None
-        e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()},
-                     "dec": {k: pin(v) for k, v in e["dec"].items()}}
+        e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()}}
         e["ext"] = {k: (torch_empty_like(torch, v)) for k, v in e["ext"].items()}
         K = self.CHUNK
-        e["ring"] = {k: (torch.empty((2 * K,) + tuple(v.shape[1:]), dtype=v.dtype, device=v.device)
-                         if v is not None else None) for k, v in e["dec"].items()}
+        # a step's q, k and v side by side in one row of bytes (each part
+        # 256-byte aligned): a chunk of steps is one contiguous copy
+        dec = {k: v for k, v in e["dec"].items() if v is not None}
+        T = next(iter(dec.values())).shape[0] if dec else 0
+        parts, off = {}, 0
+        for k, v in dec.items():
+            n = v[0].numel() * v.element_size()
+            parts[k] = (off, n)
+            off += (n + 255) // 256 * 256
+        host = torch.empty(T, off, dtype=torch.uint8).pin_memory()
+        for k, v in dec.items():
+            o, n = parts[k]
+            host[:, o:o + n].copy_(v.reshape(T, -1).view(torch.uint8).cpu())
+        e["host"]["dec"] = host
+        e["dec_step_bytes"] = off
+        ring = torch.empty(2 * K, off, dtype=torch.uint8, device=self.base.device)
+        e["ring"] = ring
         # the step inputs as views of the ring, built once (indexing a tensor
         # costs host time on every decode step otherwise)
-        e["views"] = [{k: (ring[h] if ring is not None else None) for k, ring in e["ring"].items()}
+        e["views"] = [{k: (ring[h, parts[k][0]:parts[k][0] + parts[k][1]].view(v.dtype).view(v.shape[1:])
+                           if k in dec else None) for k, v in e["dec"].items()}
                       for h in range(2 * K)]
         e["moved"] = {}          # chunk -> event on the copy stream (its copy is done)
         e["ext_moved"] = None    # event: the prefill inputs are on the device
@@ -222,7 +237,8 @@ class ReplayModel:
         on the copy stream, after the compute stream is done with chunk c-2."""
         torch = self.torch
         K = self.CHUNK
-        T = next(v for v in e["host"]["dec"].values() if v is not None).shape[0]
+        host = e["host"]["dec"]
+        T = host.shape[0]
         a, b = c * K, min(T, (c + 1) * K)
         if a >= T:
             return
@@ -230,11 +246,8 @@ class ReplayModel:
         free.record(torch.cuda.current_stream())
         self.h2d.wait_event(free)
         with torch.cuda.stream(self.h2d):
-            for k, ring in e["ring"].items():
-                if ring is not None:
-                    src = e["host"]["dec"][k][a:b]
-                    ring[(c % 2) * K:(c % 2) * K + (b - a)].copy_(src, non_blocking=True)
-                    self.h2d_bytes += src.numel() * src.element_size()
+            e["ring"][(c % 2) * K:(c % 2) * K + (b - a)].copy_(host[a:b], non_blocking=True)
+        self.h2d_bytes += (b - a) * e["dec_step_bytes"]
         ev = torch.cuda.Event()
         ev.record(self.h2d)
         e["moved"][c] = ev

@@ -399,6 +399,43 @@ rc_status attn_decode_append(const rc_attn_desc* desc, const void* q, const void
                              const rc_cascade* cascade, void* out, float* lse, void* ws,
                              size_t ws_bytes, rc_stream_t stream);
 
+/* One decode step of a run handed to attn_decode_steps.  len, max_len: the
+ * step's row lengths (device) and their host bound, replacing kv->len and
+ * kv->max_len.  store_slots: NULL, or [batch] device slot ids that kv_store
+ * fills from k_new/v_new before the step's attention (the latent layout, the
+ * FP8 pool).  With store_slots NULL and k_new set the step is an
+ * attn_decode_append; with both NULL a plain attn_decode.  ev_begin/ev_end:
+ * NULL or a cudaEvent_t recorded on the stream before the step's first launch
+ * and after its last (per-step timing). */
+typedef struct rc_decode_step {
+    const void* q;
+    const void* k_new;
+    const void* v_new;
+    const int32_t* store_slots;
+    void* out;
+    float* lse;
+    const int32_t* len;
+    int32_t max_len;
+    void* ev_begin;
+    void* ev_end;
+} rc_decode_step;
+
+/* n_steps decode steps of one batch queued by one call: for step i, in
+ * order, its store (if any) and its attn_decode / attn_decode_append, each
+ * with the arguments above and the batch's shared table rows, cascade and
+ * workspace (sized by attn_decode_workspace for the largest max_len).  The
+ * steps are launched exactly as the per-step calls would launch them, so the
+ * results are those calls' results bit for bit.  The pages describe the
+ * decode phase as a loop of one-token steps [LMI decode phase] and a
+ * scheduler that keeps the host's work off the GPU's critical path [SGLang
+ * engineering article, section 2: the overlap scheduler]; this call takes the
+ * per-step host work of that loop down to filling one array.  n_done: NULL or
+ * receives the steps queued before the first error (all of them on
+ * RC_OK); the first error's status is returned. */
+rc_status attn_decode_steps(const rc_attn_desc* desc, const rc_kv_table* kv, int32_t batch,
+                            const rc_cascade* cascade, const rc_decode_step* steps, int32_t n_steps,
+                            void* ws, size_t ws_bytes, rc_stream_t stream, int32_t* n_done);
+
 /* attn_decode without any device allocation, for callers that cannot call
  * cudaMalloc or hand over a workspace: for example a serving loop whose
  * device memory is all carved up at start-up (the KV pool takes what is left)

@@ -52,6 +52,11 @@ class rc_cascade(C.Structure):
                 ("total_seg_rows", I32)]
 
 
+class rc_decode_step(C.Structure):
+    _fields_ = [("q", VP), ("k_new", VP), ("v_new", VP), ("store_slots", VP), ("out", VP), ("lse", VP),
+                ("len", VP), ("max_len", I32), ("ev_begin", VP), ("ev_end", VP)]
+
+
 class rc_request(C.Structure):
     _fields_ = [("tokens", VP), ("prompt_len", I64), ("max_new", I64), ("slots", VP), ("matched", I64),
                 ("first", I64), ("node", I64), ("admitted", I32)]
@@ -89,6 +94,8 @@ SIGNATURES = {
     "attn_decode": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP, C.c_size_t, VP]),
     "attn_decode_append": (I32, [P(rc_attn_desc), VP, VP, VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP,
                                  C.c_size_t, VP]),
+    "attn_decode_steps": (I32, [P(rc_attn_desc), P(rc_kv_table), I32, P(rc_cascade), P(rc_decode_step), I32, VP,
+                                C.c_size_t, VP, P(I32)]),
     "attn_decode_static": (I32, [P(rc_attn_desc), VP, P(rc_kv_table), I32, P(rc_cascade), VP, VP, VP]),
     "attn_extend_workspace": (I32, [P(rc_attn_desc), I32, I32, I32, P(C.c_size_t)]),
     "attn_extend": (I32, [P(rc_attn_desc), VP, VP, P(rc_kv_table), I32, I32, VP, VP, VP, C.c_size_t, VP]),
@@ -503,6 +510,26 @@ def attn_decode_append(desc: rc_attn_desc, q, k_new, v_new, kv: rc_kv_table, bat
                                   C.byref(cascade) if cascade is not None else None, _tp(out), _tp(lse), _tp(ws),
                                   int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream))
     _check("attn_decode_append", st)
+
+
+def attn_decode_steps(desc: rc_attn_desc, kv: rc_kv_table, batch: int, steps, ws=None,
+                      cascade: rc_cascade | None = None, stream=None):
+    """Several decode steps of one batch in one call.  steps: a list of dicts
+    with q, out and len (tensors), max_len (int), and optionally k_new/v_new,
+    store_slots, lse (tensors): each step as attn_decode_append (k_new given),
+    kv_store + attn_decode (store_slots given) or attn_decode (see the header)."""
+    arr = (rc_decode_step * max(len(steps), 1))()
+    for i, s in enumerate(steps):
+        a = arr[i]
+        a.q, a.out, a.len, a.max_len = _tp(s["q"]), _tp(s["out"]), _tp(s["len"]), int(s["max_len"])
+        a.k_new, a.v_new = _tp(s.get("k_new")), _tp(s.get("v_new"))
+        a.store_slots, a.lse = _tp(s.get("store_slots")), _tp(s.get("lse"))
+    done = I32(0)
+    st = lib().attn_decode_steps(C.byref(desc), C.byref(kv), int(batch),
+                                 C.byref(cascade) if cascade is not None else None, arr, len(steps), _tp(ws),
+                                 int(ws.numel() * ws.element_size()) if ws is not None else 0, _stream(stream),
+                                 C.byref(done))
+    _check("attn_decode_steps", st)
 
 
 def attn_decode_static(desc: rc_attn_desc, q, kv: rc_kv_table, batch: int, out, lse=None,

@@ -873,6 +873,35 @@ extern "C" rc_status attn_decode_append(const rc_attn_desc* desc, const void* q,
     return decode_impl(desc, q, k_new, v_new, kv, batch, casc, out, lse, ws, ws_bytes, stream);
 }
 
+extern "C" rc_status attn_decode_steps(const rc_attn_desc* desc, const rc_kv_table* kv, int32_t batch,
+                                       const rc_cascade* casc, const rc_decode_step* steps, int32_t n_steps,
+                                       void* ws, size_t ws_bytes, rc_stream_t stream, int32_t* n_done) {
+    if (n_done) *n_done = 0;
+    if (!desc || !kv || n_steps < 0 || (n_steps > 0 && !steps)) return RC_ERR_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int32_t i = 0; i < n_steps; ++i) {
+        const rc_decode_step& s = steps[i];
+        if (s.ev_begin && cudaEventRecord((cudaEvent_t)s.ev_begin, st) != cudaSuccess) return RC_ERR_CUDA;
+        rc_kv_table t = *kv;
+        t.len = s.len;
+        t.max_len = s.max_len;
+        rc_status r;
+        if (s.store_slots) {
+            r = kv_store(&desc->pool, s.store_slots, s.k_new, s.v_new, batch, nullptr, nullptr, stream);
+            if (r == RC_OK) r = attn_decode(desc, s.q, &t, batch, casc, s.out, s.lse, ws, ws_bytes, stream);
+        } else if (s.k_new) {
+            r = attn_decode_append(desc, s.q, s.k_new, s.v_new, &t, batch, casc, s.out, s.lse, ws, ws_bytes,
+                                   stream);
+        } else {
+            r = attn_decode(desc, s.q, &t, batch, casc, s.out, s.lse, ws, ws_bytes, stream);
+        }
+        if (r != RC_OK) return r;
+        if (s.ev_end && cudaEventRecord((cudaEvent_t)s.ev_end, st) != cudaSuccess) return RC_ERR_CUDA;
+        if (n_done) *n_done = i + 1;
+    }
+    return RC_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Allocation-free variant.  The split partials go to a file-scope device
 // array instead of a caller workspace.  In host code the array's name is only

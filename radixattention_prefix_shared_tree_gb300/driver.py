@@ -31,7 +31,7 @@ import numpy as np
 
 from . import (RC_COMMIT_FINISH, RC_COMMIT_PREFILL, RC_ERR_NOMEM, RC_FCFS, RC_LPM, RC_OK, RCError, attn_decode,
                attn_decode_workspace, attn_extend, kv_store, lib, make_attn_desc, make_cascade, make_kv_table,
-               make_pool_desc, rc_request)
+               make_pool_desc, rc_decode_step, rc_request)
 
 
 @dataclass
@@ -333,9 +333,13 @@ class DeviceEngine:
         self._ev_pool = []
 
     def start_timing(self, n_events: int = 4096):
-        """Record CUDA events around device calls, from a pool made up front."""
+        """Record CUDA events around device calls, from a pool made up front
+        (each recorded once here, so its CUDA handle exists and the library
+        can record it too)."""
         self.events = {}
         self._ev_pool = [self.torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+        for e in self._ev_pool:
+            e.record()
         self._ev_next = 0
         self.timing = True
 
@@ -344,7 +348,9 @@ class DeviceEngine:
             e = self._ev_pool[self._ev_next]
             self._ev_next += 1
             return e
-        return self.torch.cuda.Event(enable_timing=True)
+        e = self.torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
 
     def _call(self, name, kernels, info, fn):
         if self.timing:
@@ -424,7 +430,8 @@ class DeviceEngine:
         casc = lay.casc if lay.use_cascade else None
         lay.kv_tables = None
         dec_max = lay.dec_max.tolist() if T else []
-        lay.ws_bytes = self._decode_ws(B, set(dec_max), casc)
+        # the workspace attn_decode plans grows with max_len: size it for the largest
+        lay.ws_bytes = self._decode_ws(B, [max(dec_max)] if dec_max else [], casc)
         lay.ws = self.workspace(lay.ws_bytes)
         lay.ws_ptr = lay.ws.data_ptr()
         lay.casc_ref = C.byref(casc) if casc is not None else None
@@ -452,6 +459,7 @@ class DeviceEngine:
             split = B * self.shape.kv_heads < 8 * sms
         lay.decode_kernels = (1 if casc is not None else 0) + 1 + (1 if split else 0)
         lay.stream = C.c_void_p(self.torch.cuda.current_stream(self.device).cuda_stream)
+        lay.step_arr = None
 
     def _decode_ws(self, B: int, max_lens, casc) -> int:
         """Largest workspace attn_decode asks for over the steps' bounds."""
@@ -502,6 +510,44 @@ class DeviceEngine:
             ev[1].record()
             self.events.setdefault("attn_decode", []).append((ev[0], ev[1], ("decode", lay, t)))
         self.launches += kernels
+
+    def decode_steps(self, lay, t0: int, ins, outs, lses=None):
+        """Decode steps t0 .. t0+n-1 of the batch in one library call
+        (attn_decode_steps): the launches decode_step makes for each step,
+        in the same order, queued by one C call.  ins[i]: step t0+i's q/k/v;
+        outs[i], lses[i]: where it writes."""
+        n = len(ins)
+        arr = lay.step_arr
+        if arr is None or len(arr) < n:
+            arr = lay.step_arr = (rc_decode_step * max(n, 16))()
+        fused = self.fuse_store
+        timed = []
+        for i in range(n):
+            t = t0 + i
+            inp, a = ins[i], arr[i]
+            k, v = inp["k"], inp["v"]
+            a.q = inp["q"].data_ptr()
+            a.out = outs[i].data_ptr()
+            a.lse = lses[i].data_ptr() if lses is not None else None
+            a.len = lay.len_ptrs[t]
+            a.max_len = lay.dec_max_list[t]
+            a.k_new = k.data_ptr()
+            a.v_new = v.data_ptr() if v is not None else None
+            a.store_slots = None if fused and v is not None else lay.slot_ptrs[t]
+            if self.timing and t % self.timing_every == 0:
+                e0, e1 = self._event(), self._event()
+                a.ev_begin, a.ev_end = e0.cuda_event, e1.cuda_event
+                timed.append((e0, e1, ("decode", lay, t)))
+            else:
+                a.ev_begin = a.ev_end = None
+        st = self._lib.attn_decode_steps(lay.desc_ref, lay.kv_ref, lay.batch_size, lay.casc_ref, arr, n,
+                                         lay.ws_ptr, lay.ws_bytes, lay.stream, None)
+        if st != RC_OK:
+            raise RCError("attn_decode_steps", st)
+        if timed:
+            self.events.setdefault("attn_decode", []).extend(timed)
+        per = lay.decode_kernels if fused and ins[0]["v"] is not None else 1 + lay.decode_kernels
+        self.launches += n * per
 
     def decode(self, lay, t: int, q, out, lse=None):
         kv, casc = lay.decode_table(t)

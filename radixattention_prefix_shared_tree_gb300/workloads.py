@@ -43,6 +43,7 @@ class Runner:
         self.on_decode = None   # optional callback(out, t, n_steps) after each decode step
         self.on_extend = None   # optional callback(out) after the prefill
         self.decode_out_slots = 1  # decode step t writes slot t mod this of `decode_outs`
+        self.decode_chunk = 16     # decode steps queued per library call
         self.decode_outs = None
 
     def request(self, prompt, max_new: int) -> Request:
@@ -149,32 +150,51 @@ class Runner:
         return lay
 
     def _decode_steps(self, batch, lay):
+        """Every decode step of the batch, in runs of up to `decode_chunk`
+        steps (aligned to multiples of it), each run queued by one library
+        call (attn_decode_steps); decode_chunk = 1 makes one decode_step call
+        per step.  Step t writes slot t mod R of `decode_outs`."""
         eng, torch = self.engine, self.engine.torch
         sh = eng.shape
-        B = len(batch)
+        B, T = len(batch), lay.max_new
+        CH = max(1, self.decode_chunk)
         R = max(1, self.decode_out_slots)
+        if self.collect:
+            R = max(R, CH)     # a run's outputs are read after the run
         outs = torch.empty(R, B, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16, device=eng.device)
         self.decode_outs = outs
         views = [outs[i] for i in range(R)]
-        lse = torch.empty(B, sh.q_heads, dtype=torch.float32, device=eng.device) if self.collect else None
+        lses = None
+        idx = None
+        if self.collect:
+            ring = torch.empty(R, B, sh.q_heads, dtype=torch.float32, device=eng.device)
+            lses = [ring[i] for i in range(R)]
+            if self.collect_rids is None:
+                idx = list(range(B))
+            else:
+                idx = [i for i, r in enumerate(batch) if r.rid in self.collect_rids]
+            sel = torch.as_tensor(idx, device=eng.device) if idx else None
         eng.prepare_decode(lay)
-        for t in range(lay.max_new):
-            out = views[t % R]
-            inp = self.model.decode_inputs(batch, t)
-            eng.decode_step(lay, t, inp["q"], inp["k"], inp["v"], out, lse)
-            if self.on_decode is not None:
-                self.on_decode(out, t, lay.max_new)
-            if self.collect:
-                if self.collect_rids is None:
-                    idx = list(range(B))
-                else:
-                    idx = [i for i, r in enumerate(batch) if r.rid in self.collect_rids]
+        t = 0
+        while t < T:
+            n = min(CH - t % CH, T - t)
+            ins = [self.model.decode_inputs(batch, t + i) for i in range(n)]
+            ov = [views[(t + i) % R] for i in range(n)]
+            lv = [lses[(t + i) % R] for i in range(n)] if lses is not None else None
+            if CH == 1:
+                inp = ins[0]
+                eng.decode_step(lay, t, inp["q"], inp["k"], inp["v"], ov[0], lv[0] if lv else None)
+            else:
+                eng.decode_steps(lay, t, ins, ov, lv)
+            for i in range(n):
+                if self.on_decode is not None:
+                    self.on_decode(ov[i], t + i, T)
                 if idx:
-                    sel = torch.as_tensor(idx, device=out.device)
-                    o = out.index_select(0, sel).view(torch.int16).cpu().numpy().view(np.uint16)
-                    l = lse.index_select(0, sel).cpu().numpy()
-                    for j, i in enumerate(idx):
-                        self.decode_out.setdefault(batch[i].rid, []).append((batch[i].prompt_len + t, o[j], l[j]))
+                    o = ov[i].index_select(0, sel).view(torch.int16).cpu().numpy().view(np.uint16)
+                    l = lv[i].index_select(0, sel).cpu().numpy()
+                    for j, b in enumerate(idx):
+                        self.decode_out.setdefault(batch[b].rid, []).append((batch[b].prompt_len + t + i, o[j], l[j]))
+            t += n
 
 
 # ------------------------------------------------------------------ workloads

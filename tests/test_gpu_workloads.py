@@ -282,3 +282,42 @@ def test_overlapped_rounds_equal_serial(cuda, which):
     assert a[0].keys() == b[0].keys() and a[1].keys() == b[1].keys() and a[2] == b[2]
     assert all(np.array_equal(a[0][k], b[0][k]) for k in a[0])
     assert all(np.array_equal(a[1][k], b[1][k]) for k in a[1])
+
+
+@pytest.mark.parametrize("which", ["few_shot_cascade", "few_shot_flat", "few_shot_fp8", "mla"])
+def test_decode_runs_equal_single_steps(cuda, which):
+    """Runs of decode steps queued by one library call (attn_decode_steps;
+    runs of 5 leave ragged ends) against one decode_step call per step:
+    every decode output and LSE bit for bit, and the per-step CUDA events
+    the runs record themselves time every 4th step."""
+    got = []
+    for chunk in (1, 5, 16):
+        if which == "mla":
+            tr = traces.mla_long(batch=6, shared_len=300, private_max=900, steps=23)
+            fn, pool, cascade, fp8 = wl.run_mla, tr.pool_slots, False, False
+        else:
+            tr = traces.few_shot(n_questions=24, max_new=23)
+            fn, pool = wl.run_few_shot, 1 << 16
+            cascade, fp8 = which != "few_shot_flat", which == "few_shot_fp8"
+        model = SynthModel(tr.shape, tr.seed, tr.vocab, device=cuda)
+        eng = DeviceEngine(tr.shape, pool, device=cuda, kv_fp8=fp8)
+        runner = wl.Runner(ra.RadixCache(pool), model, eng, cascade=cascade, collect=True,
+                           prefill_attention=not tr.shape.mla)
+        runner.decode_chunk = chunk
+        eng.timing_every = 4
+        eng.start_timing(512)
+        fn(runner, tr)
+        assert ra.rc_sync(eng.err) == ra.RC_OK
+        assert runner.last_layout.use_cascade == cascade
+        eng.torch.cuda.synchronize()
+        evs = eng.events["attn_decode"]
+        assert [info[2] for _, _, info in evs] == list(range(0, 23, 4))
+        assert all(a.elapsed_time(b) > 0 for a, b, _ in evs)
+        got.append({rid: (np.stack([o for _, o, _ in d]), np.stack([l for _, _, l in d]))
+                    for rid, d in runner.decode_out.items()})
+    base = got[0]
+    assert len(base) == (6 if which == "mla" else 24)
+    for other in got[1:]:
+        assert other.keys() == base.keys()
+        for rid in base:
+            assert np.array_equal(other[rid][0], base[rid][0]) and np.array_equal(other[rid][1], base[rid][1])
