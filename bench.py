@@ -254,11 +254,14 @@ class ReplayModel:
 
     def prefetch_extend(self, key):
         """Queue a later batch's prefill inputs on their own copy stream (they
-        move while the current batch decodes)."""
+        move while the current batch decodes), and its first chunk of decode
+        inputs into its ring."""
         torch = self.torch
         e = self.ready[key]
         if "host" not in e or e["ext_moved"] is not None:
             return
+        if e["host"]["dec"].shape[0] and 0 not in e["moved"]:
+            self._move_chunk(e, 0)
         with torch.cuda.stream(self.h2d_ext):
             for k, v in e["ext"].items():
                 if v is not None:
@@ -792,6 +795,7 @@ def run_config(args, name, rank, world, local):
         home = OutputsHome(torch, None, model.CHUNK, ext_rows if opts["prefill_attention"] else 1,
                            max(len(b) for b in batches), sh)
         model.h2d_bytes = 0
+        link0 = link_rates(torch)
         gc.collect()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -809,6 +813,7 @@ def run_config(args, name, rank, world, local):
         e2e = {"value": whole_job_rate(args.steps * n_dec, world, ems), "unit": UNIT,
                "h2d_bytes_per_step": model.h2d_bytes // args.steps, "d2h_bytes_per_step": home.bytes // args.steps,
                "ms_per_step": ems / args.steps, "host_queue_ms_per_step": 1e3 * host_s / args.steps}
+        e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
 
     cpu = None
     if rank == 0 and world == 1:
@@ -831,6 +836,49 @@ def run_config(args, name, rank, world, local):
 
 
 # ---------------------------------------------------------------- replicas
+def link_rates(torch, nbytes: int = 256 << 20, reps: int = 3) -> dict:
+    """Pinned host <-> device copy rates right now (GB/s, CUDA events): each
+    direction alone and both at once on two streams.  The e2e leg moves its
+    inputs and outputs over this link, which the host's other GPU and its
+    users share: the rates, taken before and after the leg, say how much of
+    the e2e time the link alone explains."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_out = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    cur = torch.cuda.current_stream()
+    streams = (torch.cuda.Stream(), torch.cuda.Stream())
+    copies = (lambda: d_in.copy_(h_in, non_blocking=True), lambda: h_out.copy_(d_out, non_blocking=True))
+
+    def run(which):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cur)
+        for i in which:
+            streams[i].wait_stream(cur)
+            with torch.cuda.stream(streams[i]):
+                for _ in range(reps):
+                    copies[i]()
+        for i in which:
+            cur.wait_stream(streams[i])
+        b.record(cur)
+        torch.cuda.synchronize()
+        return reps * nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+
+    run((0, 1))
+    return {"h2d": run((0,)), "d2h": run((1,)), "both_each_way": run((0, 1))}
+
+
+def link_summary(before: dict, after: dict, h2d_bytes: int, d2h_bytes: int) -> dict:
+    """The link rates around an e2e leg and the time its copies alone need
+    per step at the slower of the two readings: each direction alone, and
+    both directions at once."""
+    lo = {k: min(before[k], after[k]) for k in before}
+    alone = max(h2d_bytes / lo["h2d"], d2h_bytes / lo["d2h"]) / 1e6
+    both = max(h2d_bytes, d2h_bytes) / lo["both_each_way"] / 1e6
+    return {"gbs_before": before, "gbs_after": after,
+            "copy_ms_per_step": {"directions_alone": alone, "both_at_once": both}}
+
+
 def slowest_rank(ms: float, world: int, device) -> float:
     """The job's time over N replicas: every rank times the same region
     (barriers on both sides) and the slowest one counts.  One all-reduce of
@@ -1242,6 +1290,7 @@ def main():
         runner.on_decode = copy_decode
         runner.on_extend = copy_extend
         model.h2d_bytes = 0
+        link0 = link_rates(torch)
         gc.collect()
         gc.freeze()
         if world > 1:
@@ -1261,6 +1310,7 @@ def main():
         e2e = {"value": whole_job_rate(n_e2e * args.questions * args.max_new, world, ems), "unit": UNIT,
                "h2d_bytes_per_step": model.h2d_bytes // n_e2e, "d2h_bytes_per_step": d2h[0] // n_e2e,
                "ms_per_step": ems / n_e2e, "host_queue_ms_per_step": 1e3 * host_s / n_e2e}
+        e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
 
     cpu = None
     if rank == 0 and world == 1:
