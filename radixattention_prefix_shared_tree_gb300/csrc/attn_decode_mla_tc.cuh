@@ -28,6 +28,11 @@
 // tile t+1 has landed, whichever comes first.  Every wait is bounded and
 // flags RC_ERR_TIMEOUT when it gives up; a parity wait never has three
 // possible phases (see the last-tile handling).
+// The MMA thread and the producers issue back to back and share their
+// sub-partitions with the other warps, so their instructions are kept few:
+// the descriptors of a tile are built once and stepped along K by 32-bit
+// adds, and a producer lane's 18 copies of a row carry their offsets as
+// immediates (measured on the GB300: 1.78 -> 1.56 ms per full-size step).
 #pragma once
 
 #include "tc.cuh"
@@ -331,12 +336,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
                     slot = 0;
                     bytes = 0;
                 }
-                const __nv_bfloat16* src = p.pool + (int64_t)slot * DK;
-#pragma unroll 6
-                for (int cg = 0; cg < CK / 4; ++cg) {
-                    const int c = cg * 4 + csub;
-                    rc::cp_async16(rc::smem_u32(sT + tc::cm_offset(key, c, CK)), src + c * 8, bytes);
-                }
+                // chunks c = 4 cg + csub: 512 bytes apart in the stage, 64 in the row
+                const __nv_bfloat16* src = p.pool + (int64_t)slot * DK + csub * 8;
+                rc::cp_async16_run<512, 64>(rc::smem_u32(sT + tc::cm_offset(key, csub, CK)), src, bytes,
+                                            std::make_integer_sequence<int, CK / 4>{});
             }
             tc::cp_async_mbar_arrive(&kv_full[s]);
             // the rows of this warp's next tile (NS tiles on) start for L2 now
@@ -349,18 +352,19 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
     } else if (lane == 0) {
         // ================================================ MMA (one thread)
         const uint32_t q0 = rc::smem_u32(sQ);
+        const tc::Desc qd = tc::desc_halves(q0, 128, SBQ);
         auto issue_s = [&](int t) {
-            const uint32_t k0s = rc::smem_u32(sKV + (t % NS) * TILE_BYTES);
+            const tc::Desc kd = tc::desc_halves(rc::smem_u32(sKV + (t % NS) * TILE_BYTES), 128, SB);
             const uint32_t d = tbase + (t & 1) * TN;
-            // Q columns 0..383 from TMEM (8 columns per K step of 16)
-#pragma unroll 4
+            // Q columns 0..QT-1 from TMEM (8 columns per K step of 16), K
+            // steps 256 bytes apart in both operands
+#pragma unroll
             for (int k = 0; k < QT / 16; ++k)
-                tc::mma_bf16_ts(d, tbase + COL_Q + k * 8, tc::smem_desc(k0s + k * 256, 128, SB), idS, k > 0);
-            // columns 384..575 from shared memory
-#pragma unroll 4
+                tc::mma_bf16_ts_h(d, tbase + COL_Q + k * 8, kd.lo + k * 16, kd.hi, idS, k > 0);
+            // the rest of Q from shared memory
+#pragma unroll
             for (int k = 0; k < (DK - QT) / 16; ++k)
-                tc::mma_bf16(d, tc::smem_desc(q0 + k * 256, 128, SBQ),
-                             tc::smem_desc(k0s + (QT / 16 + k) * 256, 128, SB), idS, true);
+                tc::mma_bf16_h(d, qd.lo + k * 16, qd.hi, kd.lo + (QT / 16 + k) * 16, kd.hi, idS, 1u);
             tc::commit(&s_full[t & 1]);
         };
         ok = tc::mbar_wait(q_full, 0, kWaitIter);
@@ -376,11 +380,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
                 tc::fence_after();
                 // value half vh of the tile: columns [256 vh, 256 vh + 256) = chunks [32 vh, 32 vh + 32)
                 const int s = t % NS;
-                const uint32_t v0 = rc::smem_u32(sKV + s * TILE_BYTES) + vh * (DVH / 8) * 128;
+                const tc::Desc vd =
+                    tc::desc_halves(rc::smem_u32(sKV + s * TILE_BYTES) + vh * (DVH / 8) * 128, SB, 128);
 #pragma unroll
                 for (int j = 0; j < TN / 16; ++j)
-                    tc::mma_bf16_ts(tbase + COL_O, tbase + (t & 1) * TN + j * 8,
-                                    tc::smem_desc(v0 + j * 2 * SB, SB, 128), idPV, t > 0 || j > 0);
+                    tc::mma_bf16_ts_h(tbase + COL_O, tbase + (t & 1) * TN + j * 8, vd.lo + j * (2 * SB / 16), vd.hi,
+                                      idPV, (t > 0 || j > 0) ? 1u : 0u);
                 tc::commit(o_done);
                 tc::commit(&kv_empty[s]);
                 ++t;

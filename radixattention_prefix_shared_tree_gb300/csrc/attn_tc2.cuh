@@ -25,7 +25,10 @@
 // (P over their first 32 columns), O at +128.  The tensor core runs one
 // thread's MMAs in issue order, so S(t+2) overwrites P(t) only after P(t).V
 // has read it.  All hand-offs are mbarriers; every wait is bounded and a wait
-// that gives up flags RC_ERR_TIMEOUT.
+// that gives up flags RC_ERR_TIMEOUT.  The MMA thread builds each
+// operand's descriptor once and steps it along K with 32-bit adds, and the
+// producers' copies of a row carry their offsets as immediates, so neither
+// spends issue slots on address arithmetic.
 //
 // FP8 pool (E4M3 codes, one fp32 scale per (slot, KV head) row): the products
 // run in f16 (every E4M3 value is an f16 value; the bf16 queries convert
@@ -502,15 +505,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                     slot = 0;
                     bytes = 0;
                 }
-                const int64_t base = ((int64_t)slot * p.kv_heads + kvh) * D;
-#pragma unroll
-                for (int cg = 0; cg < CH / 4; ++cg) {
-                    const int c = cg * 4 + csub;
-                    rc::cp_async16(rc::smem_u32(sK + tc::cm_offset(key, c, CH)), p.pool_k + base + c * 8, bytes,
-                                   pol);
-                    rc::cp_async16(rc::smem_u32(sV + tc::cm_offset(key, c, CH)), p.pool_v + base + c * 8, bytes,
-                                   pol);
-                }
+                // chunks c = 4 cg + csub: 512 bytes apart in the stage, 64 in the row
+                const int64_t base = ((int64_t)slot * p.kv_heads + kvh) * D + csub * 8;
+                const uint32_t off = tc::cm_offset(key, csub, CH);
+                rc::cp_async16_run<512, 64>(rc::smem_u32(sK) + off, p.pool_k + base, bytes, pol,
+                                            std::make_integer_sequence<int, CH / 4>{});
+                rc::cp_async16_run<512, 64>(rc::smem_u32(sV) + off, p.pool_v + base, bytes, pol,
+                                            std::make_integer_sequence<int, CH / 4>{});
             }
             // each lane arrives on the stage's barrier when its copies have
             // landed; the warp goes on to the next tile at once
@@ -522,14 +523,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
     } else if (lane == 0) {
         // ================================================= MMA (warp 8+NP)
+        // descriptors built once per operand and stepped along K by 32-bit adds
+        const tc::Desc qd = tc::desc_halves(rc::smem_u32(sQ), 128, SB);
         auto issue_s = [&](int t) {
-            const uint32_t k0 = rc::smem_u32(sKV + (t % NS) * 2 * KV_BYTES);
+            const tc::Desc kd = tc::desc_halves(rc::smem_u32(sKV + (t % NS) * 2 * KV_BYTES), 128, SB);
             for (int q = 0; q < n_qt; ++q) {
-                const uint32_t q0 = rc::smem_u32(sQ + q * TM * D * 2);
+                const uint32_t qlo = qd.lo + q * (TM * D * 2 / 16);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    tc::mma_bf16(tbase + q * 256 + (t & 1) * TN, tc::smem_desc(q0 + k * 256, 128, SB),
-                                 tc::smem_desc(k0 + k * 256, 128, SB), idS, k > 0);
+                    tc::mma_bf16_h(tbase + q * 256 + (t & 1) * TN, qlo + k * 16, qd.hi, kd.lo + k * 16, kd.hi, idS,
+                                   k > 0 ? 1u : 0u);
                 tc::commit(&s_full[q * 2 + (t & 1)]);
             }
         };
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                 if (!ok) break;
                 issue_s(t + 1);
             }
-            const uint32_t v0 = rc::smem_u32(sKV + s * 2 * KV_BYTES + KV_BYTES);
+            const tc::Desc vd = tc::desc_halves(rc::smem_u32(sKV + s * 2 * KV_BYTES + KV_BYTES), SB, 128);
             for (int q = 0; q < n_qt && ok; ++q) {
                 ok = tc::mbar_wait(&p_full[q * 2 + (t & 1)], (t >> 1) & 1, kWaitIter);
                 tc::fence_after();
@@ -557,8 +560,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
                 const uint32_t pt = tbase + q * 256 + (t & 1) * TN;  // P(t) in TMEM, 8 columns per 16 keys
 #pragma unroll
                 for (int j = 0; j < TN / 16; ++j)
-                    tc::mma_bf16_ts(tbase + q * 256 + 128, pt + j * 8, tc::smem_desc(v0 + j * 2 * SB, SB, 128), idPV,
-                                    t > 0 || j > 0);
+                    tc::mma_bf16_ts_h(tbase + q * 256 + 128, pt + j * 8, vd.lo + j * (2 * SB / 16), vd.hi, idPV,
+                                      (t > 0 || j > 0) ? 1u : 0u);
                 tc::commit(&o_done[q]);
             }
             tc::commit(&kv_empty[s]);  // stage s is free once everything issued so far is done

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -33,11 +34,37 @@ RC_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// The same with constant byte offsets added to both addresses inside the
+// instruction ([reg+imm] addressing): a fully unrolled run of copies then
+// costs one instruction each.
+template <int DST_OFF, int SRC_OFF>
+RC_DEV void cp_async16_at(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0+%3], [%1+%4], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes),
+                 "n"(DST_OFF), "n"(SRC_OFF)
+                 : "memory");
+}
+// N copies i = 0..N-1 at dst + i * DST_STEP and src + i * SRC_STEP bytes.
+template <int DST_STEP, int SRC_STEP, int... I>
+RC_DEV void cp_async16_run(uint32_t dst, const void* src, uint32_t src_bytes, std::integer_sequence<int, I...>) {
+    (cp_async16_at<I * DST_STEP, I * SRC_STEP>(dst, src, src_bytes), ...);
+}
 // The same with an L2 eviction-priority policy (from l2_policy_*).
 RC_DEV void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
     asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst), "l"(src),
                  "r"(src_bytes), "l"(policy)
                  : "memory");
+}
+// cp_async16_at / cp_async16_run with an L2 eviction-priority policy.
+template <int DST_OFF, int SRC_OFF>
+RC_DEV void cp_async16_at(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0+%4], [%1+%5], 16, %2, %3;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes), "l"(policy), "n"(DST_OFF), "n"(SRC_OFF)
+                 : "memory");
+}
+template <int DST_STEP, int SRC_STEP, int... I>
+RC_DEV void cp_async16_run(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy,
+                           std::integer_sequence<int, I...>) {
+    (cp_async16_at<I * DST_STEP, I * SRC_STEP>(dst, src, src_bytes, policy), ...);
 }
 // L2 policies: lines a kernel reads once (a request's private keys, which
 // stream through) go first; lines many CTAs and the next step read again

@@ -71,6 +71,41 @@ RC_DEV void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint3
         : "memory");
 }
 
+// A descriptor held as two 32-bit halves.  The low half carries the start
+// address (bits 0..13, in 16-byte units) and the leading byte offset, so
+// stepping an operand along K is one 32-bit add of (bytes >> 4) to `lo`
+// (shared addresses stay below 2^18 bytes: the field never carries).  The
+// issue forms below take the halves and build the 64-bit operands inside the
+// asm, which keeps the MMA thread's instructions per product to a handful.
+struct Desc {
+    uint32_t lo, hi;
+};
+RC_DEV Desc desc_halves(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = smem_desc(saddr, lbo, sbo);
+    return {(uint32_t)d, (uint32_t)(d >> 32)};
+}
+RC_DEV void mma_bf16_h(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %2};\n\t"
+        "mov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+RC_DEV void mma_bf16_ts_h(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
+                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // The mbarrier gets one arrival when all tcgen05 operations this thread
 // issued before have completed.
 RC_DEV void commit(uint64_t* mbar) {
