@@ -133,6 +133,34 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class CopyLog:
+    """CUDA events around every host<->device copy of an e2e leg, recorded on
+    the copy's own stream (after its waits): how long the copies themselves
+    took during the leg, to set beside the link rates measured alone."""
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.items = []
+
+    def run(self, stream, kind, nbytes, fn):
+        a = self.torch.cuda.Event(enable_timing=True)
+        b = self.torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        self.items.append((kind, nbytes, a, b))
+
+    def summary(self, steps):
+        out = {}
+        for kind in ("h2d", "d2h"):
+            its = [x for x in self.items if x[0] == kind]
+            ms = sum(a.elapsed_time(b) for _, _, a, b in its)
+            nb = sum(n for _, n, _, _ in its)
+            out[kind] = {"copies_per_step": len(its) / steps, "busy_ms_per_step": ms / steps,
+                         "gbs": nb / (ms * 1e-3) / 1e9 if ms > 0 else None}
+        return out
+
+
 # ------------------------------------------------------------ replay model
 class ReplayModel:
     """The synthetic model with every step's Q/K/V rows generated ahead of time
@@ -145,6 +173,7 @@ class ReplayModel:
         self.ready = {}          # tuple(rids) -> dict
         self.host = None         # e2e: pinned host copies, moved to the device on use
         self.h2d_bytes = 0
+        self.copylog = None      # e2e: a CopyLog timing every copy
         self._last = None        # (batch list, entry) of the batch being served
 
     def sequence(self, prompt, max_new):
@@ -245,9 +274,16 @@ class ReplayModel:
         free = torch.cuda.Event()
         free.record(torch.cuda.current_stream())
         self.h2d.wait_event(free)
-        with torch.cuda.stream(self.h2d):
-            e["ring"][(c % 2) * K:(c % 2) * K + (b - a)].copy_(host[a:b], non_blocking=True)
-        self.h2d_bytes += (b - a) * e["dec_step_bytes"]
+        nbytes = (b - a) * e["dec_step_bytes"]
+
+        def copy():
+            with torch.cuda.stream(self.h2d):
+                e["ring"][(c % 2) * K:(c % 2) * K + (b - a)].copy_(host[a:b], non_blocking=True)
+        if self.copylog is not None:
+            self.copylog.run(self.h2d, "h2d", nbytes, copy)
+        else:
+            copy()
+        self.h2d_bytes += nbytes
         ev = torch.cuda.Event()
         ev.record(self.h2d)
         e["moved"][c] = ev
@@ -262,11 +298,18 @@ class ReplayModel:
             return
         if e["host"]["dec"].shape[0] and 0 not in e["moved"]:
             self._move_chunk(e, 0)
-        with torch.cuda.stream(self.h2d_ext):
-            for k, v in e["ext"].items():
-                if v is not None:
-                    v.copy_(e["host"]["ext"][k], non_blocking=True)
-                    self.h2d_bytes += v.numel() * v.element_size()
+        nbytes = sum(v.numel() * v.element_size() for v in e["ext"].values() if v is not None)
+
+        def copy():
+            with torch.cuda.stream(self.h2d_ext):
+                for k, v in e["ext"].items():
+                    if v is not None:
+                        v.copy_(e["host"]["ext"][k], non_blocking=True)
+        if self.copylog is not None:
+            self.copylog.run(self.h2d_ext, "h2d", nbytes, copy)
+        else:
+            copy()
+        self.h2d_bytes += nbytes
         ev = torch.cuda.Event()
         ev.record(self.h2d_ext)
         e["ext_moved"] = ev
@@ -676,6 +719,13 @@ class OutputsHome:
         self.host_dec = torch.empty(K, batch, shape.q_heads, shape.head_dim_v, dtype=torch.bfloat16).pin_memory()
         self.done = [None, None]
         self.bytes = 0
+        self.copylog = None      # a CopyLog timing every copy
+
+    def _copy(self, nbytes, fn):
+        if self.copylog is not None:
+            self.copylog.run(self.stream, "d2h", nbytes, fn)
+        else:
+            fn()
 
     def _after_compute(self):
         ev = self.torch.cuda.Event()
@@ -684,8 +734,11 @@ class OutputsHome:
 
     def on_extend(self, out):
         self._after_compute()
-        with self.torch.cuda.stream(self.stream):
-            self.host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+
+        def copy():
+            with self.torch.cuda.stream(self.stream):
+                self.host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+        self._copy(out.numel() * out.element_size(), copy)
         out.record_stream(self.stream)
         self.bytes += out.numel() * out.element_size()
 
@@ -698,8 +751,10 @@ class OutputsHome:
         a, m = (c % 2) * K, t - c * K + 1
         B = outs.shape[1]
         self._after_compute()
-        with self.torch.cuda.stream(self.stream):
-            self.host_dec[:m, :B].copy_(outs[a:a + m], non_blocking=True)
+        def copy():
+            with self.torch.cuda.stream(self.stream):
+                self.host_dec[:m, :B].copy_(outs[a:a + m], non_blocking=True)
+        self._copy(m * out.numel() * out.element_size(), copy)
         outs.record_stream(self.stream)
         self.bytes += m * out.numel() * out.element_size()
         done = self.torch.cuda.Event()
@@ -796,6 +851,8 @@ def run_config(args, name, rank, world, local):
                            max(len(b) for b in batches), sh)
         model.h2d_bytes = 0
         link0 = link_rates(torch)
+        model.copylog = home.copylog = CopyLog(torch)
+        wait0 = eng.host_wait_s
         gc.collect()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -814,6 +871,9 @@ def run_config(args, name, rank, world, local):
                "h2d_bytes_per_step": model.h2d_bytes // args.steps, "d2h_bytes_per_step": home.bytes // args.steps,
                "ms_per_step": ems / args.steps, "host_queue_ms_per_step": 1e3 * host_s / args.steps}
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
+        e2e["copies"] = model.copylog.summary(args.steps)
+        e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / args.steps
+        model.copylog = home.copylog = None
 
     cpu = None
     if rank == 0 and world == 1:
@@ -1256,10 +1316,15 @@ def main():
             ev.record(torch.cuda.current_stream())
             d2h_stream.wait_event(ev)
 
+        copylog = CopyLog(torch)
+
         def copy_extend(out):
             after_compute()
-            with torch.cuda.stream(d2h_stream):
-                host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+
+            def copy():
+                with torch.cuda.stream(d2h_stream):
+                    host_ext[:out.shape[0]].copy_(out, non_blocking=True)
+            copylog.run(d2h_stream, "d2h", out.numel() * out.element_size(), copy)
             out.record_stream(d2h_stream)
             d2h[0] += out.numel() * out.element_size()
             if st["batch"] + 1 < len(keys):
@@ -1272,8 +1337,11 @@ def main():
             outs = runner.decode_outs
             a, m = (c % 2) * K, t - c * K + 1
             after_compute()
-            with torch.cuda.stream(d2h_stream):
-                host_dec[:m].copy_(outs[a:a + m], non_blocking=True)
+
+            def copy():
+                with torch.cuda.stream(d2h_stream):
+                    host_dec[:m].copy_(outs[a:a + m], non_blocking=True)
+            copylog.run(d2h_stream, "d2h", m * out.numel() * out.element_size(), copy)
             outs.record_stream(d2h_stream)
             d2h[0] += m * out.numel() * out.element_size()
             done = torch.cuda.Event()
@@ -1291,6 +1359,8 @@ def main():
         runner.on_extend = copy_extend
         model.h2d_bytes = 0
         link0 = link_rates(torch)
+        model.copylog = copylog
+        wait0 = eng.host_wait_s
         gc.collect()
         gc.freeze()
         if world > 1:
@@ -1311,6 +1381,9 @@ def main():
                "h2d_bytes_per_step": model.h2d_bytes // n_e2e, "d2h_bytes_per_step": d2h[0] // n_e2e,
                "ms_per_step": ems / n_e2e, "host_queue_ms_per_step": 1e3 * host_s / n_e2e}
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
+        e2e["copies"] = copylog.summary(n_e2e)
+        e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / n_e2e
+        model.copylog = None
 
     cpu = None
     if rank == 0 and world == 1:

@@ -25,6 +25,7 @@ launches; PyTorch only provides device memory and the stream.
 from __future__ import annotations
 
 import ctypes as C
+import time
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -330,6 +331,7 @@ class DeviceEngine:
         self.fuse_store = not kv_fp8  # decode steps store the new token inside attn_decode_append (bf16 pools)
         self.events = {}             # call name -> [(start, end, info)]
         self.launches = 0            # kernels launched by the library (counted per call)
+        self.host_wait_s = 0.0       # host time blocked on the GPU (staging buffer reuse)
         self._ev_pool = []
 
     def start_timing(self, n_events: int = 4096):
@@ -395,7 +397,9 @@ class DeviceEngine:
         self._stage_next ^= 1
         slot = self._stage[k]
         if slot is not None:
+            t0 = time.perf_counter()
             slot[2].synchronize()
+            self.host_wait_s += time.perf_counter() - t0
         if slot is None or slot[0].numel() < n:
             cap = max(n + n // 4, 1 << 16)
             slot = [torch.empty(cap, dtype=torch.int32).pin_memory(),
