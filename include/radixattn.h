@@ -352,7 +352,14 @@ rc_status kv_store(const rc_pool_desc* pool, const int32_t* slots, const void* k
  * kv table of attn_decode holds only each row's remaining (private) keys; the
  * result equals flat decode over segments + private keys.  max_seg_len and
  * max_seg_rows are host bounds on keys and rows per segment (they size the
- * grid); total_seg_rows = seg_row_indptr[n_seg]. */
+ * grid); total_seg_rows = seg_row_indptr[n_seg].
+ * host_seg_indptr, host_seg_row_indptr: NULL, or HOST copies of seg_indptr
+ * and seg_row_indptr (n_seg + 1 entries each, equal to the device arrays,
+ * read by the call itself).  With them the cascade grid has one CTA per
+ * non-empty (segment, key chunk, row block) only; without them it spans
+ * max_seg_rows x max_seg_len for every segment and the CTAs past a short
+ * segment's rows or keys leave at once (a library convenience: the pages
+ * describe the shared layers, not a launch grid). */
 typedef struct rc_cascade {
     int32_t n_seg;
     const int32_t* seg_slots;
@@ -364,6 +371,8 @@ typedef struct rc_cascade {
     int32_t max_seg_len;
     int32_t max_seg_rows;
     int32_t total_seg_rows;
+    const int32_t* host_seg_indptr;
+    const int32_t* host_seg_row_indptr;
 } rc_cascade;
 
 /* Workspace bytes attn_decode needs for this batch (split partials). */

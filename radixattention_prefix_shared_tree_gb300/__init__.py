@@ -49,7 +49,7 @@ class rc_kv_table(C.Structure):
 class rc_cascade(C.Structure):
     _fields_ = [("n_seg", I32), ("seg_slots", VP), ("seg_indptr", VP), ("seg_row_indptr", VP),
                 ("seg_rows", VP), ("req_seg_indptr", VP), ("req_seg_pos", VP), ("max_seg_len", I32), ("max_seg_rows", I32),
-                ("total_seg_rows", I32)]
+                ("total_seg_rows", I32), ("host_seg_indptr", VP), ("host_seg_row_indptr", VP)]
 
 
 class rc_decode_step(C.Structure):
@@ -465,8 +465,16 @@ def make_kv_table(slots, start, length, max_len: int, table_len: int | None = No
 
 
 def make_cascade(seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos,
-                 max_seg_rows: int, max_seg_len: int) -> rc_cascade:
+                 max_seg_rows: int, max_seg_len: int, host_seg_indptr=None, host_seg_row_indptr=None) -> rc_cascade:
+    """Device arrays as tensors; host_seg_indptr / host_seg_row_indptr: None,
+    or numpy copies of seg_indptr / seg_row_indptr (the grid then covers the
+    non-empty segment chunks only)."""
     c = rc_cascade()
+    host = ()
+    if host_seg_indptr is not None and host_seg_row_indptr is not None:
+        host = (np.ascontiguousarray(host_seg_indptr, np.int32), np.ascontiguousarray(host_seg_row_indptr, np.int32))
+        c.host_seg_indptr = host[0].ctypes.data
+        c.host_seg_row_indptr = host[1].ctypes.data
     c.n_seg = seg_indptr.numel() - 1
     c.seg_slots = seg_slots.data_ptr() if seg_slots.numel() else None
     c.seg_indptr, c.seg_row_indptr = seg_indptr.data_ptr(), seg_row_indptr.data_ptr()
@@ -476,7 +484,7 @@ def make_cascade(seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr
     c.max_seg_rows = int(max_seg_rows)
     c.max_seg_len = int(max_seg_len)
     c.total_seg_rows = int(seg_rows.numel())
-    c._keep = (seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos)
+    c._keep = (seg_slots, seg_indptr, seg_row_indptr, seg_rows, req_seg_indptr, req_seg_pos) + host
     return c
 
 

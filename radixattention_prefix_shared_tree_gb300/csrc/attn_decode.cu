@@ -677,15 +677,36 @@ cudaError_t launch_split(const DecParams& p, int batch, int kv_heads, cudaStream
 }
 
 template <int D, int G, bool FP8>
-cudaError_t launch_cascade(const rc::MQParams& p, const rc_cascade* c, int kv_heads, cudaStream_t st) {
+cudaError_t launch_cascade(const rc::MQParams& p0, const rc_cascade* c, int kv_heads, cudaStream_t st) {
     constexpr int smem = rc_tc2::smem_bytes<D, FP8>();
     cudaError_t e = rc_host::ensure_smem<rc_tc2::attn_tc2_kernel<D, G, rc::MQMode::kCascade, FP8>>(smem);
     if (e != cudaSuccess) return e;
     constexpr int TPC = rc_tc2::ROWS / G;
+    rc::MQParams p = p0;
+    dim3 grid((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
+    p.n_seg = c->n_seg;
+    p.seg_items = 0;
+    if (c->host_seg_indptr && c->host_seg_row_indptr) {
+        // one CTA per non-empty (segment, key chunk, row block), counted the
+        // way the kernel counts them from the device arrays
+        int64_t items = 0;
+        for (int s = 0; s < c->n_seg; ++s) {
+            const int64_t rows = (int64_t)c->host_seg_row_indptr[s + 1] - c->host_seg_row_indptr[s];
+            const int64_t len = (int64_t)c->host_seg_indptr[s + 1] - c->host_seg_indptr[s];
+            if (rows <= 0) continue;
+            int64_t ch = len > 0 ? (len + p.seg_chunk - 1) / p.seg_chunk : 1;
+            if (ch > p.seg_chunks) ch = p.seg_chunks;
+            items += ch * ((rows + TPC - 1) / TPC);
+        }
+        if (items > 0 && items <= 0x7fffffff) {
+            grid = dim3((unsigned)items, kv_heads, 1);
+            p.seg_items = (int32_t)items;
+        }
+    }
     // programmatic dependent of the previous kernel on the stream (the kernel
     // waits for it before reading anything)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((c->max_seg_rows + TPC - 1) / TPC, kv_heads, c->n_seg * p.seg_chunks);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(rc_tc2::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;

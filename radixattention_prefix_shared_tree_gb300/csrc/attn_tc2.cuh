@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kBars);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kvh = blockIdx.y, z = blockIdx.z, blk = blockIdx.x;
+    const int kvh = blockIdx.y, z = blockIdx.z;
+    int blk = blockIdx.x;
     // cascade: launched as the programmatic dependent of whatever precedes it
     // on the stream (the previous step's table pass), so its CTAs take SMs as
     // that grid drains; nothing is read before that grid has finished.  The
@@ -110,6 +111,70 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     if constexpr (MODE == rc::MQMode::kCascade) {
         asm volatile("griddepcontrol.wait;\n" ::: "memory");
         asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
+    // cascade: this CTA's segment, key chunk and the segment's chunk count.
+    // With a compact grid (seg_items > 0) blockIdx.x is the item: one warp
+    // walks the segments 32 at a time, each lane counting its segment's
+    // (key chunk, row block) items, and a warp scan finds the segment that
+    // holds this item (chunk-major inside a segment).
+    int c_seg = 0, c_chunk = 0, c_nch = 1;
+    if constexpr (MODE == rc::MQMode::kCascade) {
+        if (p.seg_items > 0) {
+            __shared__ int s_map[4];
+            if (threadIdx.x < 32) {
+                const int ln = threadIdx.x;
+                const int target = blockIdx.x;
+                int base = 0, found = -1, f_chunk = 0, f_blk = 0, f_nch = 1;
+                for (int s0 = 0; s0 < p.n_seg && found < 0; s0 += 32) {
+                    const int sg = s0 + ln;
+                    int items = 0, rb = 1, ch = 1;
+                    if (sg < p.n_seg) {
+                        const int rows = p.seg_row_indptr[sg + 1] - p.seg_row_indptr[sg];
+                        const int len = p.seg_indptr[sg + 1] - p.seg_indptr[sg];
+                        rb = rows > 0 ? (rows + TPC - 1) / TPC : 1;
+                        ch = len > 0 ? min((len + p.seg_chunk - 1) / p.seg_chunk, p.seg_chunks) : 1;
+                        items = rows > 0 ? ch * rb : 0;
+                    }
+                    int incl = items;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (ln >= o) incl += v;
+                    }
+                    const int excl = base + incl - items;
+                    const unsigned m = __ballot_sync(0xffffffffu, items > 0 && target >= excl && target < excl + items);
+                    if (m) {
+                        const int src = __ffs(m) - 1;
+                        const int j = target - __shfl_sync(0xffffffffu, excl, src);
+                        const int rb_s = __shfl_sync(0xffffffffu, rb, src);
+                        f_nch = __shfl_sync(0xffffffffu, ch, src);
+                        found = s0 + src;
+                        f_chunk = j / rb_s;
+                        f_blk = j % rb_s;
+                    }
+                    base += __shfl_sync(0xffffffffu, incl, 31);
+                }
+                if (ln == 0) {
+                    s_map[0] = found;
+                    s_map[1] = f_chunk;
+                    s_map[2] = f_blk;
+                    s_map[3] = f_nch;
+                }
+            }
+            __syncthreads();
+            if (s_map[0] < 0) {  // more items than the segments hold: the host arrays differ
+                if (threadIdx.x == 0) rc::flag_error(p.err, rc::kErrBadSlot);
+                return;
+            }
+            c_seg = s_map[0];
+            c_chunk = s_map[1];
+            blk = s_map[2];
+            c_nch = s_map[3];
+        } else {
+            c_seg = z / p.seg_chunks;
+            c_chunk = z % p.seg_chunks;
+            c_nch = p.seg_chunks;
+        }
     }
     const int tok0 = blk * TPC;
 
@@ -130,14 +195,22 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         keys = p.table + row0;
         key_count = prefix + min(n_rows_tok, tok0 + TPC);
     } else {
-        const int seg = z / p.seg_chunks;
-        chunk = z % p.seg_chunks;
+        const int seg = c_seg;
+        chunk = c_chunk;
         qo0 = p.seg_row_indptr[seg];
         n_rows_tok = p.seg_row_indptr[seg + 1] - qo0;
         const int k0 = chunk * p.seg_chunk;
         keys = p.seg_slots + p.seg_indptr[seg] + k0;
         key_count = min(p.seg_indptr[seg + 1] - p.seg_indptr[seg] - k0, p.seg_chunk);
         if (tok0 >= n_rows_tok) return;
+        // compact grid: no CTA runs past the segment's last chunk, so its
+        // first chunk's CTA marks those partials empty for its rows
+        if (p.seg_items > 0 && chunk == 0 && c_nch < p.seg_chunks && tid < ROWS) {
+            const int tk = tok0 + tid / G;
+            if (tk < n_rows_tok)
+                for (int c = c_nch; c < p.seg_chunks; ++c)
+                    p.part_lse[((int64_t)(qo0 + tk) * p.q_heads + kvh * G + (tid % G)) * p.seg_chunks + c] = -INFINITY;
+        }
         if (key_count <= 0) {  // segment shorter than this chunk: an empty partial
             if (tid < ROWS) {
                 const int tk = tok0 + tid / G;

@@ -35,6 +35,10 @@ struct MQParams {
     float* part_lse;  // [total_seg_rows][q_heads][seg_chunks], log2 units (-inf: empty chunk)
     int32_t seg_chunk;   // keys per cascade CTA
     int32_t seg_chunks;  // chunks per segment (grid z = segment * seg_chunks + chunk)
+    int32_t n_seg;
+    // > 0: the grid's x is this many non-empty (segment, key chunk, row block)
+    // items, in segment order (within a segment: chunk-major), and z is 1
+    int32_t seg_items;
     // FP8 pool: pool_k / pool_v hold E4M3 codes and these the per-row scales
     const float* k_scale;  // [n_slots][kv_heads]
     const float* v_scale;

@@ -650,7 +650,8 @@ class BatchLayout:
         if plan is not None:
             self._casc_arrays = dv[len(names):]
             self.casc = make_cascade(*self._casc_arrays, max_seg_rows=plan["max_seg_rows"],
-                                     max_seg_len=plan["max_seg_len"])
+                                     max_seg_len=plan["max_seg_len"], host_seg_indptr=plan["seg_indptr"],
+                                     host_seg_row_indptr=plan["seg_row_indptr"])
         self.extend_table = make_kv_table(self.table, self.start_dev, self.len_prompt, int(L.max()) if B else 0)
 
     def decode_table(self, t: int):

@@ -231,7 +231,19 @@ def test_cascade_equals_flat_and_oracle(cuda, Hq, Hkv, D):
     cout = torch.empty_like(flat)
     clse = torch.empty_like(flat_lse)
     ra.attn_decode(desc, q, kv2, B, cout, clse, ws2, cascade=casc)
+    # the same cascade with host copies of the segment offsets: a grid of the
+    # non-empty (segment, key chunk, row block) items only, the partials of
+    # the chunks past a short segment marked empty by its first chunk's CTA;
+    # every CTA does the same work as before, so the results are bit-identical
+    casc_c = ra.make_cascade(*arrs, max_seg_rows=max(len(r) for _, r in segs),
+                             max_seg_len=max(len(x) for x, _ in segs), host_seg_indptr=seg_indptr,
+                             host_seg_row_indptr=seg_row_indptr)
+    cout_c = torch.empty_like(flat)
+    clse_c = torch.empty_like(flat_lse)
+    ra.attn_decode(desc, q, kv2, B, cout_c, clse_c, ws2, cascade=casc_c)
     assert ra.rc_sync(pool.err) == ra.RC_OK
+    assert (bits(cout_c) == bits(cout)).all()
+    assert (clse_c.cpu().numpy().view(np.uint32) == clse.cpu().numpy().view(np.uint32)).all()
     refs = _oracle_rows(pool, rows, bits(q), lens, Hq, Hkv, D, scale)
     check(bits(flat), refs, flat_lse.cpu().numpy(), label="flat")
     check(bits(cout), refs, clse.cpu().numpy(), label="cascade")
