@@ -851,6 +851,7 @@ def run_config(args, name, rank, world, local):
                            max(len(b) for b in batches), sh)
         model.h2d_bytes = 0
         link0 = link_rates(torch)
+        src_gbs = source_rate(torch, model, keys)
         model.copylog = home.copylog = CopyLog(torch)
         wait0 = eng.host_wait_s
         gc.collect()
@@ -872,6 +873,7 @@ def run_config(args, name, rank, world, local):
                "ms_per_step": ems / args.steps, "host_queue_ms_per_step": 1e3 * host_s / args.steps}
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
         e2e["copies"] = model.copylog.summary(args.steps)
+        e2e["link"]["input_buffers_gbs"] = src_gbs
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / args.steps
         model.copylog = home.copylog = None
 
@@ -926,6 +928,29 @@ def link_rates(torch, nbytes: int = 256 << 20, reps: int = 3) -> dict:
 
     run((0, 1))
     return {"h2d": run((0,)), "d2h": run((1,)), "both_each_way": run((0, 1))}
+
+
+def source_rate(torch, model, keys, nbytes: int = 32 << 20):
+    """H2D rate (GB/s, CUDA events) reading the e2e leg's own pinned input
+    buffers: the first nbytes of every batch's decode inputs, copied once.
+    Set beside link_rates (fresh buffers) it tells a slow buffer from a slow
+    link."""
+    srcs = []
+    for k in keys:
+        h = model.ready[k]["host"]["dec"]
+        if h.numel():
+            srcs.append(h.reshape(-1)[:nbytes])
+    if not srcs:
+        return None
+    d = torch.empty(max(x.numel() for x in srcs), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for x in srcs:
+        d[:x.numel()].copy_(x, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return sum(x.numel() for x in srcs) / (a.elapsed_time(b) * 1e-3) / 1e9
 
 
 def link_summary(before: dict, after: dict, h2d_bytes: int, d2h_bytes: int) -> dict:
@@ -1359,6 +1384,7 @@ def main():
         runner.on_extend = copy_extend
         model.h2d_bytes = 0
         link0 = link_rates(torch)
+        src_gbs = source_rate(torch, model, keys)
         model.copylog = copylog
         wait0 = eng.host_wait_s
         gc.collect()
@@ -1382,6 +1408,7 @@ def main():
                "ms_per_step": ems / n_e2e, "host_queue_ms_per_step": 1e3 * host_s / n_e2e}
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
         e2e["copies"] = copylog.summary(n_e2e)
+        e2e["link"]["input_buffers_gbs"] = src_gbs
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / n_e2e
         model.copylog = None
 
