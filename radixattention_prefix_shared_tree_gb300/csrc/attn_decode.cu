@@ -770,9 +770,11 @@ extern "C" rc_status attn_decode_workspace(const rc_attn_desc* desc, int32_t bat
 
 namespace {
 
+// early: the kernel queued just before is the previous step's table pass
+// (see MQParams::early)
 rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new, const void* v_new,
                       const rc_kv_table* kv, int32_t batch, const rc_cascade* casc, void* out, float* lse, void* ws,
-                      size_t ws_bytes, rc_stream_t stream) {
+                      size_t ws_bytes, rc_stream_t stream, bool early = false) {
     if (!desc || !kv || batch < 0) return RC_ERR_ARG;
     if (batch == 0) return RC_OK;
     if (!q || !out || !kv->slots || !kv->start || !kv->len || !desc->pool.k) return RC_ERR_ARG;
@@ -852,6 +854,7 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
         mp.part_lse = seg_lse;
         mp.seg_chunk = pl.seg_chunk;
         mp.seg_chunks = pl.seg_chunks;
+        mp.early = early ? 1 : 0;
     }
     cudaStream_t st = (cudaStream_t)stream;
     bool ok = false;
@@ -911,8 +914,17 @@ extern "C" rc_status attn_decode_steps(const rc_attn_desc* desc, const rc_kv_tab
             r = kv_store(&desc->pool, s.store_slots, s.k_new, s.v_new, batch, nullptr, nullptr, stream);
             if (r == RC_OK) r = attn_decode(desc, s.q, &t, batch, casc, s.out, s.lse, ws, ws_bytes, stream);
         } else if (s.k_new) {
-            r = attn_decode_append(desc, s.q, s.k_new, s.v_new, &t, batch, casc, s.out, s.lse, ws, ws_bytes,
-                                   stream);
+            if ((reinterpret_cast<uintptr_t>(s.k_new) | reinterpret_cast<uintptr_t>(s.v_new)) & 15 || !s.v_new) {
+                r = RC_ERR_ARG;
+            } else {
+                // after an append step with no event in between, the kernel queued
+                // last is that step's table pass (or its merge): this step's
+                // cascade may read before waiting for it
+                const rc_decode_step* pv = i > 0 ? &steps[i - 1] : nullptr;
+                const bool early = pv && pv->k_new && !pv->store_slots && !pv->ev_end && !s.ev_begin;
+                r = decode_impl(desc, s.q, s.k_new, s.v_new, &t, batch, casc, s.out, s.lse, ws, ws_bytes, stream,
+                                early);
+            }
         } else {
             r = attn_decode(desc, s.q, &t, batch, casc, s.out, s.lse, ws, ws_bytes, stream);
         }

@@ -108,9 +108,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
     // table pass of this call is in turn this grid's dependent: it may start
     // once every CTA here has begun (it waits for this grid's end before
     // reading the partials).
+    // (early: the wait and the trigger move to just before the first global
+    // write, see MQParams::early; the table pass then still launches only
+    // after the preceding grid has finished)
     if constexpr (MODE == rc::MQMode::kCascade) {
-        asm volatile("griddepcontrol.wait;\n" ::: "memory");
-        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+        if (!p.early) {
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+        }
     }
     // cascade: this CTA's segment, key chunk and the segment's chunk count.
     // With a compact grid (seg_items > 0) blockIdx.x is the item: one warp
@@ -205,13 +210,24 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
         if (tok0 >= n_rows_tok) return;
         // compact grid: no CTA runs past the segment's last chunk, so its
         // first chunk's CTA marks those partials empty for its rows
-        if (p.seg_items > 0 && chunk == 0 && c_nch < p.seg_chunks && tid < ROWS) {
+        if (p.seg_items > 0 && !p.early && chunk == 0 && c_nch < p.seg_chunks && tid < ROWS) {
             const int tk = tok0 + tid / G;
             if (tk < n_rows_tok)
                 for (int c = c_nch; c < p.seg_chunks; ++c)
                     p.part_lse[((int64_t)(qo0 + tk) * p.q_heads + kvh * G + (tid % G)) * p.seg_chunks + c] = -INFINITY;
         }
         if (key_count <= 0) {  // segment shorter than this chunk: an empty partial
+            if (p.early) {
+                asm volatile("griddepcontrol.wait;\n" ::: "memory");
+                asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+                if (p.seg_items > 0 && chunk == 0 && tid < ROWS) {
+                    const int tk = tok0 + tid / G;
+                    if (tk < n_rows_tok)
+                        for (int c = c_nch; c < p.seg_chunks; ++c)
+                            p.part_lse[((int64_t)(qo0 + tk) * p.q_heads + kvh * G + (tid % G)) * p.seg_chunks + c] =
+                                -INFINITY;
+                }
+            }
             if (tid < ROWS) {
                 const int tk = tok0 + tid / G;
                 if (tk < n_rows_tok)
@@ -425,6 +441,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             tc::fence_after();
         }
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
+        if constexpr (MODE == rc::MQMode::kCascade) {
+            if (p.early) {  // the partials below are what the preceding grid read
+                asm volatile("griddepcontrol.wait;\n" ::: "memory");
+                asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+                if (p.seg_items > 0 && chunk == 0 && c_nch < p.seg_chunks) {
+                    const int tk = tok0 + tid / G;  // tid < ROWS here
+                    if (tk < n_rows_tok)
+                        for (int c = c_nch; c < p.seg_chunks; ++c)
+                            p.part_lse[((int64_t)(qo0 + tk) * p.q_heads + kvh * G + (tid % G)) * p.seg_chunks + c] =
+                                -INFINITY;
+                }
+            }
+        }
         // ---- epilogue: normalised O rows and their log-sum-exp.  Rows go out
         // through shared memory so that each store instruction writes whole
         // row segments: per 32 columns, the warp's 32x32 fp32 block is staged
@@ -640,6 +669,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(const rc::MQParams
             tc::commit(&kv_empty[s]);  // stage s is free once everything issued so far is done
         }
         if (!ok) rc::flag_error(p.err, rc::kErrTimeout);
+    }
+    if constexpr (MODE == rc::MQMode::kCascade) {
+        if (p.early) {  // every thread of the CTA has waited and triggered before it leaves
+            asm volatile("griddepcontrol.wait;\n" ::: "memory");
+            asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+        }
     }
     tc::fence_before();
     __syncthreads();

@@ -39,6 +39,11 @@ struct MQParams {
     // > 0: the grid's x is this many non-empty (segment, key chunk, row block)
     // items, in segment order (within a segment: chunk-major), and z is 1
     int32_t seg_items;
+    // cascade, nonzero: the preceding grid on the stream is the previous
+    // decode step's table pass, which writes only rows' private keys and reads
+    // the partials: the kernel reads Q and the segments before waiting for
+    // it, and waits only before its first global write
+    int32_t early;
     // FP8 pool: pool_k / pool_v hold E4M3 codes and these the per-row scales
     const float* k_scale;  // [n_slots][kv_heads]
     const float* v_scale;

@@ -518,8 +518,11 @@ class DeviceEngine:
     def decode_steps(self, lay, t0: int, ins, outs, lses=None):
         """Decode steps t0 .. t0+n-1 of the batch in one library call
         (attn_decode_steps): the launches decode_step makes for each step,
-        in the same order, queued by one C call.  ins[i]: step t0+i's q/k/v;
-        outs[i], lses[i]: where it writes."""
+        in the same order, queued by one C call (inside a run, a step's
+        cascade reads before the previous step's table pass has finished).
+        ins[i]: step t0+i's q/k/v; outs[i], lses[i]: where it writes.  With
+        timing on, one pair of CUDA events spans the whole run (events between
+        steps would hold each cascade back until the previous step ends)."""
         n = len(ins)
         arr = lay.step_arr
         if arr is None or len(arr) < n:
@@ -538,12 +541,11 @@ class DeviceEngine:
             a.k_new = k.data_ptr()
             a.v_new = v.data_ptr() if v is not None else None
             a.store_slots = None if fused and v is not None else lay.slot_ptrs[t]
-            if self.timing and t % self.timing_every == 0:
-                e0, e1 = self._event(), self._event()
-                a.ev_begin, a.ev_end = e0.cuda_event, e1.cuda_event
-                timed.append((e0, e1, ("decode", lay, t)))
-            else:
-                a.ev_begin = a.ev_end = None
+            a.ev_begin = a.ev_end = None
+        if self.timing:
+            e0, e1 = self._event(), self._event()
+            arr[0].ev_begin, arr[n - 1].ev_end = e0.cuda_event, e1.cuda_event
+            timed.append((e0, e1, ("decode", lay, t0, n)))
         st = self._lib.attn_decode_steps(lay.desc_ref, lay.kv_ref, lay.batch_size, lay.casc_ref, arr, n,
                                          lay.ws_ptr, lay.ws_bytes, lay.stream, None)
         if st != RC_OK:
