@@ -24,7 +24,9 @@ times the CPU oracle instead, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import gc
+import mmap
 import json
 import os
 import statistics
@@ -133,6 +135,68 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class HugePinned:
+    """Pinned host buffers backed by transparent huge pages: an anonymous
+    mapping aligned to the huge-page size, advised MADV_HUGEPAGE, touched and
+    registered with cudaHostRegister.  On some GB300 hosts the GPU reads
+    ordinary pinned buffers (cudaHostAlloc, or registered base pages) at
+    200 GB/s only while the host has touched them recently: after about a
+    second idle the same buffers read at 3-25 GB/s, while huge-page-backed
+    ones keep 208 GB/s (measured on one such host).  The e2e leg's inputs wait
+    for seconds between being written and being read, so they live here.
+    Falls back to torch's pinned allocator if registration fails."""
+
+    HUGE = 512 << 20
+    ARENA = 4 << 30      # buffers are cut from arenas of this size (or larger)
+
+    def __init__(self, torch):
+        self.torch = torch
+        self.keep = []
+        self.fallbacks = 0
+        self.arena = None     # (uint8 tensor, used bytes)
+        try:
+            self.libc = ctypes.CDLL(None)
+        except OSError:
+            self.libc = None
+
+    def _new_arena(self, size):
+        torch = self.torch
+        size = -(-size // self.HUGE) * self.HUGE
+        mm = mmap.mmap(-1, size + self.HUGE, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        base = ctypes.addressof(ctypes.c_char.from_buffer(mm))
+        start = -(-base // self.HUGE) * self.HUGE
+        if self.libc is not None:
+            self.libc.madvise(ctypes.c_void_p(start), ctypes.c_size_t(size), 14)   # MADV_HUGEPAGE
+        u8 = torch.frombuffer(mm, dtype=torch.uint8)[start - base:start - base + size]
+        u8.fill_(0)                                       # fault the (huge) pages in
+        if int(torch.cuda.cudart().cudaHostRegister(start, size, 0)) != 0:
+            raise RuntimeError("cudaHostRegister failed")
+        self.keep.append((mm, start))
+        return u8
+
+    def empty(self, shape, dtype):
+        torch = self.torch
+        nbytes = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        need = -(-max(nbytes, 1) // 4096) * 4096
+        try:
+            if self.arena is None or self.arena[1] + need > self.arena[0].numel():
+                self.arena = [self._new_arena(max(self.ARENA, need)), 0]
+            buf, used = self.arena
+            self.arena[1] = used + need
+            return buf[used:used + nbytes].view(dtype).view(tuple(shape))
+        except Exception:
+            self.fallbacks += 1
+            return torch.empty(tuple(shape), dtype=dtype).pin_memory()
+
+    def like(self, t):
+        """A copy of tensor t (any device) in such a buffer."""
+        if t is None:
+            return None
+        h = self.empty(t.shape, t.dtype)
+        h.copy_(t)
+        return h
+
+
 class CopyLog:
     """CUDA events around every host<->device copy of an e2e leg, recorded on
     the copy's own stream (after its waits): how long the copies themselves
@@ -174,6 +238,7 @@ class ReplayModel:
         self.host = None         # e2e: pinned host copies, moved to the device on use
         self.h2d_bytes = 0
         self.copylog = None      # e2e: a CopyLog timing every copy
+        self.hostmem = None      # e2e: the HugePinned allocator of the host copies
         self._last = None        # (batch list, entry) of the batch being served
 
     def sequence(self, prompt, max_new):
@@ -217,7 +282,9 @@ class ReplayModel:
         gets them chunk by chunk on a copy stream, one chunk ahead of use."""
         torch = self.torch
         e = self.ready[key]
-        pin = lambda t: t.cpu().pin_memory() if t is not None else None
+        if self.hostmem is None:
+            self.hostmem = HugePinned(torch)
+        pin = self.hostmem.like
         e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()}}
         e["ext"] = {k: (torch_empty_like(torch, v)) for k, v in e["ext"].items()}
         K = self.CHUNK
@@ -230,7 +297,7 @@ class ReplayModel:
             n = v[0].numel() * v.element_size()
             parts[k] = (off, n)
             off += (n + 255) // 256 * 256
-        host = torch.empty(T, off, dtype=torch.uint8).pin_memory()
+        host = self.hostmem.empty((T, off), torch.uint8)
         for k, v in dec.items():
             o, n = parts[k]
             host[:, o:o + n].copy_(v.reshape(T, -1).view(torch.uint8).cpu())
