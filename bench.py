@@ -24,9 +24,7 @@ times the CPU oracle instead, on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
-import ctypes
 import gc
-import mmap
 import json
 import os
 import statistics
@@ -135,68 +133,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-class HugePinned:
-    """Pinned host buffers backed by transparent huge pages: an anonymous
-    mapping aligned to the huge-page size, advised MADV_HUGEPAGE, touched and
-    registered with cudaHostRegister.  On some GB300 hosts the GPU reads
-    ordinary pinned buffers (cudaHostAlloc, or registered base pages) at
-    200 GB/s only while the host has touched them recently: after about a
-    second idle the same buffers read at 3-25 GB/s, while huge-page-backed
-    ones keep 208 GB/s (measured on one such host).  The e2e leg's inputs wait
-    for seconds between being written and being read, so they live here.
-    Falls back to torch's pinned allocator if registration fails."""
-
-    HUGE = 512 << 20
-    ARENA = 4 << 30      # buffers are cut from arenas of this size (or larger)
-
-    def __init__(self, torch):
-        self.torch = torch
-        self.keep = []
-        self.fallbacks = 0
-        self.arena = None     # (uint8 tensor, used bytes)
-        try:
-            self.libc = ctypes.CDLL(None)
-        except OSError:
-            self.libc = None
-
-    def _new_arena(self, size):
-        torch = self.torch
-        size = -(-size // self.HUGE) * self.HUGE
-        mm = mmap.mmap(-1, size + self.HUGE, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-        base = ctypes.addressof(ctypes.c_char.from_buffer(mm))
-        start = -(-base // self.HUGE) * self.HUGE
-        if self.libc is not None:
-            self.libc.madvise(ctypes.c_void_p(start), ctypes.c_size_t(size), 14)   # MADV_HUGEPAGE
-        u8 = torch.frombuffer(mm, dtype=torch.uint8)[start - base:start - base + size]
-        u8.fill_(0)                                       # fault the (huge) pages in
-        if int(torch.cuda.cudart().cudaHostRegister(start, size, 0)) != 0:
-            raise RuntimeError("cudaHostRegister failed")
-        self.keep.append((mm, start))
-        return u8
-
-    def empty(self, shape, dtype):
-        torch = self.torch
-        nbytes = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
-        need = -(-max(nbytes, 1) // 4096) * 4096
-        try:
-            if self.arena is None or self.arena[1] + need > self.arena[0].numel():
-                self.arena = [self._new_arena(max(self.ARENA, need)), 0]
-            buf, used = self.arena
-            self.arena[1] = used + need
-            return buf[used:used + nbytes].view(dtype).view(tuple(shape))
-        except Exception:
-            self.fallbacks += 1
-            return torch.empty(tuple(shape), dtype=dtype).pin_memory()
-
-    def like(self, t):
-        """A copy of tensor t (any device) in such a buffer."""
-        if t is None:
-            return None
-        h = self.empty(t.shape, t.dtype)
-        h.copy_(t)
-        return h
-
-
 class CopyLog:
     """CUDA events around every host<->device copy of an e2e leg, recorded on
     the copy's own stream (after its waits): how long the copies themselves
@@ -238,7 +174,6 @@ class ReplayModel:
         self.host = None         # e2e: pinned host copies, moved to the device on use
         self.h2d_bytes = 0
         self.copylog = None      # e2e: a CopyLog timing every copy
-        self.hostmem = None      # e2e: the HugePinned allocator of the host copies
         self._last = None        # (batch list, entry) of the batch being served
 
     def sequence(self, prompt, max_new):
@@ -282,9 +217,7 @@ class ReplayModel:
         gets them chunk by chunk on a copy stream, one chunk ahead of use."""
         torch = self.torch
         e = self.ready[key]
-        if self.hostmem is None:
-            self.hostmem = HugePinned(torch)
-        pin = self.hostmem.like
+        pin = lambda t: t.cpu().pin_memory() if t is not None else None
         e["host"] = {"ext": {k: pin(v) for k, v in e["ext"].items()}}
         e["ext"] = {k: (torch_empty_like(torch, v)) for k, v in e["ext"].items()}
         K = self.CHUNK
@@ -297,10 +230,15 @@ class ReplayModel:
             n = v[0].numel() * v.element_size()
             parts[k] = (off, n)
             off += (n + 255) // 256 * 256
-        host = self.hostmem.empty((T, off), torch.uint8)
+        # packed on the device, then one device -> host copy (the host buffer
+        # is written by DMA, not by the CPU)
+        packed = torch.zeros(T, off, dtype=torch.uint8, device=self.base.device)
         for k, v in dec.items():
             o, n = parts[k]
-            host[:, o:o + n].copy_(v.reshape(T, -1).view(torch.uint8).cpu())
+            packed[:, o:o + n].copy_(v.reshape(T, -1).view(torch.uint8))
+        host = torch.empty(T, off, dtype=torch.uint8).pin_memory()
+        host.copy_(packed)
+        del packed
         e["host"]["dec"] = host
         e["dec_step_bytes"] = off
         ring = torch.empty(2 * K, off, dtype=torch.uint8, device=self.base.device)
@@ -946,6 +884,7 @@ def run_config(args, name, rank, world, local):
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
         e2e["copies"] = model.copylog.summary(args.steps)
         e2e["link"]["input_buffers_gbs"] = src_gbs
+        e2e["link"]["anon_huge_kb"] = anon_huge_kb()
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / args.steps
         model.copylog = home.copylog = None
 
@@ -1000,6 +939,17 @@ def link_rates(torch, nbytes: int = 256 << 20, reps: int = 3) -> dict:
 
     run((0, 1))
     return {"h2d": run((0,)), "d2h": run((1,)), "both_each_way": run((0, 1))}
+
+
+def anon_huge_kb():
+    """The process's anonymous memory in transparent huge pages (kB), or None."""
+    try:
+        for ln in open("/proc/self/smaps_rollup"):
+            if ln.startswith("AnonHugePages"):
+                return int(ln.split()[1])
+    except OSError:
+        pass
+    return None
 
 
 def source_rate(torch, model, keys, nbytes: int = 32 << 20):
@@ -1485,6 +1435,7 @@ def main():
         e2e["link"] = link_summary(link0, link_rates(torch), e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"])
         e2e["copies"] = copylog.summary(n_e2e)
         e2e["link"]["input_buffers_gbs"] = src_gbs
+        e2e["link"]["anon_huge_kb"] = anon_huge_kb()
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / n_e2e
         model.copylog = None
 
