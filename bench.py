@@ -366,11 +366,11 @@ def torch_empty_like(torch, t):
 # DRAM traffic of one attn_decode call over its algorithmic bytes, from an ncu
 # capture (dram__bytes_read.sum + dram__bytes_write.sum of the cascade and the
 # table-pass kernel) of this workload's decode steps 124 and 125, kernels as
-# they stand: 212.42 MB and 213.47 MB of DRAM traffic for 194.72 MB and
+# they stand: 212.39 MB and 213.51 MB of DRAM traffic for 194.72 MB and
 # 195.77 MB of algorithmic bytes.  Traffic grows with the keys read, so the
 # ratio scales it to the average call.
 DECODE_TRAFFIC_RATIO = 1.0905
-DECODE_TRAFFIC_CURRENT = False
+DECODE_TRAFFIC_CURRENT = True
 
 
 def row_bytes(shape):
