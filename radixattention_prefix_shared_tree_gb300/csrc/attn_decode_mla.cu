@@ -372,18 +372,8 @@ rc_status mla_decode(const rc_attn_desc* desc, const void* q, const rc_kv_table*
         t.part_lse = p.part_lse;
         t.out = p.out;
         t.lse = p.lse;
-        constexpr int smem_tc = rc_mla_tc::smem_bytes();
-        dim3 grid_tc(2 * p.n_chunks, batch);
-        if (p.n_chunks == 1) {
-            e = ensure_smem<rc_mla_tc::mla_tc_kernel<true>>(smem_tc);
-            if (e != cudaSuccess) return RC_ERR_CUDA;
-            rc_mla_tc::mla_tc_kernel<true><<<grid_tc, rc_mla_tc::THREADS, smem_tc, st>>>(t);
-            return launch_status(cudaGetLastError());
-        }
-        e = ensure_smem<rc_mla_tc::mla_tc_kernel<false>>(smem_tc);
-        if (e != cudaSuccess) return RC_ERR_CUDA;
-        rc_mla_tc::mla_tc_kernel<false><<<grid_tc, rc_mla_tc::THREADS, smem_tc, st>>>(t);
-        if (cudaGetLastError() != cudaSuccess) return RC_ERR_CUDA;
+        if (p.n_chunks == 1) return launch_status(rc_mla_tc::launch<true>(t, p.n_chunks, batch, st));
+        if (rc_mla_tc::launch<false>(t, p.n_chunks, batch, st) != cudaSuccess) return RC_ERR_CUDA;
         rc_mla::mla_merge_kernel<<<(unsigned)(batch * desc->q_heads), 32, 0, st>>>(p);
         return launch_status(cudaGetLastError());
     }

@@ -422,4 +422,14 @@ __global__ void __launch_bounds__(THREADS, 1) mla_tc_kernel(const Params p) {
     }
 }
 
+// Grid (2 x chunks, batch): x = chunk * 2 + value half.
+template <bool FUSED>
+cudaError_t launch(const Params& t, int n_chunks, int batch, cudaStream_t st) {
+    constexpr int smem = smem_bytes();
+    cudaError_t e = rc_host::ensure_smem<mla_tc_kernel<FUSED>>(smem);
+    if (e != cudaSuccess) return e;
+    mla_tc_kernel<FUSED><<<dim3(2 * n_chunks, batch), THREADS, smem, st>>>(t);
+    return cudaGetLastError();
+}
+
 }  // namespace rc_mla_tc
