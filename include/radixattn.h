@@ -432,9 +432,16 @@ typedef struct rc_decode_step {
 /* n_steps decode steps of one batch queued by one call: for step i, in
  * order, its store (if any) and its attn_decode / attn_decode_append, each
  * with the arguments above and the batch's shared table rows, cascade and
- * workspace (sized by attn_decode_workspace for the largest max_len).  The
- * steps are launched exactly as the per-step calls would launch them, so the
- * results are those calls' results bit for bit.  The pages describe the
+ * workspace (sized by attn_decode_workspace for the largest max_len).  Each
+ * step computes exactly what the per-step call computes, so the results are
+ * those calls' results bit for bit.  One difference in scheduling: when step
+ * i and step i-1 are both append steps (k_new given, no store_slots) and no
+ * event is recorded between them, step i's cascade kernel reads its q and the
+ * cascade segments while step i-1's table pass may still run, and waits for
+ * it only before writing its partials (the table pass writes only rows'
+ * private last keys).  So every step's q and the segments' keys must be
+ * written by work queued before this call, as for any call, and must not be
+ * written by it.  The pages describe the
  * decode phase as a loop of one-token steps [LMI decode phase] and a
  * scheduler that keeps the host's work off the GPU's critical path [SGLang
  * engineering article, section 2: the overlap scheduler]; this call takes the
