@@ -97,3 +97,30 @@ def test_device_calls_refuse_strided_views(built):
         ra._tp(q.transpose(0, 1))
     assert ra._tp(None) is None
     assert ra._tp(q[1]).value == q[1].data_ptr()
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """Every struct the binding passes by pointer has the header's size and
+    field offsets (a C program compiled against include/radixattn.h prints
+    them; the ctypes mirrors must agree field by field)."""
+    structs = {"rc_request": ra.rc_request, "rc_stats_t": ra.rc_stats_t, "rc_pool_desc": ra.rc_pool_desc,
+               "rc_attn_desc": ra.rc_attn_desc, "rc_kv_table": ra.rc_kv_table, "rc_cascade": ra.rc_cascade,
+               "rc_decode_step": ra.rc_decode_step}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "radixattn.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'    printf("{name} size %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'    printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["    return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = {}
+    for ln in subprocess.check_output([str(exe)], text=True).splitlines():
+        name, field, val = ln.split()
+        got[(name, field)] = int(val)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == C.sizeof(cls), name
+        for f, _ in cls._fields_:
+            assert got[(name, f)] == getattr(cls, f).offset, (name, f)
