@@ -373,6 +373,18 @@ DECODE_TRAFFIC_RATIO = 1.0905
 DECODE_TRAFFIC_CURRENT = True
 
 
+# The same ratio for the other configurations' decode calls, from ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum of every kernel of
+# three consecutive decode calls, warm-up step, kernels as they stand) over
+# the bench's average algorithmic bytes per call: agent tree 520.8 MB for 3
+# calls (cascade 30.5, table pass 121.3, merge 21.3 MB each) against 132.6 MB
+# per call -- the split partials the merge reads are not algorithmic bytes;
+# latent 5,093.7 MB for 2 calls (kernel 2,369.5, merge 177.0 MB each) against
+# 2,789.7 MB per call -- the shared prefix and the rows the previous step
+# left in L2 are read from L2.
+CONFIG_TRAFFIC_RATIO = {"agent": 1.309, "mla": 0.913}
+
+
 def row_bytes(shape):
     """K+V bytes of one token: 2 x KV heads x head_dim x 2 B; one 576-wide
     latent row (K and V share it) for the latent layout."""
@@ -847,7 +859,8 @@ def run_config(args, name, rank, world, local):
     launches = eng.launches - launches0
     assert ra.rc_sync(eng.err) == ra.RC_OK
     st = runner.cache.stats()
-    summary, roof = kernel_summary(eng, sh, None, "null: no ncu DRAM capture of this configuration")
+    summary, roof = kernel_summary(eng, sh, CONFIG_TRAFFIC_RATIO.get(name),
+                                   "null: no ncu DRAM capture of this configuration")
     value = whole_job_rate(args.steps * n_dec, world, ms)
 
     e2e = None
