@@ -507,6 +507,11 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ tai
     const int bh = blockIdx.x;
     const int b = bh / q_heads, h = bh % q_heads;
     const int lane = threadIdx.x;
+    // launched as the split pass's programmatic dependent: let the next
+    // kernel launch, then wait for the split pass (and through it the
+    // cascade) before reading anything they wrote
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    grid_dep_wait();
     const int64_t row0 = start[b];
     const int L = len[b];
     // a row the split pass rejected (outside the table) wrote no partials
@@ -869,15 +874,26 @@ rc_status decode_impl(const rc_attn_desc* desc, const void* q, const void* k_new
     const int32_t* rp = use_casc ? casc->req_seg_pos : nullptr;
     const unsigned nbh = (unsigned)batch * desc->q_heads;
     __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+    // the merge is the split pass's programmatic dependent (it waits for it
+    // inside), so its CTAs start as the split pass's leave
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nbh);
+    cfg.blockDim = dim3(32);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (D == 128)
-        merge_kernel<128><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                              pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o,
-                                              lse, P.err);
+        e = cudaLaunchKernelEx(&cfg, merge_kernel<128>, (const float*)dp.part_o, (const float*)dp.part_lse,
+                               dp.n_chunks, dp.chunk, dp.len, (const float*)seg_o, (const float*)seg_lse,
+                               pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o, lse, P.err);
     else
-        merge_kernel<64><<<nbh, 32, 0, st>>>(dp.part_o, dp.part_lse, dp.n_chunks, dp.chunk, dp.len, seg_o, seg_lse,
-                                             pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o,
-                                             lse, P.err);
-    return rc_host::launch_status(cudaGetLastError());
+        e = cudaLaunchKernelEx(&cfg, merge_kernel<64>, (const float*)dp.part_o, (const float*)dp.part_lse,
+                               dp.n_chunks, dp.chunk, dp.len, (const float*)seg_o, (const float*)seg_lse,
+                               pl.seg_chunks, ri, rp, desc->q_heads, dp.start, dp.table_len, o, lse, P.err);
+    return rc_host::launch_status(e);
 }
 
 }  // namespace
