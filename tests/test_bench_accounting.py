@@ -131,3 +131,35 @@ def test_peaks_come_from_the_measured_file():
     assert src == "measured"
     assert (hbm, bf16, bf16_sus) == (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
                                      float(p["bf16_tflops_sustained"]))
+
+
+def test_decode_summary_counts_calls_inside_timed_runs(monkeypatch):
+    """Decode events may span a run of n consecutive calls (the library's
+    step loop records one pair per run): the per-call time is the runs'
+    total over the calls they hold, and the bytes per call the mean over
+    every call inside them -- a single-call event (n = 1) and a run give the
+    same figures when their calls cost the same."""
+    rows = _tree_rows()
+    lay = _fake_layout(rows, cascade=True)
+    shape = GQA_32_8
+
+    class Ev:
+        def __init__(self, ms):
+            self.ms = ms
+
+        def elapsed_time(self, other):
+            return other.ms - self.ms
+
+    monkeypatch.setattr(bench, "peaks", lambda: (6784.8, 1904.6, 1719.1, "measured"))
+    per_call_ms = 0.05
+    # one run of 4 calls (t = 2..5) and one single call (t = 7)
+    eng = SimpleNamespace(events={"attn_decode": [(Ev(0.0), Ev(4 * per_call_ms), ("decode", lay, 2, 4)),
+                                                  (Ev(1.0), Ev(1.0 + per_call_ms), ("decode", lay, 7))]})
+    summary, roof = bench.kernel_summary(eng, shape, traffic_ratio=1.5)
+    d = summary["attn_decode"]
+    assert d["launches"] == 5
+    assert d["avg_us"] == pytest.approx(1e3 * per_call_ms)
+    want = np.mean([bench.decode_bytes(lay, t, shape)[0] for t in (2, 3, 4, 5, 7)])
+    assert d["bytes_per_launch"] == pytest.approx(want)
+    assert roof["achieved"] == pytest.approx(want / (per_call_ms * 1e-3) / 1e9)
+    assert roof["traffic"] == pytest.approx(1.5 * want)
