@@ -70,16 +70,19 @@ class Runner:
 
         overlap=True is the overlapped scheduler (the SGLang engineering
         article's zero-overhead batch scheduler, section 2: the CPU prepares
-        batch k+1 while the GPU runs batch k).  Round k's host calls that
-        follow its prefill -- the finish inserts of round k, then round k+1's
-        whole admission (order, match, pin, evict, alloc) -- run on a worker
-        thread while this thread launches round k's decode steps; the native
-        calls release the interpreter lock, so the two overlap.  The tree
-        sees the same calls in the same order as serve() round by round (the
-        decode launches touch no tree state, and every kernel of round k+1
-        is queued after round k's on the one stream, so slots round k+1
-        takes from round k are written only after round k has read them):
-        results are identical."""
+        batch k+1 while the GPU runs batch k).  Round k's finish inserts,
+        then round k+1's whole admission (order, match, pin, evict, alloc)
+        and its prompt inserts run on a worker thread while this thread
+        launches round k's decode steps; the native calls release the
+        interpreter lock, so the two overlap.  The tree sees the same calls
+        in the same order as serve() round by round (the launches touch no
+        tree state, and every kernel of round k+1 is queued after round k's
+        on the one stream, so slots round k+1 takes from round k are written
+        only after round k has read them).  A round's prompts are inserted
+        before its prefill is queued rather than after: a prompt part another
+        request inserted first then maps to that request's slots, which the
+        prefill fills with the same K/V (a deterministic function of the
+        tokens), so the results are identical."""
         if not overlap:
             while pending:
                 admitted, waiting = self.serve(pending, max_batch)
@@ -87,8 +90,15 @@ class Runner:
             return
         from concurrent.futures import ThreadPoolExecutor
         sched, policy = self.sched, self.policy
+
+        def admit_commit(queue):
+            admitted, waiting = sched.admit(queue, policy, max_batch)
+            if admitted:
+                sched.commit_prompts(admitted)
+            return admitted, waiting
+
         with ThreadPoolExecutor(1) as worker:
-            fut = worker.submit(sched.admit, pending, policy, max_batch)
+            fut = worker.submit(admit_commit, pending)
             while True:
                 admitted, waiting = fut.result()
                 nxt = after(admitted, waiting)
@@ -96,7 +106,6 @@ class Runner:
                 if admitted:
                     if self.engine is not None:
                         self._prefill(admitted)
-                    sched.commit_prompts(admitted)
                     dec = [r for r in admitted if r.max_new]
                     if self.engine is not None and dec:
                         lay = self._decode_layout(dec)     # reads the tree: before the worker goes on
@@ -104,7 +113,7 @@ class Runner:
                 def host_work(admitted=admitted, nxt=nxt):
                     if admitted:
                         sched.finish(admitted)
-                    return sched.admit(nxt, policy, max_batch) if nxt else ([], [])
+                    return admit_commit(nxt) if nxt else ([], [])
                 fut = worker.submit(host_work)
                 if lay is not None:
                     self._decode_steps(dec, lay)
