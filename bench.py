@@ -133,18 +133,48 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def made_events(torch, n, timing=False):
+    """n CUDA events, each recorded once so that the CUDA event exists (it is
+    created at its first record): made before a timed region, they spare the
+    region the host time of creating events."""
+    evs = [torch.cuda.Event(enable_timing=timing) for _ in range(n)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+class EventRing:
+    """Ordering events handed out in turn.  An event is recorded again only
+    n uses later; a stream wait queued earlier keeps the record that was
+    current when it was queued, and every wait here is queued within a few
+    uses of its record."""
+
+    def __init__(self, torch, n=256):
+        self.evs = made_events(torch, n)
+        self.i = 0
+
+    def __call__(self):
+        e = self.evs[self.i]
+        self.i = (self.i + 1) % len(self.evs)
+        return e
+
+
 class CopyLog:
     """CUDA events around every host<->device copy of an e2e leg, recorded on
     the copy's own stream (after its waits): how long the copies themselves
     took during the leg, to set beside the link rates measured alone."""
 
-    def __init__(self, torch):
+    def __init__(self, torch, n_copies=0):
         self.torch = torch
         self.items = []
+        self.spare = made_events(torch, 2 * n_copies, timing=True)
+
+    def _event(self):
+        return self.spare.pop() if self.spare else self.torch.cuda.Event(enable_timing=True)
 
     def run(self, stream, kind, nbytes, fn):
-        a = self.torch.cuda.Event(enable_timing=True)
-        b = self.torch.cuda.Event(enable_timing=True)
+        a, b = self._event(), self._event()
         a.record(stream)
         fn()
         b.record(stream)
@@ -265,6 +295,7 @@ class ReplayModel:
         torch = self.torch
         self.h2d = torch.cuda.Stream()
         self.h2d_ext = torch.cuda.Stream()
+        self.events = EventRing(torch)
 
     def _move_chunk(self, e, c):
         """Queue chunk c's decode inputs (steps cK..cK+K-1) into ring half c mod 2
@@ -276,7 +307,7 @@ class ReplayModel:
         a, b = c * K, min(T, (c + 1) * K)
         if a >= T:
             return
-        free = torch.cuda.Event()
+        free = self.events()
         free.record(torch.cuda.current_stream())
         self.h2d.wait_event(free)
         nbytes = (b - a) * e["dec_step_bytes"]
@@ -289,7 +320,7 @@ class ReplayModel:
         else:
             copy()
         self.h2d_bytes += nbytes
-        ev = torch.cuda.Event()
+        ev = self.events()
         ev.record(self.h2d)
         e["moved"][c] = ev
 
@@ -315,7 +346,7 @@ class ReplayModel:
         else:
             copy()
         self.h2d_bytes += nbytes
-        ev = torch.cuda.Event()
+        ev = self.events()
         ev.record(self.h2d_ext)
         e["ext_moved"] = ev
 
@@ -742,6 +773,7 @@ class OutputsHome:
         self.done = [None, None]
         self.bytes = 0
         self.copylog = None      # a CopyLog timing every copy
+        self.events = EventRing(torch)
 
     def _copy(self, nbytes, fn):
         if self.copylog is not None:
@@ -750,7 +782,7 @@ class OutputsHome:
             fn()
 
     def _after_compute(self):
-        ev = self.torch.cuda.Event()
+        ev = self.events()
         ev.record(self.torch.cuda.current_stream())
         self.stream.wait_event(ev)
 
@@ -779,7 +811,7 @@ class OutputsHome:
         self._copy(m * out.numel() * out.element_size(), copy)
         outs.record_stream(self.stream)
         self.bytes += m * out.numel() * out.element_size()
-        done = self.torch.cuda.Event()
+        done = self.events()
         done.record(self.stream)
         self.done[c % 2] = done
         prev = self.done[(c + 1) % 2]
@@ -875,16 +907,17 @@ def run_config(args, name, rank, world, local):
         model.h2d_bytes = 0
         link0 = link_rates(torch)
         src_gbs = source_rate(torch, model, keys)
-        model.copylog = home.copylog = CopyLog(torch)
+        model.copylog = home.copylog = CopyLog(torch, args.steps * rounds * 2 * (max_new // model.CHUNK + 2))
         wait0 = eng.host_wait_s
         gc.collect()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         h0 = time.perf_counter()
+        worker_wait = 0.0
         for _ in range(args.steps):
             model.rearm()
-            replay(home)
+            worker_wait += replay(home).worker_wait_s
         torch.cuda.current_stream().wait_stream(home.stream)
         e1.record()
         host_s = time.perf_counter() - h0
@@ -899,6 +932,10 @@ def run_config(args, name, rank, world, local):
         e2e["link"]["input_buffers_gbs"] = src_gbs
         e2e["link"]["anon_huge_kb"] = anon_huge_kb()
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / args.steps
+        e2e["host_worker_wait_ms_per_step"] = 1e3 * worker_wait / args.steps
+        # the launching thread's own work: queueing time less its waits for the GPU and for the worker
+        e2e["host_busy_ms_per_step"] = (e2e["host_queue_ms_per_step"] - e2e["host_blocked_ms_per_step"]
+                                        - e2e["host_worker_wait_ms_per_step"])
         model.copylog = home.copylog = None
 
     cpu = None
@@ -1375,12 +1412,15 @@ def main():
         host_ext = torch.empty(ext_rows, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16).pin_memory()
         host_dec = torch.empty(K, args.questions, sh.q_heads, sh.head_dim_v, dtype=torch.bfloat16).pin_memory()
 
+        events = EventRing(torch)
+
         def after_compute():
-            ev = torch.cuda.Event()
+            ev = events()
             ev.record(torch.cuda.current_stream())
             d2h_stream.wait_event(ev)
 
-        copylog = CopyLog(torch)
+        # copies per step: a chunk of decode inputs and of outputs per K steps, the prefill's both ways
+        copylog = CopyLog(torch, n_e2e * 2 * (args.max_new // model.CHUNK + 2))
 
         def copy_extend(out):
             after_compute()
@@ -1408,7 +1448,7 @@ def main():
             copylog.run(d2h_stream, "d2h", m * out.numel() * out.element_size(), copy)
             outs.record_stream(d2h_stream)
             d2h[0] += m * out.numel() * out.element_size()
-            done = torch.cuda.Event()
+            done = events()
             done.record(d2h_stream)
             st["done"][c % 2] = done
             # chunk c+1 writes the other ring half: chunk c-1's copy must be done
@@ -1425,7 +1465,7 @@ def main():
         link0 = link_rates(torch)
         src_gbs = source_rate(torch, model, keys)
         model.copylog = copylog
-        wait0 = eng.host_wait_s
+        wait0, ww0 = eng.host_wait_s, runner.worker_wait_s
         gc.collect()
         gc.freeze()
         if world > 1:
@@ -1450,6 +1490,10 @@ def main():
         e2e["link"]["input_buffers_gbs"] = src_gbs
         e2e["link"]["anon_huge_kb"] = anon_huge_kb()
         e2e["host_blocked_ms_per_step"] = 1e3 * (eng.host_wait_s - wait0) / n_e2e
+        e2e["host_worker_wait_ms_per_step"] = 1e3 * (runner.worker_wait_s - ww0) / n_e2e
+        # the launching thread's own work: queueing time less its waits for the GPU and for the worker
+        e2e["host_busy_ms_per_step"] = (e2e["host_queue_ms_per_step"] - e2e["host_blocked_ms_per_step"]
+                                        - e2e["host_worker_wait_ms_per_step"])
         model.copylog = None
 
     cpu = None

@@ -25,6 +25,8 @@ launches; PyTorch only provides device memory and the stream.
 from __future__ import annotations
 
 import ctypes as C
+import sys
+import threading
 import time
 from dataclasses import dataclass, field
 
@@ -53,6 +55,27 @@ class Request:
     @property
     def n_new(self) -> int:
         return self.prompt_len - self.first
+
+    def tokens_addr(self) -> int:
+        """Address of `tokens` for the native calls (made int32 and
+        C-contiguous first if it is not), kept while the array stays the same."""
+        c = self.__dict__.get("_addr")
+        t = self.tokens
+        if c is None or c[0] is not t:
+            if t.dtype != np.int32 or not t.flags.c_contiguous:
+                t = self.tokens = np.ascontiguousarray(t, np.int32)
+            c = self._addr = (t, t.ctypes.data)
+        return c[1]
+
+
+def _tokens_addr(r) -> int:
+    """Request.tokens_addr for any object with a `tokens` array."""
+    f = getattr(r, "tokens_addr", None)
+    if f is not None:
+        return f()
+    if r.tokens.dtype != np.int32 or not r.tokens.flags.c_contiguous:
+        r.tokens = np.ascontiguousarray(r.tokens, np.int32)
+    return r.tokens.ctypes.data
 
 
 class SchedulerError(RuntimeError):
@@ -85,9 +108,32 @@ def _ok(st, what):
 class Scheduler:
     """Host half of the request lifecycle over a cache object."""
 
+    # slot-row buffers kept for reuse by later native rounds (at most this many)
+    ROW_BUFFERS = 4
+
     def __init__(self, cache, log: list | None = None):
         self.cache = cache
         self.log = log
+        self._rows = []
+
+    def _row_buffer(self, n: int) -> np.ndarray:
+        """A flat int32 array of n entries for one round's slot rows.  The
+        buffer of an earlier round is taken again once nothing refers to it
+        any more (every request's slot row is a view that holds a reference),
+        so its pages are already mapped: the first write to ~2 MB of fresh
+        pages made admission about 3 us per request slower."""
+        for b in self._rows:
+            # references: the list, the loop variable, getrefcount's argument
+            if b.size >= n and sys.getrefcount(b) == 3:
+                return b[:n]
+        b = np.empty(max(n + n // 8, 1 << 12), np.int32)
+        if len(self._rows) >= self.ROW_BUFFERS:
+            free = [i for i, x in enumerate(self._rows) if sys.getrefcount(x) == 3]
+            if free:
+                del self._rows[min(free, key=lambda i: self._rows[i].size)]
+        if len(self._rows) < self.ROW_BUFFERS:
+            self._rows.append(b)
+        return b[:n]
 
     def _rec(self, *item):
         if self.log is not None:
@@ -144,17 +190,14 @@ class Scheduler:
         """One rc_admit over a record array filled column by column; the slot
         rows of the round's requests are views into one flat array."""
         n = len(pending)
-        for r in pending:
-            if r.tokens.dtype != np.int32 or not r.tokens.flags.c_contiguous:
-                r.tokens = np.ascontiguousarray(r.tokens, np.int32)
         req = np.zeros(n, _REQ_DTYPE)
-        req["tokens"] = np.fromiter((r.tokens.ctypes.data for r in pending), np.uint64, n)
+        req["tokens"] = np.fromiter((_tokens_addr(r) for r in pending), np.uint64, n)
         plen = np.fromiter((r.prompt_len for r in pending), np.int64, n)
         mnew = np.fromiter((r.max_new for r in pending), np.int64, n)
         req["prompt_len"], req["max_new"] = plen, mnew
         off = np.zeros(n + 1, np.int64)
         np.cumsum(plen + mnew, out=off[1:])
-        flat = np.empty(int(off[-1]), np.int32)
+        flat = self._row_buffer(int(off[-1]))
         req["slots"] = np.uint64(flat.ctypes.data) + 4 * off[:-1].astype(np.uint64)
         order = np.empty(n, np.int32)
         st, cnt = self.cache.admit_batch(policy, req, n, max_batch or 0, order)
@@ -324,8 +367,11 @@ class DeviceEngine:
         self.desc = make_attn_desc(self.pool, shape.q_heads, shape.scale)
         self.sms = torch.cuda.get_device_properties(dev).multi_processor_count if dev.type == "cuda" else 1
         self._ws = torch.zeros(1 << 20, dtype=torch.uint8, device=dev)
-        self._stage = [None, None]   # [pinned host int32, device int32, event] x 2, used in turn
+        self._stage = [None, None, None]   # [pinned host int32, device int32, event] x 3, used in turn
         self._stage_next = 0
+        self._stage_packed = [False] * len(self._stage)   # packed, copy not yet queued
+        self._stage_lock = threading.Lock()
+        self.pack_wait_s = 0.0       # pack() time blocked on the GPU (on whichever thread packs)
         self.timing = False          # record CUDA events around device calls
         self.timing_every = 1        # decode steps: events on every n-th step only
         self.fuse_store = not kv_fp8  # decode steps store the new token inside attn_decode_append (bf16 pools)
@@ -383,35 +429,59 @@ class DeviceEngine:
     def stage(self, arrays: list) -> list:
         """Host int32 arrays -> device, through one pinned staging buffer and
         one host-to-device copy; returns device views in the same order and
-        shapes.  Two staging buffers are used in turn, and one is rewritten
-        only after the copy that last read it has run.  The device copy is
-        ordered on the current stream after every earlier kernel, so kernels
-        of the previous batch have finished reading a buffer it overwrites."""
+        shapes (pack() then upload())."""
+        t0 = self.pack_wait_s
+        ticket = self.pack(arrays)
+        self.host_wait_s += self.pack_wait_s - t0
+        return self.upload(ticket)
+
+    def pack(self, arrays: list):
+        """Host half of stage(): the arrays packed into the next pinned
+        staging buffer (256-byte aligned views).  May run on another thread
+        than upload(); each ticket must be uploaded before two more are
+        packed.  A buffer is rewritten only after the copy that last read it
+        has run (host wait counted in pack_wait_s)."""
         torch = self.torch
         offs, n = [], 0
         for a in arrays:
             offs.append(n)
-            n += (a.size + 63) // 64 * 64      # 256-byte aligned views
+            n += (a.size + 63) // 64 * 64
         n = max(n, 64)
-        k = self._stage_next
-        self._stage_next ^= 1
+        with self._stage_lock:
+            k = self._stage_next
+            self._stage_next = (k + 1) % len(self._stage)
+            if self._stage_packed[k]:
+                raise RuntimeError("staging buffer packed twice without an upload")
+            self._stage_packed[k] = True
         slot = self._stage[k]
-        if slot is not None:
+        if slot is None:
+            slot = self._stage[k] = [None, None, torch.cuda.Event()]
+        else:
             t0 = time.perf_counter()
             slot[2].synchronize()
-            self.host_wait_s += time.perf_counter() - t0
-        if slot is None or slot[0].numel() < n:
-            cap = max(n + n // 4, 1 << 16)
-            slot = [torch.empty(cap, dtype=torch.int32).pin_memory(),
-                    torch.empty(cap, dtype=torch.int32, device=self.device), torch.cuda.Event()]
-            self._stage[k] = slot
-        host, dev, ev = slot
-        hv = host.numpy()
+            self.pack_wait_s += time.perf_counter() - t0
+        if slot[0] is None or slot[0].numel() < n:   # (the device half grows in upload())
+            slot[0] = torch.empty(max(n + n // 4, 1 << 16), dtype=torch.int32).pin_memory()
+        hv = slot[0].numpy()
         for a, o in zip(arrays, offs):
             hv[o:o + a.size] = a.reshape(-1)
+        return k, n, [(o, a.size, a.shape) for a, o in zip(arrays, offs)]
+
+    def upload(self, ticket) -> list:
+        """Device half of stage(): one host-to-device copy of a packed buffer,
+        ordered on the current stream after every earlier kernel (so kernels
+        of an earlier batch have finished reading the device buffer it
+        overwrites); returns the device views."""
+        k, n, views = ticket
+        slot = self._stage[k]
+        if slot[1] is None or slot[1].numel() < n:
+            slot[1] = self.torch.empty(slot[0].numel(), dtype=self.torch.int32, device=self.device)
+        host, dev, ev = slot
         dev[:n].copy_(host[:n], non_blocking=True)
         ev.record()
-        return [dev[o:o + a.size].view(a.shape) for a, o in zip(arrays, offs)]
+        with self._stage_lock:
+            self._stage_packed[k] = False
+        return [dev[o:o + size].view(shape) for o, size, shape in views]
 
     def upload_batch(self, batch: list, cascade: bool, planner=None, parts=("extend", "decode")):
         """Slot rows and index arrays of the batch -> device; returns its layout."""
@@ -439,11 +509,16 @@ class DeviceEngine:
         lay.ws = self.workspace(lay.ws_bytes)
         lay.ws_ptr = lay.ws.data_ptr()
         lay.casc_ref = C.byref(casc) if casc is not None else None
-        lay.slot_ptrs = [lay.decode_slots[t].data_ptr() for t in range(T)]
+        # step t's rows of the [T, B] int32 arrays: base + 4 B t (no per-step tensor views)
+        if T:
+            assert lay.decode_slots.is_contiguous() and lay.dec_len.is_contiguous()
+        p0 = lay.decode_slots.data_ptr() if T else 0
+        lay.slot_ptrs = [p0 + 4 * B * t for t in range(T)]
         # one table descriptor, its length row and bound set per step
         lay.kv = make_kv_table(lay.table, lay.dec_start, lay.dec_len[0], dec_max[0]) if T else None
         lay.kv_ref = C.byref(lay.kv) if T else None
-        lay.len_ptrs = [lay.dec_len[t].data_ptr() for t in range(T)]
+        p0 = lay.dec_len.data_ptr() if T else 0
+        lay.len_ptrs = [p0 + 4 * B * t for t in range(T)]
         lay.dec_max_list = dec_max
         lay.pool_ref = C.byref(self.pool)
         lay.desc_ref = C.byref(self.desc)
@@ -572,7 +647,10 @@ class BatchLayout:
     array with vectorised indexing; otherwise from each request's slot row."""
 
     def __init__(self, eng: DeviceEngine, batch: list, cascade: bool, planner=None,
-                 parts=("extend", "decode")):
+                 parts=("extend", "decode"), defer: bool = False):
+        """defer=True stops after the host arrays are packed into a staging
+        buffer (eng.pack: it may run on a worker thread); upload() then
+        queues the copy and sets the device views."""
         self.eng = eng
         self.batch = batch
         self.batch_size = B = len(batch)
@@ -642,7 +720,23 @@ class BatchLayout:
         casc_keys = ("seg_slots", "seg_indptr", "seg_row_indptr", "seg_rows", "req_seg_indptr", "req_seg_pos")
         if plan is not None:
             host += [np.asarray(plan[k]) for k in casc_keys]
-        dv = eng.stage([np.asarray(a, np.int32) for a in host])
+        host = [np.asarray(a, np.int32) for a in host]
+        self._names, self._plan, self._T, self._parts = names, plan, T, parts
+        self._ticket = None
+        if defer:
+            self._ticket = eng.pack(host)
+        else:
+            self._set_device(eng.stage(host))
+
+    def upload(self):
+        """The deferred half: the packed arrays' copy and the device views."""
+        self._set_device(self.eng.upload(self._ticket))
+        self._ticket = None
+        return self
+
+    def _set_device(self, dv):
+        names, plan, T, parts = self._names, self._plan, self._T, self._parts
+        B, L = self.batch_size, self.L
         for nm, t in zip(names, dv):
             setattr(self, nm, t)
         if "extend" not in parts:

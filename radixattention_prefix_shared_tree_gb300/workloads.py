@@ -10,6 +10,8 @@ token sequences and Q/K/V rows; the workload shapes come from the caller.
 """
 from __future__ import annotations
 
+import time
+
 import numpy as np
 
 from . import RC_LPM
@@ -19,7 +21,9 @@ from .driver import Request, Scheduler
 def new_request(model, rid: int, prompt, max_new: int) -> Request:
     toks, hashes = model.sequence(np.asarray(prompt, np.int32), max_new)
     model.register(rid, hashes)
-    return Request(rid=rid, tokens=toks, prompt_len=len(prompt), max_new=max_new)
+    r = Request(rid=rid, tokens=toks, prompt_len=len(prompt), max_new=max_new)
+    r.tokens_addr()   # taken once, at intake, rather than in every admission round
+    return r
 
 
 class Runner:
@@ -45,6 +49,7 @@ class Runner:
         self.decode_out_slots = 1  # decode step t writes slot t mod this of `decode_outs`
         self.decode_chunk = 16     # decode steps queued per library call
         self.decode_outs = None
+        self.worker_wait_s = 0.0   # overlapped rounds: time this thread waited for the worker
 
     def request(self, prompt, max_new: int) -> Request:
         r = new_request(self.model, self.next_rid, prompt, max_new)
@@ -71,10 +76,11 @@ class Runner:
         overlap=True is the overlapped scheduler (the SGLang engineering
         article's zero-overhead batch scheduler, section 2: the CPU prepares
         batch k+1 while the GPU runs batch k).  Round k's finish inserts,
-        then round k+1's whole admission (order, match, pin, evict, alloc)
-        and its prompt inserts run on a worker thread while this thread
-        launches round k's decode steps; the native calls release the
-        interpreter lock, so the two overlap.  The tree sees the same calls
+        then round k+1's whole admission (order, match, pin, evict, alloc),
+        its prompt inserts and its index arrays (slot table, cascade plan,
+        packed into a pinned staging buffer) are made on a worker thread
+        while this thread launches round k's decode steps; the native calls
+        release the interpreter lock, so the two overlap.  The tree sees the same calls
         in the same order as serve() round by round (the launches touch no
         tree state, and every kernel of round k+1 is queued after round k's
         on the one stream, so slots round k+1 takes from round k are written
@@ -93,37 +99,47 @@ class Runner:
 
         def admit_commit(queue):
             admitted, waiting = sched.admit(queue, policy, max_batch)
+            ready = None
             if admitted:
                 sched.commit_prompts(admitted)
-            return admitted, waiting
+                if self.engine is not None and self._one_layout(admitted):
+                    ready = self._round_layout(admitted, defer=True)   # packed here, uploaded by the caller
+            return admitted, waiting, ready
 
         with ThreadPoolExecutor(1) as worker:
             fut = worker.submit(admit_commit, pending)
             while True:
-                admitted, waiting = fut.result()
+                t_wait = time.perf_counter()
+                admitted, waiting, ready = fut.result()
+                self.worker_wait_s += time.perf_counter() - t_wait
                 nxt = after(admitted, waiting)
                 lay = None
-                if admitted:
-                    if self.engine is not None:
-                        self._prefill(admitted)
+                if admitted and self.engine is not None:
                     dec = [r for r in admitted if r.max_new]
-                    if self.engine is not None and dec:
-                        lay = self._decode_layout(dec)     # reads the tree: before the worker goes on
+                    ext = None
+                    if ready is not None:
+                        ext = self.last_layout = ready.upload()
+                    self._prefill(admitted, ext)
+                    if dec:   # (a decode layout reads the tree: before the worker goes on)
+                        lay = ext if ext is not None else self._decode_layout(dec)
 
                 def host_work(admitted=admitted, nxt=nxt):
                     if admitted:
                         sched.finish(admitted)
-                    return admit_commit(nxt) if nxt else ([], [])
+                    return admit_commit(nxt) if nxt else ([], [], None)
                 fut = worker.submit(host_work)
                 if lay is not None:
                     self._decode_steps(dec, lay)
                 if not nxt:
+                    t_wait = time.perf_counter()
                     fut.result()
+                    self.worker_wait_s += time.perf_counter() - t_wait
                     return
 
-    def _prefill(self, batch):
+    def _prefill(self, batch, lay=None):
         eng, torch = self.engine, self.engine.torch
-        lay = eng.upload_batch(batch, cascade=False, parts=("extend",))
+        if lay is None:
+            lay = eng.upload_batch(batch, cascade=False, parts=("extend",))
         total = int(lay.qo_host[-1])
         if total == 0:
             return
@@ -157,6 +173,21 @@ class Runner:
         lay = self.engine.upload_batch(batch, cascade=self.cascade, planner=planner, parts=("decode",))
         self.last_layout = lay
         return lay
+
+    @staticmethod
+    def _one_layout(batch) -> bool:
+        """Every request decodes, the same number of tokens: one layout
+        serves the round's prefill and its decode steps."""
+        return all(r.max_new for r in batch) and len({r.max_new for r in batch}) == 1
+
+    def _round_layout(self, batch, defer: bool = False):
+        """One layout for the prefill and the decode steps of a round
+        (_one_layout), laid out after the round's prompt inserts so the slot
+        table is staged once instead of once per phase.  defer=True: host
+        arrays packed, BatchLayout.upload() left to the launching thread."""
+        from .driver import BatchLayout
+        planner = getattr(self.cache, "cascade_plan", None)
+        return BatchLayout(self.engine, batch, self.cascade, planner, ("extend", "decode"), defer=defer)
 
     def _decode_steps(self, batch, lay):
         """Every decode step of the batch, in runs of up to `decode_chunk`
