@@ -803,11 +803,14 @@ class OutputsHome:
         c = t // K
         outs = self.runner.decode_outs
         a, m = (c % 2) * K, t - c * K + 1
-        B = outs.shape[1]
         self._after_compute()
+        # a contiguous destination: a copy into a strided slice of pinned
+        # memory goes through a staging tensor and does not return at once
+        dst = self.host_dec.view(-1)[:outs[a:a + m].numel()].view(m, *outs.shape[1:])
+
         def copy():
             with self.torch.cuda.stream(self.stream):
-                self.host_dec[:m, :B].copy_(outs[a:a + m], non_blocking=True)
+                dst.copy_(outs[a:a + m], non_blocking=True)
         self._copy(m * out.numel() * out.element_size(), copy)
         outs.record_stream(self.stream)
         self.bytes += m * out.numel() * out.element_size()
