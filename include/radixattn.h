@@ -174,6 +174,10 @@ rc_status rc_admit(rc_cache* cache, int policy, rc_request* reqs, int32_t n, int
  * RC_COMMIT_FINISH: rc_insert(prompt + generated, slots) unpinned and drop the
  *   request's pin [N49 s.2: a finished request's path, outputs included,
  *   stays] (requests with max_new == 0 are skipped).
+ * The records must be as rc_admit (and, for FINISH, the PREFILL commit) left
+ * them: each insert starts at the request's pinned node, so slots[0..first)
+ * (PREFILL) and slots[0..prompt_len) (FINISH), which hold the tree's own
+ * slots there, are not read again.
  * Errors: RC_ERR_ARG, or the first failing rc_insert / rc_release status
  * (requests before it are committed). */
 #define RC_COMMIT_PREFILL 0

@@ -135,20 +135,31 @@ struct rc_cache : rc_pool::SlotPool {
     // `sl` (if given, room for n) receives the matched slots.  A match that
     // stops inside an edge leaves that child in *mid and its matched count in
     // *mid_k (else *mid = -1).
+    //
+    // from / from_depth: start below node `from`, whose path from the root
+    // spells tok[0..from_depth) (the caller knows it: a pinned node the same
+    // tokens reached before); positions below from_depth are neither
+    // compared nor copied to `sl`.  known >= 0: the match is known to be
+    // exactly `known` tokens long (a walk of the same tokens since which no
+    // node was removed), so tokens are not compared either.
     int64_t walk(const int32_t* tok, int64_t n, std::vector<int32_t>* pth, int32_t* sl, int32_t* mid,
-                 int32_t* mid_k) const {
-        int32_t cur = 0;
-        if (pth) { pth->clear(); pth->push_back(0); }
+                 int32_t* mid_k, int32_t from = 0, int64_t from_depth = 0, int64_t known = -1) const {
+        int32_t cur = from;
+        if (pth) {
+            pth->clear();
+            for (int32_t k = from; k >= 0; k = recs[(size_t)k].parent) pth->push_back(k);
+            std::reverse(pth->begin(), pth->end());
+        }
         if (mid) *mid = -1;
-        int64_t i = 0;
-        while (i < n) {
+        int64_t i = from_depth;
+        const int64_t end = known >= 0 ? known : n;
+        while (i < end) {
             auto it = edges.find(edge_key(cur, tok[i]));
             if (it == edges.end()) break;
             int32_t c = it->second;
             const Rec& r = recs[(size_t)c];
-            const int32_t* rt = toks(r);
-            int64_t lim = std::min<int64_t>(r.len, n - i);
-            int64_t k = 1 + common_prefix(rt + 1, tok + i + 1, lim - 1);
+            int64_t lim = std::min<int64_t>(r.len, end - i);
+            int64_t k = known >= 0 ? lim : 1 + common_prefix(toks(r) + 1, tok + i + 1, lim - 1);
             if (sl) std::memcpy(sl + i, slot_arena.data() + r.off, (size_t)k * 4);
             i += k;
             if (k < r.len) {
@@ -161,11 +172,18 @@ struct rc_cache : rc_pool::SlotPool {
         return i;
     }
 
+    // Tokens on the path root..node i (its depth).
+    int64_t depth(int32_t i) const {
+        int64_t d = 0;
+        for (; i > 0; i = recs[(size_t)i].parent) d += recs[(size_t)i].len;
+        return d;
+    }
+
     // walk() with the end of the match made a node boundary: a stop inside
     // an edge splits it and the upper part ends `pth`.
-    int64_t descend(const int32_t* tok, int64_t n, std::vector<int32_t>* pth, int32_t* sl) {
+    int64_t descend(const int32_t* tok, int64_t n, std::vector<int32_t>* pth, int32_t* sl, int64_t known = -1) {
         int32_t mid = -1, k = 0;
-        int64_t m = walk(tok, n, pth, sl, &mid, &k);
+        int64_t m = walk(tok, n, pth, sl, &mid, &k, 0, 0, known);
         if (mid >= 0) {
             int32_t up = split(mid, k);
             if (pth) pth->push_back(up);
@@ -235,11 +253,16 @@ rc_status rc_create(int64_t pool_slots, rc_cache** out) {
 
 void rc_destroy(rc_cache* c) { delete c; }
 
-rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, int64_t* matched,
-                          int32_t* out_slots, rc_node* out_node) {
+}  // extern "C"
+
+namespace {
+
+// rc_match_prefix; known >= 0: the match length is already known (see walk).
+rc_status match_impl(rc_cache* c, const int32_t* tok, int64_t n, int pin, int64_t* matched, int32_t* out_slots,
+                     rc_node* out_node, int64_t known) {
     if (!c || n < 0 || (n > 0 && !tok) || !matched || !out_node) return RC_ERR_ARG;
     c->clock += 1;
-    int64_t m = c->descend(tok, n, &c->path, out_slots);
+    int64_t m = c->descend(tok, n, &c->path, out_slots, known);
     c->touch(c->path, pin != 0);
     *matched = m;
     *out_node = c->recs[(size_t)c->path.back()].id;
@@ -250,6 +273,15 @@ rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, i
     return RC_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+rc_status rc_match_prefix(rc_cache* c, const int32_t* tok, int64_t n, int pin, int64_t* matched,
+                          int32_t* out_slots, rc_node* out_node) {
+    return match_impl(c, tok, n, pin, matched, out_slots, out_node, -1);
+}
+
 // Every slot id in [0, pool); a branch-free scan.
 static bool slots_in_pool(const rc_cache* c, const int32_t* slots, int64_t n) {
     const uint32_t pool = (uint32_t)c->pool;  // at most 2^31 - 1: a negative id reads as >= pool
@@ -258,17 +290,24 @@ static bool slots_in_pool(const rc_cache* c, const int32_t* slots, int64_t n) {
     return bad == 0;
 }
 
-rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64_t n, int pin,
-                    int64_t* already_present, rc_node* out_node, int32_t* out_slots) {
+}  // extern "C"
+
+namespace {
+
+// rc_insert starting below node `from`, whose path spells tok[0..d0) and
+// holds slots[0..d0) (see walk): those positions are neither compared nor
+// range-checked again.  from = 0, d0 = 0 is rc_insert itself.
+rc_status insert_impl(rc_cache* c, const int32_t* tok, const int32_t* slots, int64_t n, int pin,
+                      int64_t* already_present, rc_node* out_node, int32_t* out_slots, int32_t from, int64_t d0) {
     if (!c || n < 0 || (n > 0 && (!tok || !slots)) || !already_present || !out_node) return RC_ERR_ARG;
-    if (!slots_in_pool(c, slots, n)) return RC_ERR_ARG;
+    if (!slots_in_pool(c, slots + d0, n - d0)) return RC_ERR_ARG;
     std::vector<int32_t>& have = c->scratch_slots;
     if ((int64_t)have.size() < n) have.resize((size_t)n);
     int32_t mid = -1, mid_k = 0;
-    int64_t m = c->walk(tok, n, &c->path, have.data(), &mid, &mid_k);   // look first, change nothing
+    int64_t m = c->walk(tok, n, &c->path, have.data(), &mid, &mid_k, from, d0);   // look first, change nothing
     c->new_epoch();
     // positions whose slot is already the cached one need no check
-    const int64_t same = common_prefix(slots, have.data(), m);
+    const int64_t same = d0 + common_prefix(slots + d0, have.data() + d0, m - d0);
     for (int64_t i = same; i < n; ++i) {
         int32_t s = slots[i];
         if (i < m && s == have[(size_t)i]) continue;
@@ -304,7 +343,8 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     c->n_free += dup;
     c->touch(c->path, pin != 0);
     if (out_slots) {
-        if (m) std::memcpy(out_slots, have.data(), (size_t)m * 4);
+        if (d0 && out_slots != slots) std::memmove(out_slots, slots, (size_t)d0 * 4);   // the tree's, by contract
+        if (m > d0) std::memcpy(out_slots + d0, have.data() + d0, (size_t)(m - d0) * 4);
         if (n > m && out_slots != slots) std::memmove(out_slots + m, slots + m, (size_t)(n - m) * 4);
     }
     *already_present = m;
@@ -313,6 +353,15 @@ rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64
     c->insert_new_tokens += n - m;
     c->insert_dup_freed += dup;
     return RC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rc_status rc_insert(rc_cache* c, const int32_t* tok, const int32_t* slots, int64_t n, int pin,
+                    int64_t* already_present, rc_node* out_node, int32_t* out_slots) {
+    return insert_impl(c, tok, slots, n, pin, already_present, out_node, out_slots, 0, 0);
 }
 
 rc_status rc_release(rc_cache* c, rc_node node) {
@@ -379,21 +428,39 @@ rc_status rc_free(rc_cache* c, const int32_t* slots, int64_t n) {
     return r == -1 ? RC_ERR_ARG : r == -2 ? RC_ERR_STATE : RC_OK;
 }
 
-rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, const int64_t* lens,
-                      int32_t n, int32_t* out_order) {
+}  // extern "C"
+
+namespace {
+
+// sched_order; peek (optional, room for n) receives each prompt's peek match
+// length under RC_LPM (left untouched under RC_FCFS).
+rc_status order_impl(rc_cache* c, int policy, const int32_t* const* prompts, const int64_t* lens, int32_t n,
+                     int32_t* out_order, int64_t* peek) {
     if (!c || n < 0 || (n > 0 && (!prompts || !lens || !out_order))) return RC_ERR_ARG;
     if (policy != RC_FCFS && policy != RC_LPM) return RC_ERR_ARG;
     for (int32_t i = 0; i < n; ++i)
         if (lens[i] < 0 || (lens[i] > 0 && !prompts[i])) return RC_ERR_ARG;
     for (int32_t i = 0; i < n; ++i) out_order[i] = i;
-    if (policy == RC_LPM && n > 1) {
+    if (policy == RC_LPM && (n > 1 || peek)) {
         std::vector<std::pair<int64_t, int32_t>> key((size_t)n);
-        for (int32_t i = 0; i < n; ++i)
-            key[(size_t)i] = {-c->walk(prompts[i], lens[i], nullptr, nullptr, nullptr, nullptr), i};
+        for (int32_t i = 0; i < n; ++i) {
+            const int64_t m = c->walk(prompts[i], lens[i], nullptr, nullptr, nullptr, nullptr);
+            if (peek) peek[i] = m;
+            key[(size_t)i] = {-m, i};
+        }
         std::sort(key.begin(), key.end());  // (-match, index): longest first, then arrival
         for (int32_t i = 0; i < n; ++i) out_order[i] = key[(size_t)i].second;
     }
     return RC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rc_status sched_order(rc_cache* c, int policy, const int32_t* const* prompts, const int64_t* lens,
+                      int32_t n, int32_t* out_order) {
+    return order_impl(c, policy, prompts, lens, n, out_order, nullptr);
 }
 
 rc_status rc_admit(rc_cache* c, int policy, rc_request* reqs, int32_t n, int32_t max_batch, int32_t* out_order,
@@ -414,17 +481,22 @@ rc_status rc_admit(rc_cache* c, int policy, rc_request* reqs, int32_t n, int32_t
         reqs[i].node = -1;
     }
     std::vector<int32_t> order((size_t)n);
-    rc_status st = sched_order(c, policy, prompts.data(), lens.data(), n, order.data());
+    std::vector<int64_t> peek((size_t)n, -1);
+    rc_status st = order_impl(c, policy, prompts.data(), lens.data(), n, order.data(), peek.data());
     if (st != RC_OK) return st;
+    // the LPM peeks stay exact match lengths until a node is removed: the
+    // matches below only split edges (same tokens), pin and stamp
+    const int64_t evicted0 = c->evicted_nodes;
     int32_t count = 0;
     for (int32_t k = 0; k < n; ++k) {
         if (max_batch > 0 && count >= max_batch) break;
         rc_request& r = reqs[order[(size_t)k]];
         int64_t m = 0;
         rc_node node = 0;
+        const int64_t known = c->evicted_nodes == evicted0 ? peek[(size_t)order[(size_t)k]] : -1;
         // the matched slots land in the row itself (room for prompt_len + max_new >= matched);
         // the new ones then overwrite it from `first` on
-        st = rc_match_prefix(c, r.tokens, r.prompt_len, 1, &m, r.slots, &node);
+        st = match_impl(c, r.tokens, r.prompt_len, 1, &m, r.slots, &node, known);
         if (st != RC_OK) return st;
         const int64_t first = r.max_new > 0 ? std::min(m, r.prompt_len - 1) : m;
         const int64_t need = r.prompt_len - first + r.max_new;
@@ -460,9 +532,29 @@ rc_status rc_commit(rc_cache* c, rc_request* reqs, const int32_t* idx, int32_t n
         if (mode == RC_COMMIT_FINISH && r.max_new == 0) continue;
         const int64_t len = mode == RC_COMMIT_PREFILL ? r.prompt_len : r.prompt_len + r.max_new;
         const int pin = mode == RC_COMMIT_PREFILL && r.max_new > 0;
+        // The request's pinned node spells its first tokens: the match of
+        // rc_admit (slots[0..first) are its slots), or the prompt inserted
+        // by the prefill commit (slots[0..prompt_len) are the tree's).  The
+        // insert starts at its deepest ancestor within those positions.
+        int32_t from = 0;
+        int64_t d0 = 0;
+        const auto it = c->by_id.find(r.node);
+        if (it != c->by_id.end()) {
+            const int64_t known = mode == RC_COMMIT_PREFILL ? r.first : r.prompt_len;
+            int32_t k = it->second;
+            int64_t d = c->depth(k);
+            while (k > 0 && d > known) {
+                d -= c->recs[(size_t)k].len;
+                k = c->recs[(size_t)k].parent;
+            }
+            if (d <= known && known <= len) {
+                from = k;
+                d0 = d;
+            }
+        }
         int64_t present = 0;
         rc_node node = -1;
-        rc_status st = rc_insert(c, r.tokens, r.slots, len, pin, &present, &node, r.slots);
+        rc_status st = insert_impl(c, r.tokens, r.slots, len, pin, &present, &node, r.slots, from, d0);
         if (st != RC_OK) return st;
         st = rc_release(c, r.node);
         if (st != RC_OK) return st;
