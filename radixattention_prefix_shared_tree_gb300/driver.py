@@ -191,10 +191,13 @@ class Scheduler:
         rows of the round's requests are views into one flat array."""
         n = len(pending)
         req = np.zeros(n, _REQ_DTYPE)
-        req["tokens"] = np.fromiter((_tokens_addr(r) for r in pending), np.uint64, n)
-        plen = np.fromiter((r.prompt_len for r in pending), np.int64, n)
-        mnew = np.fromiter((r.max_new for r in pending), np.int64, n)
-        req["prompt_len"], req["max_new"] = plen, mnew
+        addr, plen, mnew = [0] * n, [0] * n, [0] * n
+        for i, r in enumerate(pending):   # one pass over the requests
+            c = getattr(r, "_addr", None)   # Request.tokens_addr's cache
+            addr[i] = c[1] if c is not None and c[0] is r.tokens else _tokens_addr(r)
+            plen[i], mnew[i] = r.prompt_len, r.max_new
+        req["tokens"], req["prompt_len"], req["max_new"] = addr, plen, mnew
+        plen, mnew = req["prompt_len"], req["max_new"]
         off = np.zeros(n + 1, np.int64)
         np.cumsum(plen + mnew, out=off[1:])
         flat = self._row_buffer(int(off[-1]))
