@@ -433,9 +433,8 @@ class DeviceEngine:
         """Host int32 arrays -> device, through one pinned staging buffer and
         one host-to-device copy; returns device views in the same order and
         shapes (pack() then upload())."""
-        t0 = self.pack_wait_s
         ticket = self.pack(arrays)
-        self.host_wait_s += self.pack_wait_s - t0
+        self.host_wait_s += ticket[3]
         return self.upload(ticket)
 
     def pack(self, arrays: list):
@@ -457,25 +456,27 @@ class DeviceEngine:
                 raise RuntimeError("staging buffer packed twice without an upload")
             self._stage_packed[k] = True
         slot = self._stage[k]
+        waited = 0.0
         if slot is None:
             slot = self._stage[k] = [None, None, torch.cuda.Event()]
         else:
             t0 = time.perf_counter()
             slot[2].synchronize()
-            self.pack_wait_s += time.perf_counter() - t0
+            waited = time.perf_counter() - t0
+            self.pack_wait_s += waited
         if slot[0] is None or slot[0].numel() < n:   # (the device half grows in upload())
             slot[0] = torch.empty(max(n + n // 4, 1 << 16), dtype=torch.int32).pin_memory()
         hv = slot[0].numpy()
         for a, o in zip(arrays, offs):
             hv[o:o + a.size] = a.reshape(-1)
-        return k, n, [(o, a.size, a.shape) for a, o in zip(arrays, offs)]
+        return k, n, [(o, a.size, a.shape) for a, o in zip(arrays, offs)], waited
 
     def upload(self, ticket) -> list:
         """Device half of stage(): one host-to-device copy of a packed buffer,
         ordered on the current stream after every earlier kernel (so kernels
         of an earlier batch have finished reading the device buffer it
         overwrites); returns the device views."""
-        k, n, views = ticket
+        k, n, views, _ = ticket
         slot = self._stage[k]
         if slot[1] is None or slot[1].numel() < n:
             slot[1] = self.torch.empty(slot[0].numel(), dtype=self.torch.int32, device=self.device)

@@ -80,15 +80,16 @@ class Runner:
         its prompt inserts and its index arrays (slot table, cascade plan,
         packed into a pinned staging buffer) are made on a worker thread
         while this thread launches round k's decode steps; the native calls
-        release the interpreter lock, so the two overlap.  The tree sees the same calls
-        in the same order as serve() round by round (the launches touch no
-        tree state, and every kernel of round k+1 is queued after round k's
-        on the one stream, so slots round k+1 takes from round k are written
-        only after round k has read them).  A round's prompts are inserted
-        before its prefill is queued rather than after: a prompt part another
-        request inserted first then maps to that request's slots, which the
-        prefill fills with the same K/V (a deterministic function of the
-        tokens), so the results are identical."""
+        release the interpreter lock, so the two overlap.  The tree sees the
+        same calls in the same order as serve() round by round (the launches
+        touch no tree state, and every kernel of round k+1 is queued after
+        round k's on the one stream, so slots round k+1 takes from round k
+        are written only after round k has read them).  A round's prompts
+        are inserted before its prefill is queued rather than after: a
+        prompt part another request inserted first then maps to that
+        request's slots, which the prefill fills with the same K/V (a
+        deterministic function of the tokens), so the results are
+        identical."""
         if not overlap:
             while pending:
                 admitted, waiting = self.serve(pending, max_batch)
