@@ -285,3 +285,60 @@ def test_overlapped_rounds_equal_serial_host(built, which):
         outs.append((rec.rec, cache.dump(), cache.stats()))
     assert outs[0] == outs[1]
     assert any(r[0] == "admit" and r[2] for r in outs[0][0])   # rounds with waiting requests
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_rounds_admit_commit_bit_exact(built, seed):
+    """Random multi-round serving against the oracle's own admission round
+    and commits (note 49, sections 2, 4 and 5): prompts drawn as extensions
+    of earlier ones over a 4-token vocabulary (deep sharing, mid-edge
+    splits, fully cached prompts that recompute their last token), a pool
+    small enough to evict inside admission, batch caps, prefill-only
+    requests.  The native path inserts from each request's pinned node and
+    reuses the order's peek lengths; every record, tree and statistic must
+    equal the oracle's."""
+    class R:
+        def __init__(self, rid, toks, mnew):
+            self.rid, self.tokens = rid, np.asarray(toks, np.int32)
+            self.prompt_len, self.max_new = len(toks) - mnew, mnew
+            self.node, self.slots = -1, None
+
+    def run(kind):
+        rng = np.random.default_rng(seed)
+        cache = oracle.OracleTree(160) if kind == "oracle" else ra.RadixCache(160)
+        srv = oracle.OracleServer(cache) if kind == "oracle" else Scheduler(cache)
+        seen, rec, rid = [np.asarray([0, 1], np.int32)], [], 0
+        pending = []
+        for rnd in range(30):
+            for _ in range(int(rng.integers(1, 5))):
+                base = seen[int(rng.integers(0, len(seen)))]
+                cut = int(rng.integers(0, len(base) + 1))
+                extra = rng.integers(0, 4, int(rng.integers(0 if cut else 1, 9))).astype(np.int32)
+                prompt = np.concatenate([base[:cut], extra]).astype(np.int32)
+                if len(prompt) == 0:
+                    continue
+                mnew = int(rng.integers(0, 4))
+                gen = rng.integers(0, 4, mnew).astype(np.int32)
+                pending.append(R(rid, np.concatenate([prompt, gen]), mnew))
+                seen.append(np.concatenate([prompt, gen]))
+                rid += 1
+            policy = ra.RC_LPM if rng.random() < 0.8 else ra.RC_FCFS
+            cap = int(rng.integers(1, 5)) if rng.random() < 0.5 else None
+            adm, wait = srv.admit(pending, policy, cap)
+            rec.append(("admit", [(r.rid, r.matched, r.first, tuple(int(x) for x in r.slots)) for r in adm],
+                        sorted(r.rid for r in wait)))
+            srv.commit_prompts(adm)
+            rec.append(("prefill", [(r.rid, tuple(int(x) for x in r.slots[:r.prompt_len])) for r in adm],
+                        cache.dump(), sorted(cache.stats().items())))
+            srv.finish(adm)
+            rec.append(("finish", [(r.rid, tuple(int(x) for x in r.slots)) for r in adm],
+                        cache.dump(), sorted(cache.stats().items())))
+            pending = wait
+        return rec
+
+    a, b = run("oracle"), run("native")
+    assert len(a) == len(b)
+    for i, (x, y) in enumerate(zip(a, b)):
+        assert x == y, f"record {i} ({x[0]}) differs"
+    assert any(r[0] == "admit" and r[2] for r in a)                       # rounds left requests waiting
+    assert any(dict(r[3])["evicted_nodes"] for r in a if r[0] == "finish")  # admission evicted
