@@ -45,7 +45,7 @@ def test_row_buffers_reused_only_when_unreferenced(built):
     nat = Scheduler(ra.RadixCache(4096))
     orc = oracle.OracleServer(oracle.OracleTree(4096))
 
-    # round 1, kept alive: round 2 must not write into its rows
+    # batch A's requests kept alive: batch B's admission must not write into their rows
     a1, b1 = _round(nat, orc, _requests(rng, base, 6, 0))
     addr1 = a1[0].slots.__array_interface__["data"][0]
     for s in (nat, orc):
@@ -59,7 +59,7 @@ def test_row_buffers_reused_only_when_unreferenced(built):
         s.commit_prompts(a2 if s is nat else b2)
         s.finish(a2 if s is nat else b2)
 
-    # round 1's requests dropped: round 3 takes its buffer again, rows still exact
+    # batch A's requests dropped: batch C's admission takes A's buffer again, rows still exact
     del a1, b1, kept
     gc.collect()
     a3, b3 = _round(nat, orc, _requests(rng, base, 6, 200))
@@ -76,7 +76,7 @@ def test_row_buffer_pool_is_bounded(built):
     base = rng.integers(0, 1000, 16).astype(np.int32)
     nat = Scheduler(ra.RadixCache(1 << 14))
     held = []
-    for k in range(Scheduler.ROW_BUFFERS + 3):   # every round kept alive
+    for k in range(Scheduler.ROW_BUFFERS + 3):   # every batch's requests kept alive
         a, _ = nat.admit(_requests(rng, base, 4, 10 * k), ra.RC_LPM)
         nat.commit_prompts(a)
         nat.finish(a)
